@@ -1,0 +1,474 @@
+"""Benchmark of the ragged BF16 grouped GEMM on GB300: one step = forward +
+data gradient + weight gradient over one batch of synthetic inputs.
+
+Default workload: MoE gate_up, E=8 experts, M=131072 routed rows split evenly,
+K=4096 hidden, N=3072, BF16 inputs (X~N(0,1), W~N(0,1/K), G~N(0,1)), BF16
+output, deterministic mode.  Operands (2.1 GB per step) are larger than the
+129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--out-dtype bf16|fp32] [--det 0|1]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the FP64 CPU
+oracle on the host cores instead (a bounded sample of the same workload per
+step).  Under torchrun each rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "grouped-GEMM TFLOP/s (fwd/dgrad/wgrad) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="moe_gate_up")
+    ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "fp32"])
+    ap.add_argument("--det", type=int, default=1)
+    ap.add_argument("--passes", default="fwd,dgrad,wgrad")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def get_workload(name):
+    from moe_ragged_grouped_gb300 import workloads as wl
+    if name == "moe_gate_up":
+        return wl.moe_gate_up()
+    if name == "moe_down":
+        return wl.moe_down()
+    if name == "moe_skew":
+        return wl.moe_skewed(False)
+    if name == "moe_skew_t":
+        return wl.moe_skewed(True)
+    if name == "tiny":
+        return wl.tiny()
+    if name.startswith("dense_"):
+        d_in, d_out = (int(v) for v in name[len("dense_"):].split("to"))
+        return wl.dense_projection(d_in, d_out)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_ragged_grouped_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload_name, pass_, out_dtype, det):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    key = f"{workload_name}|{pass_}|{out_dtype}|det{int(det)}"
+    return d.get("per_launch_bytes", {}).get(key)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t_start = self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except Exception:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t_start - 0.15 <= r[0] <= self.t_end + 0.15] or rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+
+def run_ours(args, wk):
+    import torch
+    from moe_ragged_grouped_gb300 import build as gg_build
+    from moe_ragged_grouped_gb300 import cake_gg as gg
+
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        gg_build.build()
+    if dist is not None:
+        dist.barrier()
+    gg.load_library()
+
+    passes = [p for p in args.passes.split(",") if p]
+    od, det = args.out_dtype, args.det
+    X, W, G = wk.make_torch(seed=0, device=dev)
+    offs = torch.from_numpy(wk.offsets).to(dev)
+    M, E, N, K = wk.M, wk.E, wk.N, wk.K
+    tdt = torch.float32 if od == "fp32" else torch.bfloat16
+    Y = torch.empty((M, N), dtype=tdt, device=dev)
+    dX = torch.empty((M, K), dtype=tdt, device=dev)
+    dW = torch.empty((E, N, K), dtype=tdt, device=dev)
+    plans = {p: gg.cake_gg_plan(p, E, M, N, K, od, det) for p in passes}
+    wss = {p: gg.make_workspace(plans[p], dev) for p in passes}
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+
+    def launch(p):
+        if p == "fwd":
+            rc = gg.cake_gg_fwd(plans[p], X, W, Y, offs, od, det, wss[p], stream=s)
+        elif p == "dgrad":
+            rc = gg.cake_gg_dgrad(plans[p], G, W, dX, offs, od, det, wss[p], stream=s)
+        else:
+            rc = gg.cake_gg_wgrad(plans[p], G, X, dW, offs, od, det, wss[p], stream=s)
+        if rc != 0:
+            raise gg.CakeGGError(rc, p)
+
+    for _ in range(args.warmup):
+        for p in passes:
+            launch(p)
+    torch.cuda.synchronize(dev)
+    for p in passes:
+        st = gg.cake_gg_check_status(wss[p], s)
+        if st != 0:
+            raise gg.CakeGGError(st, f"{p} device status")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        for j, p in enumerate(passes):
+            launch(p)
+            evs[i][j + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_end()
+    elapsed_ms = start.elapsed_time(end)
+    per_pass_ms = {p: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                   for j, p in enumerate(passes)}
+    if dist is not None:
+        dist.barrier()
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clocks = sampler.finish() if sampler else None
+
+    flop_step = wk.flops(len(passes))
+    value = flop_step * args.steps * ws / (elapsed_ms * 1e-3) / 1e12
+    ms_per_step = elapsed_ms / args.steps
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if args.e2e_steps > 0:
+        hX = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+        hW = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+        hG = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+        hX.copy_(X)
+        hW.copy_(W)
+        hG.copy_(G)
+        outs = {"fwd": Y, "dgrad": dX, "wgrad": dW}
+        houts = {p: torch.empty(outs[p].shape, dtype=tdt, pin_memory=True) for p in passes}
+        h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hG))
+        d2h = sum(houts[p].numel() * houts[p].element_size() for p in passes)
+
+        def e2e_step():
+            X.copy_(hX, non_blocking=True)
+            W.copy_(hW, non_blocking=True)
+            G.copy_(hG, non_blocking=True)
+            for p in passes:
+                launch(p)
+            for p in passes:
+                houts[p].copy_(outs[p], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b)
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": flop_step * args.e2e_steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms / args.e2e_steps}
+
+    # ---- roofline of the dominant kernel ----
+    peaks = measured_peaks()
+    dom = max(per_pass_ms, key=per_pass_ms.get)
+    achieved = wk.flops(1) / (per_pass_ms[dom] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic_for(wk.name, dom, od, det),
+                "kernel": f"cake_gg_kernel<{dom}>",
+                "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+                "per_pass_ms": {p: round(v, 4) for p, v in per_pass_ms.items()},
+                "per_pass_tflops": {p: round(wk.flops(1) / (v * 1e-3) / 1e12, 1) for p, v in per_pass_ms.items()}}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wk, X, W, G, passes, args.cpu_seconds)
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wk.name, "E": E, "M": M, "N": N, "K": K,
+                       "group_sizes": sizes_desc(wk), "passes": passes, "out_dtype": od,
+                       "deterministic": bool(det), "accumulate": "fp32",
+                       "l2": "no flush: operands per step (%.2f GB) exceed the 129 MB L2" % (
+                           (X.numel() + W.numel() + G.numel()) * 2 / 1e9),
+                       "parallelism": f"replicas x{ws}",
+                       "plans": {p: {k: v for k, v in plans[p].as_dict().items()
+                                     if k in ("tile_n", "stages", "swap_ab", "split_chunk")} for p in passes}},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": len(passes) * args.steps, "clocks": clocks}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def sizes_desc(wk):
+    s = wk.sizes
+    if len(set(s)) == 1:
+        return f"balanced {s[0]} x {len(s)}"
+    return s
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+
+def _sample_plan(wk, passes, rng, n_per_pass):
+    import numpy as np
+    off = wk.offsets
+    M = int(off[-1])
+    sizes = np.diff(off)
+    out = {}
+    for p in passes:
+        n = n_per_pass[p]
+        if p in ("fwd", "dgrad"):
+            rows = rng.integers(0, M, n)
+            cols = rng.integers(0, wk.N if p == "fwd" else wk.K, n)
+            L = np.full(n, wk.K if p == "fwd" else wk.N, np.float64)
+            out[p] = (rows, cols, L)
+        else:
+            nonempty = np.nonzero(sizes)[0]
+            es = nonempty[rng.integers(0, len(nonempty), n)]
+            ns = rng.integers(0, wk.N, n)
+            ks = rng.integers(0, wk.K, n)
+            out[p] = (es, ns, ks, sizes[es].astype(np.float64))
+    return out
+
+
+def _run_oracle_sample(oracle, wk, Xb, Wb, Gb, samp):
+    off = wk.offsets
+    flop = 0.0
+    t0 = time.perf_counter()
+    for p, s in samp.items():
+        if p == "fwd":
+            oracle.fwd_at(Xb, Wb, off, s[0], s[1])
+            flop += 2.0 * s[2].sum()
+        elif p == "dgrad":
+            oracle.dgrad_at(Gb, Wb, off, s[0], s[1])
+            flop += 2.0 * s[2].sum()
+        else:
+            oracle.wgrad_at(Gb, Xb, off, wk.E, s[0], s[1], s[2])
+            flop += 2.0 * s[3].sum()
+    return flop, time.perf_counter() - t0
+
+
+def _calibrate(oracle, wk, Xb, Wb, Gb, passes, seconds):
+    """Sample sizes per pass so that one oracle sample of all passes takes about `seconds`."""
+    import numpy as np
+    rng = np.random.default_rng(1234)
+    n = {}
+    for p in passes:
+        k = 64
+        while True:
+            samp = _sample_plan(wk, [p], rng, {p: k})
+            _, dt = _run_oracle_sample(oracle, wk, Xb, Wb, Gb, samp)
+            if dt >= 0.1 or k >= 1 << 22:
+                break
+            k *= 4
+        per = max(dt / k, 1e-9)
+        n[p] = max(16, int(seconds / len(passes) / per))
+    return n
+
+
+def host_bits(wk, X, W, G):
+    from moe_ragged_grouped_gb300 import workloads as wl
+    return wl.torch_bf16_to_bits(X), wl.torch_bf16_to_bits(W), wl.torch_bf16_to_bits(G)
+
+
+def cpu_baseline(wk, X, W, G, passes, seconds):
+    import numpy as np
+    import oracle
+    Xb, Wb, Gb = host_bits(wk, X, W, G)
+    n = _calibrate(oracle, wk, Xb, Wb, Gb, passes, seconds / 4)
+    n = {p: int(v * 4) for p, v in n.items()}
+    samp = _sample_plan(wk, passes, np.random.default_rng(99), n)
+    flop, dt = _run_oracle_sample(oracle, wk, Xb, Wb, Gb, samp)
+    return {"value": flop / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": ("%s output elements sampled uniformly (each a full FP64 dot product over its "
+                       "reduction length), %.1f s of CPU work" % (
+                           ", ".join(f"{n[p]} {p}" for p in passes), dt)),
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, wk):
+    import numpy as np
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    passes = [p for p in args.passes.split(",") if p]
+    try:
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+    except Exception:
+        dev = "cpu"
+    X, W, G = wk.make_torch(seed=0, device=dev)
+    Xb, Wb, Gb = host_bits(wk, X, W, G)
+    del X, W, G
+    per_step = 1.5
+    n = _calibrate(oracle, wk, Xb, Wb, Gb, passes, per_step)
+    rng = np.random.default_rng(7)
+    for _ in range(args.warmup):
+        _run_oracle_sample(oracle, wk, Xb, Wb, Gb, _sample_plan(wk, passes, rng, n))
+    flop = dt = 0.0
+    for _ in range(args.steps):
+        f, t = _run_oracle_sample(oracle, wk, Xb, Wb, Gb, _sample_plan(wk, passes, rng, n))
+        flop += f
+        dt += t
+    value = flop / dt / 1e12
+    sample = ("per step: %s output elements sampled uniformly (FP64 dot products over the full "
+              "reduction length)" % ", ".join(f"{n[p]} {p}" for p in passes))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wk.name, "E": wk.E, "M": wk.M, "N": wk.N, "K": wk.K,
+                       "group_sizes": sizes_desc(wk), "passes": passes, "out_dtype": args.out_dtype,
+                       "deterministic": bool(args.det)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    wk = get_workload(args.workload)
+    if args.workload != "moe_gate_up" and "wgrad" in args.passes and wk.passes == ("wgrad",):
+        args.passes = "wgrad"
+    if args.impl == "reference":
+        run_reference(args, wk)
+    else:
+        run_ours(args, wk)
+
+
+if __name__ == "__main__":
+    main()

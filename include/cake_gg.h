@@ -1,0 +1,150 @@
+/*
+ * cake_gg.h -- C ABI of the GB300 (sm_103a) ragged BF16 grouped GEMM.
+ *
+ * The operation (flashinfer PR #8258, "perf(cake_moe_grouped_gemm): run the
+ * split k512 wgrad tail whole on the least-loaded clusters", opening summary):
+ * a ragged grouped GEMM for MoE expert training with BF16 inputs and FP32
+ * accumulation, in three passes -- forward Y = X W^T, data gradient dX = G W,
+ * weight gradient dW = G^T X -- with BF16 or FP32 output.  Expert e owns the
+ * rows [offsets[e], offsets[e+1]) of X, G, Y and dX.  The dense projection
+ * family (flashinfer PR #8363, "Summary" and "Definitions") is the E = 1 case.
+ *
+ * Layouts (row-major, last index contiguous, no padding between rows):
+ *   X  [M_max, K] bf16      W  [E, N, K] bf16      G  [M_max, N] bf16
+ *   Y  [M_max, N] out_dtype dX [M_max, K] out_dtype dW [E, N, K] out_dtype
+ *   offsets [E+1] int32, device memory: offsets[0] == 0, non-decreasing,
+ *   offsets[E] <= M_max.  Rows >= offsets[E] of Y and dX are never written;
+ *   the weight gradient ignores them.  An empty expert gets an exact zero dW.
+ *
+ * Deterministic mode (PR #8258: "bitwise reproducible from run to run"): every
+ * output element is computed by a fixed sequence of FP32 operations that
+ * depends only on (pass, E, M_max, N, K, out_dtype) and the offsets -- never on
+ * max_sms, on which CTA runs a tile, or on arrival order.  Split reductions
+ * add FP32 partials in split order and round once.  Non-deterministic mode
+ * (PR #8258: tail partial tiles added "into a shared FP32 sum with atomic
+ * reductions", last CTA per tile found by a "per-tile ticket") may change the
+ * order of the weight gradient's split sums from run to run.  The forward and
+ * data-gradient passes never split and are deterministic in both modes.
+ *
+ * Ownership: the caller owns every buffer (inputs, outputs, offsets,
+ * workspace) and the plan.  The compute calls allocate nothing, free nothing
+ * and never synchronise the host; they enqueue work on `stream` (a
+ * cudaStream_t, NULL = the legacy default stream) and return.  The workspace
+ * must stay allocated and unused by anyone else until the stream has run the
+ * call; calls that share one workspace must be ordered on one stream.
+ *
+ * Errors: host-detected problems return a non-zero cake_gg_status_t and
+ * enqueue nothing.  Problems only the GPU can see (bad offsets, a bounded wait
+ * that expired) are written to the workspace's status word; the kernel then
+ * skips its remaining work and returns (it never traps).  Output contents are
+ * unspecified after any error.  cake_gg_check_status() reads the status word.
+ */
+#ifndef CAKE_GG_H
+#define CAKE_GG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CAKE_GG_ABI_VERSION 1
+
+typedef enum {
+    CAKE_GG_OK = 0,
+    CAKE_GG_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, plan/call mismatch   */
+    CAKE_GG_ERR_ALIGNMENT = 2,    /* a base pointer not 16-byte aligned, or N/K not multiples of 8 */
+    CAKE_GG_ERR_OVERFLOW = 3,     /* a size product overflows 64-bit or a TMA coordinate   */
+    CAKE_GG_ERR_UNSUPPORTED = 4,  /* current device is not sm_103 (GB300), or a dtype is unknown */
+    CAKE_GG_ERR_WORKSPACE = 5,    /* workspace missing or smaller than plan->workspace_bytes */
+    CAKE_GG_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed                      */
+    CAKE_GG_ERR_BAD_OFFSETS = 7,  /* device-detected: offsets not 0-based, decreasing or > M_max */
+    CAKE_GG_ERR_TIMEOUT = 8       /* device-detected: a bounded wait inside the kernel expired */
+} cake_gg_status_t;
+
+typedef enum { CAKE_GG_FWD = 0, CAKE_GG_DGRAD = 1, CAKE_GG_WGRAD = 2 } cake_gg_pass_t;
+typedef enum { CAKE_GG_BF16 = 0, CAKE_GG_FP32 = 1 } cake_gg_dtype_t;
+
+/* Plan: a caller-owned plain struct filled by cake_gg_plan(); nothing to free.
+ * The first block holds the problem as given; the second holds the choices
+ * made for it.  The choices are a pure function of the first block minus
+ * max_sms, so max_sms changes only how many CTAs run, never a result bit. */
+typedef struct cake_gg_plan {
+    int32_t abi_version;     /* CAKE_GG_ABI_VERSION                                 */
+    int32_t pass;            /* cake_gg_pass_t                                      */
+    int32_t E;               /* experts, 1 .. 1024                                  */
+    int32_t N;               /* W rows per expert (output width of the forward)     */
+    int32_t K;               /* W columns (reduction length of the forward)         */
+    int32_t out_dtype;       /* cake_gg_dtype_t                                     */
+    int64_t M_max;           /* rows allocated in X / G / Y / dX (0 .. 2^31 - 1)    */
+    int32_t deterministic;   /* 1 = bitwise reproducible, 0 = split sums by atomics */
+    int32_t max_sms;         /* cap on persistent CTAs; 0 = every SM of the device  */
+    /* chosen by cake_gg_plan() */
+    int32_t tile_m;          /* MMA rows per tile (128)                             */
+    int32_t tile_n;          /* MMA columns per tile (64 .. 256)                    */
+    int32_t tile_k;          /* reduction elements per pipeline stage (64)          */
+    int32_t stages;          /* shared-memory ring depth                            */
+    int32_t cta_group;       /* CTAs per MMA (1)                                    */
+    int32_t swap_ab;         /* weight gradient: 1 = MMA rows run over K (thin N)   */
+    int32_t split_chunk;     /* weight gradient: k-blocks per split, 0 = no split   */
+    int32_t debug_flags;     /* test-only fault injection; 0 in normal use          */
+    uint64_t timeout_ns;     /* limit of every in-kernel wait (default 2 s)         */
+    uint64_t workspace_bytes;/* bytes of workspace the compute call needs           */
+    int32_t reserved[8];
+} cake_gg_plan_t;
+
+/* Debug flag (tests only): CTA 0 arms its first pipeline stage but issues no
+ * copy into it, so the consumer's bounded wait expires and the call reports
+ * CAKE_GG_ERR_TIMEOUT through the status word. */
+#define CAKE_GG_DEBUG_DROP_FIRST_LOAD 1
+
+/* Fill *plan for one pass.  Pure host arithmetic: no CUDA call, no allocation.
+ * Checks E in [1, 1024], N, K >= 1 and multiples of 8 (16-byte rows for the
+ * tensor-memory-access engine), M_max in [0, 2^31 - 1], out_dtype and pass,
+ * and that every byte size fits in 64 bits.  max_sms < 0 is invalid. */
+int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32_t N,
+                 int32_t K, int out_dtype, int deterministic, int32_t max_sms);
+
+/* Forward Y = X W_e^T per expert (PR #8258 opening summary).  X, W, Y,
+ * offsets: device pointers, 16-byte aligned.  out_dtype and deterministic
+ * must equal the plan's.  Writes rows [0, offsets[E]) of Y only. */
+int cake_gg_fwd(const cake_gg_plan_t *plan, const void *X, const void *W, void *Y,
+                const int32_t *offsets, int out_dtype, int deterministic,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Data gradient dX = G W_e per expert.  G [M_max, N], W [E, N, K],
+ * dX [M_max, K].  Writes rows [0, offsets[E]) of dX only. */
+int cake_gg_dgrad(const cake_gg_plan_t *plan, const void *G, const void *W, void *dX,
+                  const int32_t *offsets, int out_dtype, int deterministic,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Weight gradient dW_e = G_e^T X_e per expert, the sum over the expert's rows
+ * (the ragged reduction).  G [M_max, N], X [M_max, K], dW [E, N, K]; every
+ * element of dW is written (zeros for an empty expert). */
+int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
+                  const int32_t *offsets, int out_dtype, int deterministic,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream` and return the status word the last call that used
+ * `workspace` left there (CAKE_GG_OK, _BAD_OFFSETS or _TIMEOUT), or
+ * CAKE_GG_ERR_CUDA if the synchronisation itself failed. */
+int cake_gg_check_status(const void *workspace, void *stream);
+
+/* Static, never-NULL description of a status code. */
+const char *cake_gg_strerror(int code);
+
+/* Host-side replica of the kernel's tile walk, for testing the scheduler on
+ * any machine.  Given host offsets[E+1], writes up to `capacity` tiles, each
+ * as 8 int32 {expert, m_tile, n_tile, split, n_splits, kblock_begin,
+ * kblock_end, ticket}, in the order the persistent CTAs take them, and stores
+ * the total tile count in *count.  Returns CAKE_GG_ERR_BAD_OFFSETS for offsets
+ * the kernel would reject. */
+int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *offsets_host,
+                      int64_t capacity, int32_t *tiles_out, int64_t *count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAKE_GG_H */

@@ -1,0 +1,459 @@
+// cake_gg_capi.cu -- the C ABI of include/cake_gg.h: planning, argument
+// validation, TMA descriptor set-up and kernel launch.  Host code only.
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/cake_gg.h"
+#include "cake_gg_launch.h"
+#include "cake_gg_sched.h"
+
+using namespace cakegg;
+
+namespace {
+
+constexpr int kSplitTargetUnits = 4 * 152;  // weight-gradient work units aimed for when splitting
+constexpr int kMinSplitChunk = 4;           // k-blocks (256 rows) per split at least
+constexpr size_t kSmemLimit = 232448;       // opt-in dynamic shared memory per CTA
+constexpr uint64_t kHeaderBytes = 256;      // workspace: status word and padding
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+bool mul_ok(uint64_t a, uint64_t b, uint64_t *out)
+{
+    if (a != 0 && b > UINT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+bool add_ok(uint64_t a, uint64_t b, uint64_t *out)
+{
+    if (b > UINT64_MAX - a) return false;
+    *out = a + b;
+    return true;
+}
+
+uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+int env_int(const char *name, int dflt)
+{
+    const char *s = std::getenv(name);
+    if (!s || !*s) return dflt;
+    return std::atoi(s);
+}
+
+int tmem_cols_for(int bn)
+{
+    int cols = 32;
+    while (cols < 2 * bn) cols <<= 1;
+    return cols;
+}
+
+// Byte layout of the workspace for a plan: header | tickets | partial tiles.
+struct WsLayout {
+    uint64_t tickets_off, tickets_bytes;
+    uint64_t partials_off, partials_bytes;
+    uint64_t clear_bytes;  // prefix cleared by every call
+    uint64_t total;
+    bool ok;
+};
+
+WsLayout ws_layout(const cake_gg_plan_t &pl)
+{
+    WsLayout w{};
+    w.ok = true;
+    w.tickets_off = kHeaderBytes;
+    w.partials_off = kHeaderBytes;
+    w.clear_bytes = kHeaderBytes;
+    w.total = kHeaderBytes;
+    if (pl.pass != CAKE_GG_WGRAD || pl.split_chunk <= 0) return w;
+    const Geom g = make_geom(kModeWgrad, pl.E, pl.N, pl.K, pl.M_max, pl.tile_n, pl.swap_ab, pl.split_chunk);
+    const uint64_t tpe = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles);
+    uint64_t n_tickets = 0, tile_bytes = 0, tmp = 0;
+    w.ok &= mul_ok(tpe, uint64_t(pl.E), &n_tickets);
+    w.ok &= mul_ok(uint64_t(kTileM) * 4u, uint64_t(pl.tile_n), &tile_bytes);
+    w.ok &= mul_ok(n_tickets, 4, &tmp);
+    w.tickets_bytes = align_up(tmp, 256);
+    w.partials_off = w.tickets_off + w.tickets_bytes;
+    uint64_t tiles = 0;
+    if (pl.deterministic) {
+        // sum over experts of ceil(rows_e / (64 * chunk)) is at most M_max / (64 * chunk) + E
+        const uint64_t splits = uint64_t(pl.M_max) / (uint64_t(kTileK) * uint64_t(pl.split_chunk)) +
+                                uint64_t(pl.E) + 1;
+        w.ok &= mul_ok(tpe, splits, &tiles);
+    } else {
+        tiles = n_tickets;
+    }
+    w.ok &= mul_ok(tiles, tile_bytes, &w.partials_bytes);
+    w.ok &= add_ok(w.partials_off, w.partials_bytes, &w.total);
+    // the deterministic partial slots are fully overwritten before they are read;
+    // the atomic accumulators must start at zero
+    w.clear_bytes = pl.deterministic ? w.partials_off : w.total;
+    return w;
+}
+
+// ---------------------------------------------------------------- device info
+
+struct DevInfo {
+    bool init;
+    int cc_major, cc_minor, sms;
+};
+
+DevInfo g_dev[64];
+
+int device_info(DevInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CAKE_GG_ERR_CUDA;
+    DevInfo &d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return CAKE_GG_ERR_CUDA;
+        d.init = true;
+    }
+    *out = d;
+    if (d.cc_major != 10 || d.cc_minor != 3) return CAKE_GG_ERR_UNSUPPORTED;
+    return CAKE_GG_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder()
+{
+    if (g_encode) return CAKE_GG_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return CAKE_GG_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return CAKE_GG_OK;
+}
+
+// BF16 tensor of rank 2 ({inner, outer}) or 3 ({inner, mid, outer}), dense,
+// 128-byte swizzled boxes, zero fill outside the tensor.
+int encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, uint32_t box0,
+               uint32_t box1)
+{
+    cuuint64_t gdim[3] = {dims[0], dims[1], rank > 2 ? dims[2] : 1};
+    cuuint64_t gstride[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
+                          gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by the three compute calls.
+int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *b, void *out,
+               const int32_t *offsets, int out_dtype, int deterministic, void *ws, size_t ws_bytes)
+{
+    if (!plan || plan->abi_version != CAKE_GG_ABI_VERSION || plan->pass != pass) return CAKE_GG_ERR_INVALID_ARG;
+    if (plan->out_dtype != out_dtype || (plan->deterministic != 0) != (deterministic != 0))
+        return CAKE_GG_ERR_INVALID_ARG;
+    if (plan->E < 1 || plan->E > kMaxE || plan->N < 1 || plan->K < 1 || plan->M_max < 0 ||
+        plan->M_max > INT32_MAX)
+        return CAKE_GG_ERR_INVALID_ARG;
+    if (plan->tile_m != kTileM || plan->tile_k != kTileK || plan->cta_group != 1 ||
+        plan->tile_n < 64 || plan->tile_n > 256 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
+        plan->stages > kMaxStages || plan->split_chunk < 0 ||
+        smem_bytes_for(plan->tile_n, plan->stages) > kSmemLimit)
+        return CAKE_GG_ERR_INVALID_ARG;
+    if (plan->N % 8 != 0 || plan->K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
+    // operands with M_max rows may be null when there are no rows at all
+    const bool no_rows = plan->M_max == 0;
+    const bool a_may_be_null = no_rows;                              // X, G
+    const bool b_may_be_null = no_rows && pass == CAKE_GG_WGRAD;     // X (W is never empty)
+    const bool out_may_be_null = no_rows && pass != CAKE_GG_WGRAD;   // Y, dX (dW is never empty)
+    if ((!a && !a_may_be_null) || (!b && !b_may_be_null) || (!out && !out_may_be_null) || !offsets || !ws)
+        return CAKE_GG_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(out) || !aligned16(ws)) return CAKE_GG_ERR_ALIGNMENT;
+    if ((reinterpret_cast<uintptr_t>(offsets) & 3u) != 0) return CAKE_GG_ERR_ALIGNMENT;
+    const WsLayout w = ws_layout(*plan);
+    if (!w.ok) return CAKE_GG_ERR_OVERFLOW;
+    if (ws_bytes < w.total) return CAKE_GG_ERR_WORKSPACE;
+    return CAKE_GG_OK;
+}
+
+int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, void *out,
+        const int32_t *offsets, void *ws, cudaStream_t stream)
+{
+    DevInfo dev;
+    int rc = device_info(&dev);
+    if (rc != CAKE_GG_OK) return rc;
+    if ((rc = get_encoder()) != CAKE_GG_OK) return rc;
+
+    const int E = plan->E, N = plan->N, K = plan->K, bn = plan->tile_n;
+    const uint64_t M = uint64_t(plan->M_max);
+    const bool out_f32 = plan->out_dtype == CAKE_GG_FP32;
+    const WsLayout w = ws_layout(*plan);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+
+    if (cudaMemsetAsync(ws, 0, w.clear_bytes, stream) != cudaSuccess) return CAKE_GG_ERR_CUDA;
+    if (M == 0) {
+        // no rows at all: forward / data gradient write nothing, dW is zero
+        if (mode == kModeWgrad) {
+            const size_t bytes = size_t(E) * N * K * (out_f32 ? 4 : 2);
+            if (cudaMemsetAsync(out, 0, bytes, stream) != cudaSuccess) return CAKE_GG_ERR_CUDA;
+        }
+        return CAKE_GG_OK;
+    }
+
+    CUtensorMap ma, mb;
+    if (mode == kModeFwd) {
+        const uint64_t dx[2] = {uint64_t(K), M};
+        const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
+        if ((rc = encode_map(&ma, opA, 2, dx, 64, kTileM)) != CAKE_GG_OK) return rc;
+        if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(bn))) != CAKE_GG_OK) return rc;
+    } else if (mode == kModeDgrad) {
+        const uint64_t dg[2] = {uint64_t(N), M};
+        const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
+        if ((rc = encode_map(&ma, opA, 2, dg, 64, kTileM)) != CAKE_GG_OK) return rc;
+        if ((rc = encode_map(&mb, opB, 3, dw, 64, 64)) != CAKE_GG_OK) return rc;
+    } else {
+        // opA = G [M, N], opB = X [M, K]; swapped operands put X on the MMA rows
+        const uint64_t dg[2] = {uint64_t(N), M};
+        const uint64_t dx[2] = {uint64_t(K), M};
+        const void *pa = plan->swap_ab ? opB : opA;
+        const void *pb = plan->swap_ab ? opA : opB;
+        if ((rc = encode_map(&ma, pa, 2, plan->swap_ab ? dx : dg, 64, 64)) != CAKE_GG_OK) return rc;
+        if ((rc = encode_map(&mb, pb, 2, plan->swap_ab ? dg : dx, 64, 64)) != CAKE_GG_OK) return rc;
+    }
+
+    KParams p{};
+    p.offsets = offsets;
+    p.out = out;
+    p.status = reinterpret_cast<int32_t *>(wsb);
+    p.tickets = reinterpret_cast<int32_t *>(wsb + w.tickets_off);
+    p.partials = reinterpret_cast<float *>(wsb + w.partials_off);
+    p.M_max = plan->M_max;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.bn = bn;
+    p.stages = plan->stages;
+    p.kchunk = mode == kModeWgrad ? plan->split_chunk : 0;
+    p.det = plan->deterministic ? 1 : 0;
+    p.tmem_cols = tmem_cols_for(bn);
+    p.debug_flags = plan->debug_flags;
+    p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
+
+    // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
+    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk);
+    uint64_t tile_bound;
+    if (mode == kModeWgrad) {
+        uint64_t splits = uint64_t(E);
+        if (p.kchunk > 0) splits = M / (uint64_t(kTileK) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
+        tile_bound = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles) * splits;
+    } else {
+        tile_bound = (M / kTileM + uint64_t(E) + 1) * uint64_t(g.n_tiles);
+    }
+    int grid = dev.sms;
+    if (plan->max_sms > 0 && plan->max_sms < grid) grid = plan->max_sms;
+    if (tile_bound < uint64_t(grid)) grid = int(tile_bound);
+    if (grid < 1) grid = 1;
+
+    const size_t smem = smem_bytes_for(bn, plan->stages);
+    cudaError_t err;
+    if (mode == kModeFwd) err = launch_fwd(out_f32, ma, mb, p, grid, smem, stream);
+    else if (mode == kModeDgrad) err = launch_dgrad(out_f32, ma, mb, p, grid, smem, stream);
+    else err = launch_wgrad(out_f32, plan->swap_ab != 0, ma, mb, p, grid, smem, stream);
+    return err == cudaSuccess ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *cake_gg_strerror(int code)
+{
+    switch (code) {
+    case CAKE_GG_OK: return "success";
+    case CAKE_GG_ERR_INVALID_ARG: return "invalid argument (null pointer, size out of range or plan/call mismatch)";
+    case CAKE_GG_ERR_ALIGNMENT: return "misaligned pointer, or N/K not a multiple of 8";
+    case CAKE_GG_ERR_OVERFLOW: return "size arithmetic overflows";
+    case CAKE_GG_ERR_UNSUPPORTED: return "unsupported device (needs sm_103 / GB300) or dtype";
+    case CAKE_GG_ERR_WORKSPACE: return "workspace missing or too small";
+    case CAKE_GG_ERR_CUDA: return "CUDA call failed";
+    case CAKE_GG_ERR_BAD_OFFSETS: return "device found invalid group offsets";
+    case CAKE_GG_ERR_TIMEOUT: return "a bounded wait inside the kernel expired";
+    default: return "unknown status";
+    }
+}
+
+int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32_t N, int32_t K,
+                 int out_dtype, int deterministic, int32_t max_sms)
+{
+    if (!plan) return CAKE_GG_ERR_INVALID_ARG;
+    std::memset(plan, 0, sizeof(*plan));
+    if (pass < CAKE_GG_FWD || pass > CAKE_GG_WGRAD) return CAKE_GG_ERR_INVALID_ARG;
+    if (out_dtype != CAKE_GG_BF16 && out_dtype != CAKE_GG_FP32) return CAKE_GG_ERR_UNSUPPORTED;
+    if (E < 1 || E > kMaxE || N < 1 || K < 1 || M_max < 0 || M_max > INT32_MAX || max_sms < 0)
+        return CAKE_GG_ERR_INVALID_ARG;
+    if (N % 8 != 0 || K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
+    // every tensor's byte size must fit in 64 bits (and W / dW element counts in int64)
+    uint64_t t0, t1;
+    if (!mul_ok(uint64_t(M_max), uint64_t(N) + uint64_t(K), &t0) || !mul_ok(t0, 4, &t0) ||
+        !mul_ok(uint64_t(E), uint64_t(N), &t1) || !mul_ok(t1, uint64_t(K), &t1) || !mul_ok(t1, 4, &t1) ||
+        t1 > uint64_t(INT64_MAX))
+        return CAKE_GG_ERR_OVERFLOW;
+
+    plan->abi_version = CAKE_GG_ABI_VERSION;
+    plan->pass = pass;
+    plan->E = E;
+    plan->N = N;
+    plan->K = K;
+    plan->M_max = M_max;
+    plan->out_dtype = out_dtype;
+    plan->deterministic = deterministic ? 1 : 0;
+    plan->max_sms = max_sms;
+    plan->tile_m = kTileM;
+    plan->tile_k = kTileK;
+    plan->cta_group = 1;
+    plan->timeout_ns = kDefaultTimeoutNs;
+
+    auto pick_bn = [](int32_t width) {
+        if (width >= 256) return 256;
+        return ((width + 63) / 64) * 64;
+    };
+    int32_t bn;
+    if (pass == CAKE_GG_FWD) bn = pick_bn(N);
+    else if (pass == CAKE_GG_DGRAD) bn = pick_bn(K);
+    else {
+        plan->swap_ab = (N <= 64 && K > N) ? 1 : 0;
+        bn = pick_bn(plan->swap_ab ? N : K);
+    }
+    const int env_bn = env_int("CAKE_GG_TILE_N", 0);
+    if (env_bn >= 64 && env_bn <= 256 && env_bn % 64 == 0) bn = env_bn;
+    plan->tile_n = bn;
+
+    int stages = kMaxStages;
+    while (stages > 2 && smem_bytes_for(bn, stages) > kSmemLimit) --stages;
+    const int env_st = env_int("CAKE_GG_STAGES", 0);
+    if (env_st >= 2 && env_st <= stages) stages = env_st;
+    plan->stages = stages;
+
+    if (pass == CAKE_GG_WGRAD) {
+        const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
+        const int64_t tpe = int64_t(g.m_tiles_w) * g.n_tiles;
+        if (tpe * E > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
+        int32_t chunk = 0;
+        if (tpe * E < kSplitTargetUnits / 2) {
+            const int64_t total_kb = (M_max + kTileK - 1) / kTileK + E;
+            int64_t c = (tpe * total_kb + kSplitTargetUnits - 1) / kSplitTargetUnits;
+            if (c < kMinSplitChunk) c = kMinSplitChunk;
+            chunk = c > INT32_MAX ? INT32_MAX : int32_t(c);
+        }
+        const char *es = std::getenv("CAKE_GG_SPLIT_CHUNK");
+        if (es && *es) {
+            const int v = std::atoi(es);
+            if (v >= 0) chunk = v;
+        }
+        plan->split_chunk = chunk;
+    }
+    const WsLayout w = ws_layout(*plan);
+    if (!w.ok) return CAKE_GG_ERR_OVERFLOW;
+    plan->workspace_bytes = w.total;
+    return CAKE_GG_OK;
+}
+
+int cake_gg_fwd(const cake_gg_plan_t *plan, const void *X, const void *W, void *Y,
+                const int32_t *offsets, int out_dtype, int deterministic, void *workspace,
+                size_t workspace_bytes, void *stream)
+{
+    int rc = check_call(plan, CAKE_GG_FWD, X, W, Y, offsets, out_dtype, deterministic, workspace,
+                        workspace_bytes);
+    if (rc != CAKE_GG_OK) return rc;
+    return run(plan, kModeFwd, X, W, Y, offsets, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int cake_gg_dgrad(const cake_gg_plan_t *plan, const void *G, const void *W, void *dX,
+                  const int32_t *offsets, int out_dtype, int deterministic, void *workspace,
+                  size_t workspace_bytes, void *stream)
+{
+    int rc = check_call(plan, CAKE_GG_DGRAD, G, W, dX, offsets, out_dtype, deterministic, workspace,
+                        workspace_bytes);
+    if (rc != CAKE_GG_OK) return rc;
+    return run(plan, kModeDgrad, G, W, dX, offsets, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
+                  const int32_t *offsets, int out_dtype, int deterministic, void *workspace,
+                  size_t workspace_bytes, void *stream)
+{
+    int rc = check_call(plan, CAKE_GG_WGRAD, G, X, dW, offsets, out_dtype, deterministic, workspace,
+                        workspace_bytes);
+    if (rc != CAKE_GG_OK) return rc;
+    return run(plan, kModeWgrad, G, X, dW, offsets, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int cake_gg_check_status(const void *workspace, void *stream)
+{
+    if (!workspace) return CAKE_GG_ERR_INVALID_ARG;
+    int32_t st = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&st, workspace, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return CAKE_GG_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CAKE_GG_ERR_CUDA;
+    return st;
+}
+
+int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t capacity,
+                      int32_t *tiles_out, int64_t *count)
+{
+    if (!plan || !off || !count || capacity < 0 || (capacity > 0 && !tiles_out))
+        return CAKE_GG_ERR_INVALID_ARG;
+    const int E = plan->E;
+    if (E < 1 || E > kMaxE) return CAKE_GG_ERR_INVALID_ARG;
+    if (off[0] != 0 || int64_t(off[E]) > plan->M_max) return CAKE_GG_ERR_BAD_OFFSETS;
+    for (int e = 0; e < E; ++e)
+        if (off[e + 1] < off[e]) return CAKE_GG_ERR_BAD_OFFSETS;
+    const int mode = plan->pass == CAKE_GG_FWD ? kModeFwd : plan->pass == CAKE_GG_DGRAD ? kModeDgrad : kModeWgrad;
+    const Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
+                             mode == kModeWgrad ? plan->split_chunk : 0);
+    std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
+    for (int e = 0; e < E; ++e) {
+        cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
+        cost[e] = expert_cost(g, off[e + 1] - off[e]);
+        order[e] = e;
+    }
+    if (walk_is_sorted(g))
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+    pref[0] = 0;
+    spref[0] = 0;
+    for (int i = 0; i < E; ++i) {
+        pref[i + 1] = pref[i] + cnt[order[i]];
+        spref[i + 1] = spref[i] + expert_splits(g, off[i + 1] - off[i]);
+    }
+    const int64_t total = pref[E];
+    *count = total;
+    for (int64_t t = 0; t < total && t < capacity; ++t) {
+        const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data());
+        int32_t *o = tiles_out + t * 8;
+        o[0] = ti.e;
+        o[1] = ti.mt;
+        o[2] = ti.nt;
+        o[3] = ti.s;
+        o[4] = ti.S;
+        o[5] = ti.kb0;
+        o[6] = ti.kb1;
+        o[7] = ti.ticket;
+    }
+    return CAKE_GG_OK;
+}
+
+}  // extern "C"

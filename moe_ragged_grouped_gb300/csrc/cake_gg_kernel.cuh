@@ -1,0 +1,583 @@
+// cake_gg_kernel.cuh -- persistent, warp-specialised tcgen05 grouped GEMM for sm_103a.
+//
+// One kernel template serves the three passes of the ragged grouped GEMM
+// (flashinfer PR #8258, opening summary: Y = X W^T, dX = G W, dW = G^T X,
+// FP32 accumulation, BF16 or FP32 output).  Each CTA owns one SM:
+//
+//   warp 0      TMA producer: 2-D / 3-D tensor copies into a ring of
+//               `stages` shared-memory stages (full / empty mbarriers)
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma.kind::f16, 128 x tile_n
+//               x 16 per instruction, FP32 accumulators in two TMEM buffers so
+//               the epilogue of one tile overlaps the main loop of the next
+//   warps 2..5  epilogue: tcgen05.ld -> registers -> BF16 (round to nearest
+//               even, once) or FP32 -> global, masked at expert and tensor
+//               edges; the weight gradient's split tiles finish through a
+//               per-tile ticket (PR #8258: "the last CTA to arrive on a tile ...
+//               loads the sum ... and writes the output tile"), summing the
+//               FP32 partials in split order in deterministic mode or through
+//               FP32 atomic adds otherwise.
+//
+// Operands are staged with a 128-byte swizzle.  K-major tiles (rows of 64
+// reduction elements) come from one box of {64, rows}; MN-major tiles come
+// from boxes of {64 MN, 64 reduction rows}, 8 KB each, placed 8 KB apart.
+//
+// Every wait is bounded (timeout_ns, global timer).  On expiry the CTA records
+// CAKE_GG_ERR_TIMEOUT in the status word, stops issuing work, waits (bounded)
+// for its own copies and MMAs in flight, frees its TMEM and returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "cake_gg_ptx.cuh"
+#include "cake_gg_sched.h"
+
+namespace cakegg {
+
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kStatusBadOffsets = 7;
+constexpr int kStatusTimeout = 8;
+constexpr uint32_t kABytes = kTileM * kTileK * 2;  // 16 KB: A tile of one stage
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;        // one 64 x 64 MN-major box
+
+struct KParams {
+    const int32_t *offsets;
+    void *out;
+    int32_t *status;
+    int32_t *tickets;
+    float *partials;
+    int64_t M_max;
+    int32_t E, N, K;
+    int32_t bn;
+    int32_t stages;
+    int32_t kchunk;
+    int32_t det;
+    int32_t tmem_cols;
+    int32_t debug_flags;
+    uint64_t timeout_ns;
+};
+
+// Control block after the operand ring.
+struct __align__(16) Ctrl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort_flag;
+    int32_t bad;
+    int32_t last_flag;
+    int32_t off[kMaxE + 1];
+    int32_t order[kMaxE];
+    int32_t pref[kMaxE + 1];
+    int32_t spref[kMaxE + 1];
+};
+
+__host__ __device__ constexpr uint32_t stage_bytes_for(int bn) { return kABytes + uint32_t(bn) * 128u; }
+
+__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages)
+{
+    return 1024 + size_t(stages) * stage_bytes_for(bn) + sizeof(Ctrl);
+}
+
+// Bounded wait on one mbarrier phase, by every lane of the calling warp;
+// returns a warp-uniform verdict (false: timed out or another role aborted).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctrl *c,
+                                          const KParams &p)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait(bar, parity);
+            if (ok) break;
+            if (*reinterpret_cast<volatile int32_t *>(&c->abort_flag)) break;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                *reinterpret_cast<volatile int32_t *>(&c->abort_flag) = 1;
+                atomicCAS(p.status, 0, kStatusTimeout);
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Same, for a single thread.
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, Ctrl *c,
+                                            const KParams &p, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int32_t *>(&c->abort_flag)) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *reinterpret_cast<volatile int32_t *>(&c->abort_flag) = 1;
+            atomicCAS(p.status, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Wait for a phase regardless of the abort flag (used to drain copies / MMAs
+// already in flight before the CTA releases its memory).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return;
+    }
+}
+
+// ---------------------------------------------------------------- epilogue stores
+
+// 32 consecutive columns of one output row (non-transposed), masked at 8-column
+// granularity (the row length is a multiple of 8).
+template <bool OUT_F32>
+__device__ __forceinline__ void store_row32(void *out, int64_t elem_off, int32_t cols_left,
+                                            const float (&v)[32])
+{
+    if (OUT_F32) {
+        float *dst = static_cast<float *>(out) + elem_off;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (g * 8 < cols_left) {
+                float4 *d4 = reinterpret_cast<float4 *>(dst + g * 8);
+                d4[0] = make_float4(v[g * 8 + 0], v[g * 8 + 1], v[g * 8 + 2], v[g * 8 + 3]);
+                d4[1] = make_float4(v[g * 8 + 4], v[g * 8 + 5], v[g * 8 + 6], v[g * 8 + 7]);
+            }
+        }
+    } else {
+        uint16_t *dst = static_cast<uint16_t *>(out) + elem_off;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (g * 8 < cols_left) {
+                uint4 q;
+                q.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
+                q.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
+                q.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
+                q.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
+                *reinterpret_cast<uint4 *>(dst + g * 8) = q;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x)
+{
+    return static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu);
+}
+
+template <bool OUT_F32>
+__device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
+{
+    if (OUT_F32) static_cast<float *>(out)[idx] = v;
+    else static_cast<uint16_t *>(out)[idx] = f32_to_bf16_rn(v);
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int MODE, bool SWAP, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    cake_gg_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const KParams p)
+{
+    constexpr bool A_MN = (MODE == kModeWgrad);
+    constexpr bool B_MN = (MODE != kModeFwd);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *ring = smem_raw + (ring_u32 - raw_u32);
+    const uint32_t stage_bytes = stage_bytes_for(p.bn);
+    Ctrl *c = reinterpret_cast<Ctrl *>(ring + size_t(p.stages) * stage_bytes);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int E = p.E;
+    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk);
+
+    // ---- setup: offsets, validation, walk tables (temporaries in the ring) ----
+    int32_t *t_cnt = reinterpret_cast<int32_t *>(ring);
+    int32_t *t_cost = t_cnt + kMaxE;
+    if (tid == 0) {
+        c->abort_flag = 0;
+        c->bad = 0;
+    }
+    for (int i = tid; i <= E; i += kThreads) c->off[i] = p.offsets[i];
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+        const int32_t a = c->off[e], b = c->off[e + 1];
+        if ((e == 0 && a != 0) || b < a || (e == E - 1 && int64_t(b) > p.M_max)) c->bad = 1;
+        const int32_t rows = b - a;
+        t_cnt[e] = expert_tiles(g, rows < 0 ? 0 : rows);
+        t_cost[e] = expert_cost(g, rows < 0 ? 0 : rows);
+    }
+    __syncthreads();
+    if (c->bad) {
+        if (tid == 0) atomicCAS(p.status, 0, kStatusBadOffsets);
+        return;
+    }
+    if (walk_is_sorted(g)) {
+        for (int e = tid; e < E; e += kThreads) {
+            const int32_t ce = t_cost[e];
+            int32_t rank = 0;
+            for (int j = 0; j < E; ++j) {
+                const int32_t cj = t_cost[j];
+                rank += (cj > ce) || (cj == ce && j < e);
+            }
+            c->order[rank] = e;
+        }
+    } else {
+        for (int e = tid; e < E; e += kThreads) c->order[e] = e;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive prefix sums by one warp: tiles in processing order, splits by expert id
+        const int per = (E + 31) / 32;
+        const int b0 = lane * per;
+        int32_t sum_t = 0, sum_s = 0;
+        for (int i = b0; i < b0 + per && i < E; ++i) {
+            sum_t += t_cnt[c->order[i]];
+            sum_s += expert_splits(g, c->off[i + 1] - c->off[i]);
+        }
+        int32_t inc_t = sum_t, inc_s = sum_s;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t ot = __shfl_up_sync(0xffffffffu, inc_t, d);
+            const int32_t os = __shfl_up_sync(0xffffffffu, inc_s, d);
+            if (lane >= d) {
+                inc_t += ot;
+                inc_s += os;
+            }
+        }
+        int32_t run_t = inc_t - sum_t, run_s = inc_s - sum_s;
+        for (int i = b0; i < b0 + per && i < E; ++i) {
+            c->pref[i] = run_t;
+            c->spref[i] = run_s;
+            run_t += t_cnt[c->order[i]];
+            run_s += expert_splits(g, c->off[i + 1] - c->off[i]);
+        }
+        if (lane == 31) {
+            c->pref[E] = inc_t;
+            c->spref[E] = inc_s;
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c->tmem_base), uint32_t(p.tmem_cols));
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(smem_u32(&c->full[s]), 1);
+            mbar_init(smem_u32(&c->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&c->tfull[a]), 1);
+            mbar_init(smem_u32(&c->tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&c->drain), 1);
+        fence_barrier_init();
+    }
+    // the set-up temporaries in the ring are overwritten by TMA (async proxy) later
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+
+    const int64_t total = c->pref[E];
+    const uint32_t tmem_base = c->tmem_base;
+    const uint32_t acc_stride = uint32_t(p.tmem_cols) / 2;
+
+    if (warp == 0) {
+        // ======================= TMA producer =======================
+        if (lane == 0) {
+            tma_prefetch_desc(&mapA);
+            tma_prefetch_desc(&mapB);
+            const uint32_t tx = stage_bytes;
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref);
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                    if (!thread_wait(smem_u32(&c->empty[stage]), phase ^ 1u, c, p, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&c->full[stage]);
+                    const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
+                    const uint32_t sb = sa + kABytes;
+                    mbar_arrive_expect_tx(fb, tx);
+                    const bool drop = (p.debug_flags & 1) && blockIdx.x == 0 && issued == 0;
+                    if (!drop) {
+                        if (MODE == kModeWgrad) {
+                            const int32_t r = ti.row0 + kb * kTileK;
+                            tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
+                            tma_load_2d(sa + kBoxBytes, &mapA, fb, ti.mt * kTileM + 64, r);
+                            for (int j = 0; j < p.bn / 64; ++j)
+                                tma_load_2d(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j, r);
+                        } else if (MODE == kModeFwd) {
+                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
+                            tma_load_3d(sb, &mapB, fb, kb * kTileK, ti.nt * p.bn, ti.e);
+                        } else {
+                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
+                            for (int j = 0; j < p.bn / 64; ++j)
+                                tma_load_3d(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j,
+                                            kb * kTileK, ti.e);
+                        }
+                    }
+                    ++issued;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: the most recent issue into each stage must land before exit
+                const int64_t n = issued < p.stages ? issued : p.stages;
+                for (int64_t i = 0; i < n; ++i) {
+                    const int64_t q = issued - 1 - i;
+                    drain_wait(smem_u32(&c->full[q % p.stages]), uint32_t((q / p.stages) & 1),
+                               20000000ull);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ======================= MMA issuer =======================
+        const uint32_t idesc = idesc_bf16_f32(kTileM, uint32_t(p.bn), A_MN, B_MN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        bool any_mma = false;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref);
+            const int acc = it & 1;
+            const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
+            if (!warp_wait(smem_u32(&c->tempty[acc]), acc_phase ^ 1u, c, p)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + uint32_t(acc) * acc_stride;
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
+                const uint32_t sb = sa + kABytes;
+                if (MODE == kModeWgrad) {
+                    // rows of the last k-block past the expert's end belong to the
+                    // next expert (or lie beyond M_max): zero them in both operands
+                    const int32_t valid = ti.row_end - (ti.row0 + kb * kTileK);
+                    if (valid < kTileK) {
+                        const int nbox = 2 + p.bn / 64;
+                        const int nrow = kTileK - valid;
+                        const int chunks = nbox * nrow * 8;
+                        for (int i = lane; i < chunks; i += 32) {
+                            const int box = i / (nrow * 8);
+                            const int rem = i - box * nrow * 8;
+                            const int row = valid + rem / 8;
+                            const int ch = rem % 8;
+                            uint8_t *dst = ring + (sa - ring_u32) + box * kBoxBytes + row * 128 + ch * 16;
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int ks = 0; ks < kTileK / 16; ++ks) {
+                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + ks * 2048, kBoxBytes, 1024)
+                                                 : smem_desc_sw128(sa + ks * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + ks * 2048, kBoxBytes, 1024)
+                                                 : smem_desc_sw128(sb + ks * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb > ti.kb0 || ks > 0) ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&c->empty[stage]));
+                }
+                any_mma = true;
+                __syncwarp();
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(smem_u32(&c->tfull[acc]));
+            __syncwarp();
+        }
+        if (!ok && any_mma) {
+            if (lane == 0) {
+                umma_commit(smem_u32(&c->drain));
+                drain_wait(smem_u32(&c->drain), 0, 20000000ull);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ======================= epilogue (warps 2..5) =======================
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int lrow = q * 32 + lane;    // tile row held by this thread
+        const int etid = tid - 64;         // 0..127
+        int it = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref);
+            const int acc = it & 1;
+            const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
+            bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
+            ok = named_bar_and(1, 128, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+
+            const bool empty_tile = ti.kb1 <= ti.kb0;
+            const bool split = (MODE == kModeWgrad) && ti.S > 1;
+            const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc) * acc_stride;
+
+            // output geometry of this tile
+            int64_t out_base = 0;   // element offset of tile (row 0, col 0)
+            int64_t ld = 0;         // row stride (elements) of the output
+            int32_t rows_valid = 0; // tile rows that exist
+            int32_t cols_valid = 0; // tile columns that exist
+            if (MODE == kModeFwd) {
+                ld = p.N;
+                out_base = int64_t(ti.row0) * ld + int64_t(ti.nt) * p.bn;
+                rows_valid = ti.row_end - ti.row0;
+                cols_valid = p.N - ti.nt * p.bn;
+            } else if (MODE == kModeDgrad) {
+                ld = p.K;
+                out_base = int64_t(ti.row0) * ld + int64_t(ti.nt) * p.bn;
+                rows_valid = ti.row_end - ti.row0;
+                cols_valid = p.K - ti.nt * p.bn;
+            } else if (!SWAP) {
+                ld = p.K;
+                out_base = int64_t(ti.e) * p.N * p.K + int64_t(ti.mt) * kTileM * ld + int64_t(ti.nt) * p.bn;
+                rows_valid = p.N - ti.mt * kTileM;
+                cols_valid = p.K - ti.nt * p.bn;
+            } else {
+                // C[m = k, n = n] -> dW[e, n, k]: transposed store
+                ld = p.K;
+                out_base = int64_t(ti.e) * p.N * p.K + int64_t(ti.nt) * p.bn * ld + int64_t(ti.mt) * kTileM;
+                rows_valid = p.K - ti.mt * kTileM;
+                cols_valid = p.N - ti.nt * p.bn;
+            }
+            if (cols_valid > p.bn) cols_valid = p.bn;
+            const bool row_ok = lrow < rows_valid;
+
+            float *slot_ptr = nullptr;
+            if (split) {
+                slot_ptr = p.det ? p.partials + ti.slot * int64_t(kTileM) * p.bn
+                                 : p.partials + int64_t(ti.ticket) * kTileM * p.bn;
+            }
+
+            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                float v[32];
+                if (empty_tile) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                } else {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + uint32_t(c0), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                }
+                if (split) {
+                    // partial tile, layout [col/4][row] float4: a warp writes 512 contiguous bytes
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        float *dst = slot_ptr + (int64_t((c0 >> 2) + j4) * kTileM + lrow) * 4;
+                        if (p.det)
+                            *reinterpret_cast<float4 *>(dst) =
+                                make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                        else
+                            red_add_v4_f32(dst, v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                    }
+                } else if (row_ok && c0 < cols_valid) {
+                    if (MODE == kModeWgrad && SWAP) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < cols_valid)
+                                store_scalar<OUT_F32>(p.out, out_base + int64_t(c0 + j) * ld + lrow, v[j]);
+                    } else {
+                        store_row32<OUT_F32>(p.out, out_base + int64_t(lrow) * ld + c0, cols_valid - c0, v);
+                    }
+                }
+            }
+            // accumulator buffer free for the MMA warp
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&c->tempty[acc]));
+
+            if (split) {
+                // ticket: the last split of this output tile to arrive finishes it
+                __syncwarp();
+                named_bar_sync(1, 128);
+                if (etid == 0) {
+                    __threadfence();
+                    const int old = atomic_add_acq_rel_gpu(p.tickets + ti.ticket, 1);
+                    c->last_flag = (old == ti.S - 1);
+                }
+                __syncwarp();
+                named_bar_sync(1, 128);
+                const bool last = c->last_flag != 0;
+                named_bar_sync(1, 128);  // everyone read last_flag before the next tile rewrites it
+                if (last) {
+                    __threadfence();
+                    const float *base0 = p.det ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
+                                               : slot_ptr;
+                    const int nsum = p.det ? ti.S : 1;
+                    for (int c4 = 0; c4 < p.bn / 4; ++c4) {
+                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int s = 0; s < nsum; ++s) {
+                            const float4 b = ld_cg_f4(base0 + int64_t(s) * kTileM * p.bn +
+                                                      (int64_t(c4) * kTileM + lrow) * 4);
+                            if (s == 0) a = b;
+                            else {
+                                a.x += b.x;
+                                a.y += b.y;
+                                a.z += b.z;
+                                a.w += b.w;
+                            }
+                        }
+                        const int col = c4 * 4;
+                        if (row_ok && col < cols_valid) {
+                            const float vv[4] = {a.x, a.y, a.z, a.w};
+                            if (MODE == kModeWgrad && SWAP) {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    store_scalar<OUT_F32>(p.out, out_base + int64_t(col + j) * ld + lrow, vv[j]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    store_scalar<OUT_F32>(p.out, out_base + int64_t(lrow) * ld + col + j, vv[j]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: every role is done; release TMEM ----
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, uint32_t(p.tmem_cols));
+    }
+}
+
+}  // namespace cakegg

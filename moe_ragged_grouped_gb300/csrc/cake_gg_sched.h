@@ -1,0 +1,179 @@
+// cake_gg_sched.h -- ragged tile walk of the persistent grouped-GEMM kernel.
+//
+// Shared by the kernel (device) and by cake_gg_tile_walk (host) so that the
+// host replica used in tests is the same code the GPU runs.
+//
+// Tiles.  Every pass computes C[m, n] = sum_k A[m, k] B[n, k] on 128 x tile_n
+// output tiles.
+//  * forward / data gradient: m runs over an expert's rows (ragged), n over
+//    the output columns (N resp. K); the reduction (K resp. N) is dense.
+//  * weight gradient: m runs over N (or over K when swap_ab), n over the
+//    other one; the reduction runs over the expert's rows (ragged).  A long
+//    reduction may be split into chunks of `split_chunk` 64-row k-blocks; the
+//    number of splits of expert e, S_e, depends only on its row count.
+//
+// Order.  Experts are walked in a processing order and, inside an expert, in
+// m-tile-major order (n fastest, then split).  The weight gradient walks its
+// experts heaviest-first (most k-blocks per split first, ties by index) when
+// E <= kSortMaxE, so the longest tiles start first ("unsorted" group orders
+// in flashinfer PR #8258's row classes do not change the tail).  CTAs take
+// tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...  Which CTA takes a tile
+// never changes what the tile computes.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define CAKE_HD __host__ __device__ __forceinline__
+#else
+#define CAKE_HD inline
+#endif
+
+namespace cakegg {
+
+constexpr int kModeFwd = 0;
+constexpr int kModeDgrad = 1;
+constexpr int kModeWgrad = 2;
+
+constexpr int kTileM = 128;     // MMA rows (TMEM lanes)
+constexpr int kTileK = 64;      // reduction elements per stage (one 128-byte swizzle row)
+constexpr int kMaxE = 1024;     // experts supported by the on-chip tables
+constexpr int kSortMaxE = 256;  // heaviest-first walk only up to this many experts
+
+struct Geom {
+    int32_t mode;
+    int32_t E;
+    int32_t N;
+    int32_t K;
+    int64_t M_max;
+    int32_t bn;           // tile_n
+    int32_t swap;         // weight gradient: m over K
+    int32_t kchunk;       // weight gradient: k-blocks per split (0 = none)
+    int32_t n_tiles;      // output column tiles
+    int32_t m_tiles_w;    // weight gradient: output row tiles
+    int32_t nkb;          // forward / data gradient: reduction k-blocks
+};
+
+CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
+
+CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
+                       int32_t swap, int32_t kchunk)
+{
+    Geom g;
+    g.mode = mode;
+    g.E = E;
+    g.N = N;
+    g.K = K;
+    g.M_max = M_max;
+    g.bn = bn;
+    g.swap = swap;
+    g.kchunk = kchunk;
+    if (mode == kModeFwd) {
+        g.n_tiles = ceil_div_i(N, bn);
+        g.nkb = ceil_div_i(K, kTileK);
+        g.m_tiles_w = 0;
+    } else if (mode == kModeDgrad) {
+        g.n_tiles = ceil_div_i(K, bn);
+        g.nkb = ceil_div_i(N, kTileK);
+        g.m_tiles_w = 0;
+    } else {
+        const int32_t mdim = swap ? K : N;
+        const int32_t ndim = swap ? N : K;
+        g.m_tiles_w = ceil_div_i(mdim, kTileM);
+        g.n_tiles = ceil_div_i(ndim, bn);
+        g.nkb = 0;
+    }
+    return g;
+}
+
+// Splits of an expert with `rows` rows (weight gradient); 1 when unsplit or empty.
+CAKE_HD int32_t expert_splits(const Geom &g, int32_t rows)
+{
+    if (g.mode != kModeWgrad || g.kchunk <= 0) return 1;
+    const int32_t nkb = ceil_div_i(rows, kTileK);
+    return nkb <= 0 ? 1 : ceil_div_i(nkb, g.kchunk);
+}
+
+// Tiles of one expert.
+CAKE_HD int32_t expert_tiles(const Geom &g, int32_t rows)
+{
+    if (g.mode == kModeWgrad) return g.m_tiles_w * g.n_tiles * expert_splits(g, rows);
+    return ceil_div_i(rows, kTileM) * g.n_tiles;
+}
+
+// Sort key of the heaviest-first walk: k-blocks in one split of the expert.
+CAKE_HD int32_t expert_cost(const Geom &g, int32_t rows)
+{
+    const int32_t nkb = ceil_div_i(rows, kTileK);
+    const int32_t s = expert_splits(g, rows);
+    return ceil_div_i(nkb, s);
+}
+
+CAKE_HD bool walk_is_sorted(const Geom &g) { return g.mode == kModeWgrad && g.E <= kSortMaxE; }
+
+// One unit of work.
+struct Tile {
+    int32_t e;        // expert
+    int32_t mt;       // output row tile
+    int32_t nt;       // output column tile
+    int32_t s;        // split index
+    int32_t S;        // splits of this output tile
+    int32_t kb0;      // first k-block (64 reduction elements each)
+    int32_t kb1;      // one past the last k-block
+    int32_t row0;     // fwd/dgrad: first row of the tile; wgrad: first row of the expert
+    int32_t row_end;  // one past the expert's last row
+    int32_t ticket;   // wgrad: output tile index e * (m_tiles_w * n_tiles) + mt * n_tiles + nt
+    int64_t slot;     // wgrad split: partial slot of this split
+};
+
+// Tables: off[E+1] offsets; order[E] processing position -> expert;
+// pref[E+1] tile prefix in processing order; spref[E+1] split prefix by
+// expert id (weight gradient).
+CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int32_t *order,
+                         const int32_t *pref, const int32_t *spref)
+{
+    // last position p with pref[p] <= t (positions of empty experts have
+    // pref[p] == pref[p+1] and are never selected since t < pref[E])
+    int32_t lo = 0, hi = g.E - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (static_cast<int64_t>(pref[mid]) <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile ti;
+    const int32_t e = order[lo];
+    const int32_t local = static_cast<int32_t>(t - pref[lo]);
+    const int32_t r0 = off[e];
+    const int32_t r1 = off[e + 1];
+    ti.e = e;
+    ti.row_end = r1;
+    if (g.mode == kModeWgrad) {
+        const int32_t S = expert_splits(g, r1 - r0);
+        const int32_t nkb_e = ceil_div_i(r1 - r0, kTileK);
+        const int32_t s = local % S;
+        const int32_t rest = local / S;
+        ti.nt = rest % g.n_tiles;
+        ti.mt = rest / g.n_tiles;
+        ti.s = s;
+        ti.S = S;
+        const int32_t chunk = S > 1 ? g.kchunk : nkb_e;
+        ti.kb0 = s * chunk;
+        ti.kb1 = (s + 1) * chunk < nkb_e ? (s + 1) * chunk : nkb_e;
+        ti.row0 = r0;
+        ti.ticket = (e * g.m_tiles_w + ti.mt) * g.n_tiles + ti.nt;
+        ti.slot = (static_cast<int64_t>(spref[e]) * g.m_tiles_w * g.n_tiles) +
+                  static_cast<int64_t>(ti.mt * g.n_tiles + ti.nt) * S + s;
+    } else {
+        ti.mt = local / g.n_tiles;
+        ti.nt = local % g.n_tiles;
+        ti.s = 0;
+        ti.S = 1;
+        ti.kb0 = 0;
+        ti.kb1 = g.nkb;
+        ti.row0 = r0 + ti.mt * kTileM;
+        ti.ticket = 0;
+        ti.slot = 0;
+    }
+    return ti;
+}
+
+}  // namespace cakegg

@@ -1,0 +1,195 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+* the library loads and exports every entry point include/cake_gg.h declares;
+* cake_gg_plan validates its arguments and never depends on max_sms;
+* the kernel's tile walk (host replica, same code as the device) covers every
+  output element exactly once, partitions each expert's reduction into
+  contiguous splits, and walks the weight gradient heaviest-first.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from moe_ragged_grouped_gb300 import build as gg_build
+from moe_ragged_grouped_gb300 import cake_gg as gg
+from moe_ragged_grouped_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    gg_build.build()
+    gg.load_library()
+
+
+def declared_entry_points():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(cake_gg_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_entry_points()
+    assert "cake_gg_plan" in names and "cake_gg_wgrad" in names
+    lib = ctypes.CDLL(gg.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(gg.EXPORTED) <= set(names)
+
+
+def test_plan_struct_layout_matches_header():
+    # 6 int32, int64, 10 int32, 2 uint64, 8 int32 reserved
+    assert ctypes.sizeof(gg.CakeGGPlan) == 120
+    assert gg.CakeGGPlan.M_max.offset == 24
+    assert gg.CakeGGPlan.timeout_ns.offset == 72
+    assert gg.CakeGGPlan.workspace_bytes.offset == 80
+
+
+def test_strerror_never_null():
+    for code in range(-1, 12):
+        assert isinstance(gg.cake_gg_strerror(code), str)
+    assert "workspace" in gg.cake_gg_strerror(gg.CAKE_GG_ERR_WORKSPACE)
+
+
+@pytest.mark.parametrize("args,code", [
+    (("fwd", 0, 128, 64, 64, "bf16", 1), gg.CAKE_GG_ERR_INVALID_ARG),        # E = 0
+    (("fwd", 1025, 128, 64, 64, "bf16", 1), gg.CAKE_GG_ERR_INVALID_ARG),     # E too large
+    (("fwd", 2, 128, 60, 64, "bf16", 1), gg.CAKE_GG_ERR_ALIGNMENT),          # N % 8
+    (("dgrad", 2, 128, 64, 12, "bf16", 1), gg.CAKE_GG_ERR_ALIGNMENT),        # K % 8
+    (("wgrad", 2, -1, 64, 64, "fp32", 1), gg.CAKE_GG_ERR_INVALID_ARG),       # M < 0
+    (("wgrad", 2, 2 ** 31, 64, 64, "fp32", 1), gg.CAKE_GG_ERR_INVALID_ARG),  # M too large
+    ((5, 2, 128, 64, 64, "bf16", 1), gg.CAKE_GG_ERR_INVALID_ARG),            # bad pass
+    (("fwd", 2, 128, 64, 64, 7, 1), gg.CAKE_GG_ERR_UNSUPPORTED),             # bad dtype
+    (("wgrad", 1024, 2 ** 31 - 1, 2 ** 30, 2 ** 30, "fp32", 1), gg.CAKE_GG_ERR_OVERFLOW),
+])
+def test_plan_rejects_bad_arguments(args, code):
+    with pytest.raises(gg.CakeGGError) as ei:
+        gg.cake_gg_plan(*args)
+    assert ei.value.code == code
+
+
+def test_plan_rejects_negative_max_sms():
+    with pytest.raises(gg.CakeGGError):
+        gg.cake_gg_plan("fwd", 1, 128, 64, 64, "bf16", 1, -3)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad", "wgrad"])
+@pytest.mark.parametrize("shape", [(8, 131072, 3072, 4096), (1, 16384, 48, 4096), (4, 512, 128, 256),
+                                   (32, 131072, 4096, 1536), (1, 16384, 512, 5120)])
+def test_plan_choices_do_not_depend_on_max_sms(pass_, shape):
+    E, M, N, K = shape
+    plans = [gg.cake_gg_plan(pass_, E, M, N, K, "fp32", 1, s).as_dict() for s in (0, 100, 148, 152)]
+    for p in plans[1:]:
+        for key in ("tile_m", "tile_n", "tile_k", "stages", "swap_ab", "split_chunk", "workspace_bytes"):
+            assert p[key] == plans[0][key]
+    assert plans[0]["tile_n"] % 64 == 0 and 64 <= plans[0]["tile_n"] <= 256
+
+
+def test_thin_weight_gradient_swaps_and_splits():
+    p = gg.cake_gg_plan("wgrad", 1, 16384, 48, 4096, "fp32", 1)
+    assert p.swap_ab == 1 and p.tile_n == 64 and p.split_chunk > 0
+    q = gg.cake_gg_plan("wgrad", 8, 131072, 3072, 4096, "bf16", 1)
+    assert q.swap_ab == 0 and q.split_chunk == 0 and q.workspace_bytes == 256
+
+
+def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
+    if env:
+        os.environ.update(env)
+    try:
+        off = wl.offsets_from_sizes(sizes)
+        E, M = len(sizes), int(off[-1]) + 5
+        plan = gg.cake_gg_plan(pass_, E, M, N, K, "fp32", det)
+    finally:
+        for k in (env or {}):
+            del os.environ[k]
+    tiles = gg.cake_gg_tile_walk(plan, off)
+    bm, bn = plan.tile_m, plan.tile_n
+    if pass_ in ("fwd", "dgrad"):
+        nout = N if pass_ == "fwd" else K
+        cover = np.zeros((M, nout), np.int32)
+        for e, mt, nt, s, S, kb0, kb1, _ in tiles:
+            assert S == 1 and s == 0 and kb0 == 0
+            r0 = off[e] + mt * bm
+            assert r0 < off[e + 1]
+            cover[r0:min(r0 + bm, off[e + 1]), nt * bn:min((nt + 1) * bn, nout)] += 1
+        assert (cover[:off[-1]] == 1).all() and (cover[off[-1]:] == 0).all()
+    else:
+        mdim, ndim = (K, N) if plan.swap_ab else (N, K)
+        cover = np.zeros((len(sizes), mdim, ndim), np.int32)
+        splits = {}
+        for e, mt, nt, s, S, kb0, kb1, ticket in tiles:
+            splits.setdefault((e, mt, nt), []).append((s, S, kb0, kb1, ticket))
+        for (e, mt, nt), lst in splits.items():
+            lst.sort()
+            S = lst[0][1]
+            assert [x[0] for x in lst] == list(range(S))
+            nkb = -(-(off[e + 1] - off[e]) // 64)
+            # contiguous partition of [0, nkb)
+            assert lst[0][2] == 0 and lst[-1][3] == nkb
+            for a, b in zip(lst, lst[1:]):
+                assert a[3] == b[2] and b[2] < b[3]
+            assert len({x[4] for x in lst}) == 1
+            cover[e, mt * bm:min((mt + 1) * bm, mdim), nt * bn:min((nt + 1) * bn, ndim)] += 1
+        assert (cover == 1).all()
+        # heaviest-first over experts (k-blocks per split, ties by expert index)
+        costs = []
+        for e, mt, nt, s, S, kb0, kb1, _ in tiles:
+            if not costs or costs[-1][0] != e:
+                costs.append((e, -(-(-(-(off[e + 1] - off[e]) // 64)) // S)))
+        seq = [c for _, c in costs]
+        assert seq == sorted(seq, reverse=True)
+    return plan, tiles
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad", "wgrad"])
+@pytest.mark.parametrize("sizes", [[128] * 4, [0, 1, 129, 300, 0], [5000], [0, 21381 // 16, 34780 // 16, 79903 // 16],
+                                   [17, 0, 0, 64, 63, 65, 1]])
+def test_tile_walk_covers_each_output_once(pass_, sizes):
+    _check_walk_coverage(pass_, sizes, N=192, K=320)
+
+
+def test_tile_walk_split_partitions():
+    plan, tiles = _check_walk_coverage("wgrad", [0, 3000, 700, 64], N=128, K=256,
+                                       env={"CAKE_GG_SPLIT_CHUNK": "4"})
+    assert plan.split_chunk == 4
+    assert max(t[4] for t in tiles) == -(-(-(-3000 // 64)) // 4)
+
+
+def test_tile_walk_thin_swap():
+    plan, tiles = _check_walk_coverage("wgrad", [16384], N=48, K=4096)
+    assert plan.swap_ab == 1
+    assert len({(t[1], t[2]) for t in tiles}) == 32
+
+
+def test_tile_walk_rejects_bad_offsets():
+    plan = gg.cake_gg_plan("fwd", 2, 100, 64, 64, "bf16", 1)
+    for bad in ([1, 5, 9], [0, 9, 5], [0, 5, 101]):
+        with pytest.raises(gg.CakeGGError) as ei:
+            gg.cake_gg_tile_walk(plan, np.array(bad, np.int32))
+        assert ei.value.code == gg.CAKE_GG_ERR_BAD_OFFSETS
+
+
+def test_compute_calls_reject_bad_arguments_before_any_cuda_call():
+    """Host validation runs before the library touches CUDA (works without a GPU)."""
+    plan = gg.cake_gg_plan("fwd", 2, 256, 64, 64, "bf16", 1)
+    good = 1 << 20
+    # null pointer
+    assert gg.cake_gg_fwd(plan, 0, good, good, good, "bf16", 1, good, 4096, 0) == gg.CAKE_GG_ERR_INVALID_ARG
+    # misaligned pointer
+    assert gg.cake_gg_fwd(plan, good + 2, good, good, good, "bf16", 1, good, 4096, 0) == gg.CAKE_GG_ERR_ALIGNMENT
+    # plan / call mismatch: dtype, determinism, pass
+    assert gg.cake_gg_fwd(plan, good, good, good, good, "fp32", 1, good, 4096, 0) == gg.CAKE_GG_ERR_INVALID_ARG
+    assert gg.cake_gg_fwd(plan, good, good, good, good, "bf16", 0, good, 4096, 0) == gg.CAKE_GG_ERR_INVALID_ARG
+    assert gg.cake_gg_dgrad(plan, good, good, good, good, "bf16", 1, good, 4096, 0) == gg.CAKE_GG_ERR_INVALID_ARG
+    # workspace too small
+    assert gg.cake_gg_fwd(plan, good, good, good, good, "bf16", 1, good, 16, 0) == gg.CAKE_GG_ERR_WORKSPACE
+    wplan = gg.cake_gg_plan("wgrad", 1, 16384, 48, 4096, "fp32", 1)
+    assert gg.cake_gg_wgrad(wplan, good, good, good, good, "fp32", 1, good,
+                            wplan.workspace_bytes - 1, 0) == gg.CAKE_GG_ERR_WORKSPACE

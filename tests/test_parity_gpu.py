@@ -1,0 +1,176 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Element-by-element comparisons on seeded inputs sized so the oracle finishes
+in seconds while still spanning several tiles and ragged tails; exact
+(bitwise) comparisons where the inputs make every FP32 sum exact; guard bands
+around every output; rows beyond the last offset untouched.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from moe_ragged_grouped_gb300 import build as gg_build
+from moe_ragged_grouped_gb300 import cake_gg as gg
+from moe_ragged_grouped_gb300 import workloads as wl
+
+from gg_testutil import (assert_parity, guarded_empty, guards_intact, out_to_f64, reference, run,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    gg_build.build()
+    return gg.load_library()
+
+
+def make_inputs(sizes, N, K, seed, extra_rows=0, nan_tail=True):
+    rng = np.random.default_rng(seed)
+    E, M = len(sizes), sum(sizes) + extra_rows
+    Xb = wl.randn_bf16((M, K), 1.0, rng)
+    Wb = wl.randn_bf16((E, N, K), 1.0 / np.sqrt(K), rng)
+    Gb = wl.randn_bf16((M, N), 1.0, rng)
+    if nan_tail and extra_rows:
+        Xb[sum(sizes):] = 0x7FC0
+        Gb[sum(sizes):] = 0x7FC0
+    return Xb, Wb, Gb, wl.offsets_from_sizes(sizes)
+
+
+def out_shape(pass_, M, E, N, K):
+    return {"fwd": (M, N), "dgrad": (M, K), "wgrad": (E, N, K)}[pass_]
+
+
+def check_case(pass_, sizes, N, K, out_dtype, det, seed=0, extra_rows=0, max_sms=0):
+    Xb, Wb, Gb, off = make_inputs(sizes, N, K, seed, extra_rows)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    E, M = len(sizes), Xb.shape[0]
+    shape = out_shape(pass_, M, E, N, K)
+    buf, view, guard = guarded_empty(shape, out_dtype)
+    run(pass_, X, W, G, off, out_dtype, det, max_sms=max_sms, out=view)
+    import torch
+    torch.cuda.synchronize()
+    assert guards_intact(buf, guard, int(np.prod(shape)), out_dtype), "guard band overwritten"
+    got = out_to_f64(view)
+    ref = reference(pass_, Xb, Wb, Gb, off)
+    if pass_ != "wgrad":
+        tail = got[off[-1]:]
+        assert np.isnan(tail).all(), "rows beyond offsets[E] were written"
+        got = got[:off[-1]]
+    return assert_parity(pass_, got, ref, Xb, Wb, Gb, off, f"{pass_} {out_dtype} det={det} sizes={sizes}")
+
+
+PASSES = ["fwd", "dgrad", "wgrad"]
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("det", [1, 0])
+def test_tiny_config(pass_, out_dtype, det):
+    """E=4 experts x 128 rows, K=256, N=128 (X~N(0,1), W~N(0,1/K), G~N(0,1), seed 0)."""
+    check_case(pass_, [128] * 4, 128, 256, out_dtype, det, seed=0)
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_ragged_groups_with_empty_experts(pass_, out_dtype):
+    check_case(pass_, [0, 1, 129, 300, 0, 77], 192, 320, out_dtype, 1, seed=1, extra_rows=9)
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+def test_wide_tiles_several_ktiles(pass_):
+    check_case(pass_, [257, 511, 6], 512, 576, "fp32", 1, seed=2, extra_rows=3)
+
+
+@pytest.mark.parametrize("det", [1, 0])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_thin_weight_gradient_swapped_split(det, out_dtype):
+    """Dense projection shape family: E=1, d_out=48 (MMA rows over d_in, split reduction)."""
+    check_case("wgrad", [3000], 48, 512, out_dtype, det, seed=3, extra_rows=5)
+
+
+@pytest.mark.parametrize("det", [1, 0])
+@pytest.mark.parametrize("sizes", [[1500, 517, 0, 64], [4000]])
+def test_split_reduction_forced(det, sizes, monkeypatch):
+    monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "3")
+    check_case("wgrad", sizes, 128, 256, "fp32", det, seed=4, extra_rows=7)
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("det", [1, 0])
+def test_exact_integer_inputs_are_bitwise(pass_, det, monkeypatch):
+    """Inputs in {-2..2}: every FP32 sum is exact in any order, so GPU == oracle bitwise."""
+    if pass_ == "wgrad":
+        monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "2")
+    rng = np.random.default_rng(5)
+    sizes = [700, 0, 333, 64]
+    E, N, K = len(sizes), 128, 192
+    M = sum(sizes)
+    Xb = wl.small_int_bf16((M, K), rng)
+    Wb = wl.small_int_bf16((E, N, K), rng)
+    Gb = wl.small_int_bf16((M, N), rng)
+    off = wl.offsets_from_sizes(sizes)
+    got = out_to_f64(run(pass_, to_dev(Xb), to_dev(Wb), to_dev(Gb), off, "fp32", det))
+    ref = reference(pass_, Xb, Wb, Gb, off)
+    if pass_ != "wgrad":
+        got = got[:off[-1]]
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_one_hot_forward_selects_weight_columns():
+    rng = np.random.default_rng(6)
+    sizes = [130, 70]
+    E, N, K = 2, 128, 256
+    M = sum(sizes)
+    Wb = wl.randn_bf16((E, N, K), 1.0, rng)
+    Xb = np.zeros((M, K), np.uint16)
+    ks = rng.integers(0, K, M)
+    Xb[np.arange(M), ks] = 0x3F80
+    off = wl.offsets_from_sizes(sizes)
+    got = wl.torch_bf16_to_bits(run("fwd", to_dev(Xb), to_dev(Wb), to_dev(np.zeros((M, N), np.uint16)),
+                                    off, "bf16", 1))
+    for r in range(M):
+        e = 0 if r < off[1] else 1
+        np.testing.assert_array_equal(got[r], Wb[e][:, ks[r]])
+
+
+def test_all_zero_and_empty_weight_gradient():
+    sizes = [0, 200, 0]
+    Xb, Wb, Gb, off = make_inputs(sizes, 64, 128, seed=7)
+    got = out_to_f64(run("wgrad", to_dev(Xb), to_dev(Wb), to_dev(Gb), off, "fp32", 1))
+    assert not got[0].any() and not got[2].any() and got[1].any()
+    z = np.zeros_like(Xb)
+    got = out_to_f64(run("fwd", to_dev(z), to_dev(Wb), to_dev(Gb), off, "fp32", 1))
+    assert not got[:off[-1]].any()
+
+
+def test_no_rows_at_all():
+    import torch
+    Wb = wl.randn_bf16((3, 64, 64), 1.0, np.random.default_rng(0))
+    X = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    G = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    off = np.zeros(4, np.int32)
+    dW = torch.full((3, 64, 64), 7.0, device="cuda")
+    run("wgrad", X, to_dev(Wb), G, off, "fp32", 1, out=dW)
+    assert not dW.any()
+
+
+def test_device_detects_bad_offsets_and_recovers():
+    import torch
+    Xb, Wb, Gb, off = make_inputs([100, 100], 64, 64, seed=8)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    bad = torch.tensor([0, 150, 120], dtype=torch.int32, device="cuda")   # decreasing
+    with pytest.raises(gg.CakeGGError) as ei:
+        gg.grouped_gemm("fwd", X, W, bad, out_dtype="bf16")
+    assert ei.value.code == gg.CAKE_GG_ERR_BAD_OFFSETS
+    too_big = torch.tensor([0, 150, 201], dtype=torch.int32, device="cuda")  # > M_max
+    with pytest.raises(gg.CakeGGError) as ei:
+        gg.grouped_gemm("wgrad", G, X, too_big, out_dtype="fp32")
+    assert ei.value.code == gg.CAKE_GG_ERR_BAD_OFFSETS
+    # the context is still usable
+    check_case("fwd", [100, 100], 64, 64, "bf16", 1, seed=8)
