@@ -60,7 +60,8 @@ typedef enum {
     CAKE_GG_ERR_WORKSPACE = 5,    /* workspace missing or smaller than plan->workspace_bytes */
     CAKE_GG_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed                      */
     CAKE_GG_ERR_BAD_OFFSETS = 7,  /* device-detected: offsets not 0-based, decreasing or > M_max */
-    CAKE_GG_ERR_TIMEOUT = 8       /* device-detected: a bounded wait inside the kernel expired */
+    CAKE_GG_ERR_TIMEOUT = 8,      /* device-detected: a bounded wait inside the kernel expired */
+    CAKE_GG_ERR_SCRATCH_LIMIT = 9 /* the problem needs more scratch than cake_gg_wgrad_noalloc's fixed maximum */
 } cake_gg_status_t;
 
 typedef enum { CAKE_GG_FWD = 0, CAKE_GG_DGRAD = 1, CAKE_GG_WGRAD = 2 } cake_gg_pass_t;
@@ -125,6 +126,35 @@ int cake_gg_dgrad(const cake_gg_plan_t *plan, const void *G, const void *W, void
 int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
                   const int32_t *offsets, int out_dtype, int deterministic,
                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Weight gradient without any allocation and without a caller workspace.
+ *
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that cannot allocate device memory: a plugin or custom-operator interface
+ * that hands the library only its input and output pointers and a stream
+ * (no allocator, no workspace hook), and code that must not allocate once it
+ * is running (an allocation can synchronise the device or fail under memory
+ * pressure in the middle of a training step).
+ *
+ * Same arguments and result as cake_gg_wgrad() minus the workspace: the
+ * library uses its own scratch, a fixed array of CAKE_GG_NOALLOC_SCRATCH_BYTES
+ * in device memory that every GPU which loads the library holds until the
+ * process exits.  Nothing is allocated or freed by the call.
+ *  - A plan whose workspace_bytes exceeds CAKE_GG_NOALLOC_SCRATCH_BYTES is
+ *    rejected with CAKE_GG_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - The first call on each device looks up the scratch array's device
+ *    address (with that device current); make that first call before any
+ *    stream capture begins.
+ *  - Every call on a device shares the one scratch array, which keeps the
+ *    last call's contents; each call clears the parts that must start at
+ *    zero.  Calls whose kernels overlap on the GPU (different streams without
+ *    ordering between them) race on the scratch and give wrong results:
+ *    order them on one stream.
+ *  - Device-detected errors are written to the scratch's status word, which
+ *    callers cannot read; outputs are unspecified after such an error. */
+#define CAKE_GG_NOALLOC_SCRATCH_BYTES (16u << 20)
+int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
+                          const int32_t *offsets, int out_dtype, int deterministic, void *stream);
 
 /* Synchronise `stream` and return the status word the last call that used
  * `workspace` left there (CAKE_GG_OK, _BAD_OFFSETS or _TIMEOUT), or

@@ -26,6 +26,8 @@ CAKE_GG_ERR_WORKSPACE = 5
 CAKE_GG_ERR_CUDA = 6
 CAKE_GG_ERR_BAD_OFFSETS = 7
 CAKE_GG_ERR_TIMEOUT = 8
+CAKE_GG_ERR_SCRATCH_LIMIT = 9
+CAKE_GG_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 CAKE_GG_FWD, CAKE_GG_DGRAD, CAKE_GG_WGRAD = 0, 1, 2
 CAKE_GG_BF16, CAKE_GG_FP32 = 0, 1
@@ -101,6 +103,8 @@ def load_library(path: str = LIB_PATH):
     lib.cake_gg_tile_walk.argtypes = [plan_p, ctypes.POINTER(ctypes.c_int32), i64,
                                       ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]
     lib.cake_gg_tile_walk.restype = ctypes.c_int
+    lib.cake_gg_wgrad_noalloc.argtypes = [plan_p, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp]
+    lib.cake_gg_wgrad_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -178,6 +182,19 @@ def cake_gg_wgrad(plan, G, X, dW, offsets, out_dtype, deterministic, workspace, 
     """cake_gg_wgrad(): dW_e = G_e^T X_e per expert; returns the status code."""
     return _call("cake_gg_wgrad", plan, G, X, dW, offsets, out_dtype, deterministic, workspace,
                  workspace_bytes, stream)
+
+
+def cake_gg_wgrad_noalloc(plan, G, X, dW, offsets, out_dtype, deterministic, stream=None) -> int:
+    """cake_gg_wgrad_noalloc(): the weight gradient using the library's fixed scratch.
+
+    For callers that cannot allocate device memory (no workspace argument, no
+    allocation inside the call).  Returns the status code;
+    CAKE_GG_ERR_SCRATCH_LIMIT when plan.workspace_bytes exceeds
+    CAKE_GG_NOALLOC_SCRATCH_BYTES.
+    """
+    s = _stream(stream, G, X, dW)
+    return load_library().cake_gg_wgrad_noalloc(ctypes.byref(plan), _ptr(G), _ptr(X), _ptr(dW), _ptr(offsets),
+                                                _dtype_code(out_dtype), int(bool(deterministic)), s)
 
 
 def cake_gg_check_status(workspace, stream=None) -> int:

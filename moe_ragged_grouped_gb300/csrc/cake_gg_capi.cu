@@ -291,6 +291,8 @@ const char *cake_gg_strerror(int code)
     case CAKE_GG_ERR_CUDA: return "CUDA call failed";
     case CAKE_GG_ERR_BAD_OFFSETS: return "device found invalid group offsets";
     case CAKE_GG_ERR_TIMEOUT: return "a bounded wait inside the kernel expired";
+    case CAKE_GG_ERR_SCRATCH_LIMIT:
+        return "problem needs more scratch than the no-allocation entry point's fixed maximum";
     default: return "unknown status";
     }
 }
@@ -457,3 +459,36 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation entry point
+//
+// Scratch for cake_gg_wgrad_noalloc: a fixed device array (status word,
+// tickets, partial tiles) that stands in for the caller's workspace.  Host
+// code must not pass the symbol itself to a kernel (on the host it names a
+// host-side shadow, not device memory); its device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[CAKE_GG_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void *g_noalloc_scratch_addr[64];  // per device; filled by the first call on that device
+}
+
+extern "C" int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
+                                     const int32_t *offsets, int out_dtype, int deterministic,
+                                     void *stream)
+{
+    if (!plan) return CAKE_GG_ERR_INVALID_ARG;
+    if (plan->workspace_bytes > CAKE_GG_NOALLOC_SCRATCH_BYTES) return CAKE_GG_ERR_SCRATCH_LIMIT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CAKE_GG_ERR_CUDA;
+    if (!g_noalloc_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return CAKE_GG_ERR_CUDA;
+        g_noalloc_scratch_addr[dev] = ptr;
+    }
+    void *scratch = g_noalloc_scratch_addr[dev];
+    int rc = check_call(plan, CAKE_GG_WGRAD, G, X, dW, offsets, out_dtype, deterministic, scratch,
+                        CAKE_GG_NOALLOC_SCRATCH_BYTES);
+    if (rc != CAKE_GG_OK) return rc;
+    return run(plan, kModeWgrad, G, X, dW, offsets, scratch, static_cast<cudaStream_t>(stream));
+}
