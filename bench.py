@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each pass from a captured CUDA graph (removes host launch overhead)")
     return ap.parse_args()
 
 
@@ -53,6 +55,9 @@ def get_workload(name):
     from moe_ragged_grouped_gb300 import workloads as wl
     if name == "moe_gate_up":
         return wl.moe_gate_up()
+    if name == "moe_gate_up_m16k":
+        w = wl.moe_gate_up()
+        return wl.Workload("moe_gate_up_E8_M16384_K4096_N3072", 8, 3072, 4096, wl.balanced_sizes(8, 16384))
     if name == "moe_down":
         return wl.moe_down()
     if name == "moe_skew":
@@ -202,6 +207,7 @@ def run_ours(args, wk):
     s = stream.cuda_stream
 
     def launch(p):
+        s = torch.cuda.current_stream(dev).cuda_stream
         if p == "fwd":
             rc = gg.cake_gg_fwd(plans[p], X, W, Y, offs, od, det, wss[p], stream=s)
         elif p == "dgrad":
@@ -215,6 +221,21 @@ def run_ours(args, wk):
         for p in passes:
             launch(p)
     torch.cuda.synchronize(dev)
+    run_pass = launch
+    if args.graph:
+        graphs = {}
+        cap = torch.cuda.Stream(dev)
+        for p in passes:
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_, stream=cap):
+                launch(p)
+            graphs[p] = g_
+        torch.cuda.synchronize(dev)
+        run_pass = lambda p: graphs[p].replay()
+        for _ in range(2):
+            for p in passes:
+                run_pass(p)
+        torch.cuda.synchronize(dev)
     for p in passes:
         st = gg.cake_gg_check_status(wss[p], s)
         if st != 0:
@@ -233,7 +254,7 @@ def run_ours(args, wk):
     for i in range(args.steps):
         evs[i][0].record(stream)
         for j, p in enumerate(passes):
-            launch(p)
+            run_pass(p)
             evs[i][j + 1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
@@ -320,6 +341,7 @@ def run_ours(args, wk):
                        "l2": "no flush: operands per step (%.2f GB) exceed the 129 MB L2" % (
                            (X.numel() + W.numel() + G.numel()) * 2 / 1e9),
                        "parallelism": f"replicas x{ws}",
+                       "launch": "cuda-graph replay per pass" if args.graph else "eager",
                        "plans": {p: {k: v for k, v in plans[p].as_dict().items()
                                      if k in ("tile_n", "stages", "swap_ab", "split_chunk")} for p in passes}},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -70,7 +70,9 @@ typedef enum { CAKE_GG_BF16 = 0, CAKE_GG_FP32 = 1 } cake_gg_dtype_t;
 /* Plan: a caller-owned plain struct filled by cake_gg_plan(); nothing to free.
  * The first block holds the problem as given; the second holds the choices
  * made for it.  The choices are a pure function of the first block minus
- * max_sms, so max_sms changes only how many CTAs run, never a result bit. */
+ * max_sms, so max_sms changes only how many CTAs run, never a result bit.
+ * With pair = 2 the launch uses clusters of two CTAs, so the number of CTAs
+ * is max_sms rounded down to an even number (at least 2). */
 typedef struct cake_gg_plan {
     int32_t abi_version;     /* CAKE_GG_ABI_VERSION                                 */
     int32_t pass;            /* cake_gg_pass_t                                      */
@@ -86,7 +88,7 @@ typedef struct cake_gg_plan {
     int32_t tile_n;          /* MMA columns per tile (64 .. 256)                    */
     int32_t tile_k;          /* reduction elements per pipeline stage (64)          */
     int32_t stages;          /* shared-memory ring depth                            */
-    int32_t cta_group;       /* CTAs per MMA (1)                                    */
+    int32_t pair;            /* CTAs per cluster sharing one B tile by multicast (1 or 2) */
     int32_t swap_ab;         /* weight gradient: 1 = MMA rows run over K (thin N)   */
     int32_t split_chunk;     /* weight gradient: k-blocks per split, 0 = no split   */
     int32_t debug_flags;     /* test-only fault injection; 0 in normal use          */

@@ -56,7 +56,7 @@ class CakeGGPlan(ctypes.Structure):
         ("tile_n", ctypes.c_int32),
         ("tile_k", ctypes.c_int32),
         ("stages", ctypes.c_int32),
-        ("cta_group", ctypes.c_int32),
+        ("pair", ctypes.c_int32),
         ("swap_ab", ctypes.c_int32),
         ("split_chunk", ctypes.c_int32),
         ("debug_flags", ctypes.c_int32),

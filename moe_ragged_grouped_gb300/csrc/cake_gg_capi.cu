@@ -18,9 +18,9 @@ using namespace cakegg;
 
 namespace {
 
-constexpr int kSplitTargetUnits = 4 * 152;  // weight-gradient work units aimed for when splitting
+constexpr int kWaveCtas = 152;              // GB300 SMs: the wave size the split model assumes
 constexpr int kMinSplitChunk = 4;           // k-blocks (256 rows) per split at least
-constexpr size_t kSmemLimit = 232448;       // opt-in dynamic shared memory per CTA
+constexpr size_t kSmemLimit = kSmemOptInLimit;
 constexpr uint64_t kHeaderBytes = 256;      // workspace: status word and padding
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -45,6 +45,36 @@ int env_int(const char *name, int dflt)
     const char *s = std::getenv(name);
     if (!s || !*s) return dflt;
     return std::atoi(s);
+}
+
+// Reduction split of the weight gradient: the number of splits S minimising a
+// simple time model -- full waves of kWaveCtas CTAs, each unit costing its
+// k-blocks plus, when split, the partial-tile round trip and the finish
+// (expressed in k-block equivalents) -- returned as k-blocks per split
+// (0 = no split).  A pure function of the problem: never of the CTA count
+// a launch uses, so deterministic results do not depend on max_sms.
+int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn)
+{
+    if (out_tiles <= 0 || kblocks_per_expert < 2 * kMinSplitChunk) return 0;
+    const double partial_kb = 2.0 * 2.0 * 1024.0 * bn / (16384.0 + 128.0 * bn);  // write + read, x2 margin
+    const double c_split = partial_kb + 4.0;
+    auto cost = [&](int64_t S) {
+        const int64_t units = out_tiles * S;
+        const int64_t waves = (units + kWaveCtas - 1) / kWaveCtas;
+        const double per = double(kblocks_per_expert) / double(S) + (S > 1 ? c_split : 0.0);
+        return double(waves) * per;
+    };
+    int64_t best_s = 1;
+    double best = cost(1);
+    for (int64_t S = 2; S <= 64 && kblocks_per_expert / S >= kMinSplitChunk; ++S) {
+        const double c = cost(S);
+        if (c < best * 0.97) {
+            best = c;
+            best_s = S;
+        }
+    }
+    if (best_s == 1) return 0;
+    return int32_t((kblocks_per_expert + best_s - 1) / best_s);
 }
 
 int tmem_cols_for(int bn)
@@ -140,16 +170,19 @@ int get_encoder()
     return CAKE_GG_OK;
 }
 
-// BF16 tensor of rank 2 ({inner, outer}) or 3 ({inner, mid, outer}), dense,
-// 128-byte swizzled boxes, zero fill outside the tensor.
+// BF16 (or FP32) tensor of rank 2 ({inner, outer}) or 3 ({inner, mid, outer}),
+// dense, 128-byte swizzled boxes, zero fill outside the tensor for loads and
+// clipping at its bounds for stores.
 int encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, uint32_t box0,
-               uint32_t box1)
+               uint32_t box1, bool fp32 = false)
 {
+    const uint64_t es = fp32 ? 4 : 2;
     cuuint64_t gdim[3] = {dims[0], dims[1], rank > 2 ? dims[2] : 1};
-    cuuint64_t gstride[2] = {dims[0] * 2, dims[0] * dims[1] * 2};
+    cuuint64_t gstride[2] = {dims[0] * es, dims[0] * dims[1] * es};
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
+    CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          cuuint32_t(rank), const_cast<void *>(base),
                           gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -168,7 +201,8 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
     if (plan->E < 1 || plan->E > kMaxE || plan->N < 1 || plan->K < 1 || plan->M_max < 0 ||
         plan->M_max > INT32_MAX)
         return CAKE_GG_ERR_INVALID_ARG;
-    if (plan->tile_m != kTileM || plan->tile_k != kTileK || plan->cta_group != 1 ||
+    if (plan->tile_m != kTileM || plan->tile_k != kTileK || (plan->pair != 1 && plan->pair != 2) ||
+        (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
         plan->tile_n < 64 || plan->tile_n > 256 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
         smem_bytes_for(plan->tile_n, plan->stages) > kSmemLimit)
@@ -213,12 +247,27 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
         return CAKE_GG_OK;
     }
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mo;
+    std::memset(&mo, 0, sizeof mo);
+    const bool tma_store = env_int("CAKE_GG_TMA_STORE", 1) != 0 && !(mode == kModeWgrad && plan->swap_ab);
+    if (tma_store) {
+        // output boxes: 32 rows x 128 bytes (64 BF16 or 32 FP32 columns)
+        const uint32_t cw = out_f32 ? 32 : 64;
+        if (mode == kModeWgrad) {
+            const uint64_t d[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
+            rc = encode_map(&mo, out, 3, d, cw, 32, out_f32);
+        } else {
+            const uint64_t d[2] = {uint64_t(mode == kModeFwd ? N : K), M};
+            rc = encode_map(&mo, out, 2, d, cw, 32, out_f32);
+        }
+        if (rc != CAKE_GG_OK) return rc;
+    }
     if (mode == kModeFwd) {
         const uint64_t dx[2] = {uint64_t(K), M};
         const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
         if ((rc = encode_map(&ma, opA, 2, dx, 64, kTileM)) != CAKE_GG_OK) return rc;
-        if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(bn))) != CAKE_GG_OK) return rc;
+        if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(plan->pair == 2 ? bn / 2 : bn))) != CAKE_GG_OK)
+            return rc;
     } else if (mode == kModeDgrad) {
         const uint64_t dg[2] = {uint64_t(N), M};
         const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
@@ -249,29 +298,32 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.kchunk = mode == kModeWgrad ? plan->split_chunk : 0;
     p.det = plan->deterministic ? 1 : 0;
     p.tmem_cols = tmem_cols_for(bn);
+    p.tma_store = tma_store ? 1 : 0;
     p.debug_flags = plan->debug_flags;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
-    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk);
-    uint64_t tile_bound;
+    const int P = plan->pair;
+    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P);
+    uint64_t unit_bound;
     if (mode == kModeWgrad) {
         uint64_t splits = uint64_t(E);
         if (p.kchunk > 0) splits = M / (uint64_t(kTileK) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
-        tile_bound = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles) * splits;
+        unit_bound = uint64_t(m_units_w(g)) * uint64_t(g.n_tiles) * splits;
     } else {
-        tile_bound = (M / kTileM + uint64_t(E) + 1) * uint64_t(g.n_tiles);
+        unit_bound = (M / (uint64_t(kTileM) * P) + uint64_t(E) + 1) * uint64_t(g.n_tiles);
     }
     int grid = dev.sms;
     if (plan->max_sms > 0 && plan->max_sms < grid) grid = plan->max_sms;
-    if (tile_bound < uint64_t(grid)) grid = int(tile_bound);
-    if (grid < 1) grid = 1;
+    if (unit_bound * P < uint64_t(grid)) grid = int(unit_bound * P);
+    grid -= grid % P;
+    if (grid < P) grid = P;
 
     const size_t smem = smem_bytes_for(bn, plan->stages);
     cudaError_t err;
-    if (mode == kModeFwd) err = launch_fwd(out_f32, ma, mb, p, grid, smem, stream);
-    else if (mode == kModeDgrad) err = launch_dgrad(out_f32, ma, mb, p, grid, smem, stream);
-    else err = launch_wgrad(out_f32, plan->swap_ab != 0, ma, mb, p, grid, smem, stream);
+    if (mode == kModeFwd) err = launch_fwd(out_f32, P, ma, mb, mo, p, grid, smem, stream);
+    else if (mode == kModeDgrad) err = launch_dgrad(out_f32, P, ma, mb, mo, p, grid, smem, stream);
+    else err = launch_wgrad(out_f32, plan->swap_ab != 0, P, ma, mb, mo, p, grid, smem, stream);
     return err == cudaSuccess ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
 }
 
@@ -325,7 +377,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->max_sms = max_sms;
     plan->tile_m = kTileM;
     plan->tile_k = kTileK;
-    plan->cta_group = 1;
+    plan->pair = 1;
     plan->timeout_ns = kDefaultTimeoutNs;
 
     auto pick_bn = [](int32_t width) {
@@ -342,6 +394,11 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     const int env_bn = env_int("CAKE_GG_TILE_N", 0);
     if (env_bn >= 64 && env_bn <= 256 && env_bn % 64 == 0) bn = env_bn;
     plan->tile_n = bn;
+    // two CTAs share (multicast) the B tile when it is wide; swapped thin
+    // weight gradients stay single
+    plan->pair = (bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab)) ? 2 : 1;
+    const int env_pair = env_int("CAKE_GG_PAIR", -1);
+    if (env_pair == 0) plan->pair = 1;
 
     int stages = kMaxStages;
     while (stages > 2 && smem_bytes_for(bn, stages) > kSmemLimit) --stages;
@@ -353,19 +410,12 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
         const int64_t tpe = int64_t(g.m_tiles_w) * g.n_tiles;
         if (tpe * E > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
-        int32_t chunk = 0;
-        if (tpe * E < kSplitTargetUnits / 2) {
-            const int64_t total_kb = (M_max + kTileK - 1) / kTileK + E;
-            int64_t c = (tpe * total_kb + kSplitTargetUnits - 1) / kSplitTargetUnits;
-            if (c < kMinSplitChunk) c = kMinSplitChunk;
-            chunk = c > INT32_MAX ? INT32_MAX : int32_t(c);
-        }
+        plan->split_chunk = choose_split_chunk(tpe * E, (M_max / E + kTileK - 1) / kTileK, bn);
         const char *es = std::getenv("CAKE_GG_SPLIT_CHUNK");
         if (es && *es) {
             const int v = std::atoi(es);
-            if (v >= 0) chunk = v;
+            if (v >= 0) plan->split_chunk = v;
         }
-        plan->split_chunk = chunk;
     }
     const WsLayout w = ws_layout(*plan);
     if (!w.ok) return CAKE_GG_ERR_OVERFLOW;
@@ -426,7 +476,7 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
         if (off[e + 1] < off[e]) return CAKE_GG_ERR_BAD_OFFSETS;
     const int mode = plan->pass == CAKE_GG_FWD ? kModeFwd : plan->pass == CAKE_GG_DGRAD ? kModeDgrad : kModeWgrad;
     const Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
-                             mode == kModeWgrad ? plan->split_chunk : 0);
+                             mode == kModeWgrad ? plan->split_chunk : 0, plan->pair);
     std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
     for (int e = 0; e < E; ++e) {
         cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
@@ -441,20 +491,27 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
         pref[i + 1] = pref[i] + cnt[order[i]];
         spref[i + 1] = spref[i] + expert_splits(g, off[i + 1] - off[i]);
     }
-    const int64_t total = pref[E];
-    *count = total;
-    for (int64_t t = 0; t < total && t < capacity; ++t) {
-        const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data());
-        int32_t *o = tiles_out + t * 8;
-        o[0] = ti.e;
-        o[1] = ti.mt;
-        o[2] = ti.nt;
-        o[3] = ti.s;
-        o[4] = ti.S;
-        o[5] = ti.kb0;
-        o[6] = ti.kb1;
-        o[7] = ti.ticket;
+    const int64_t units = pref[E];
+    int64_t n = 0;
+    for (int64_t t = 0; t < units; ++t) {
+        for (int r = 0; r < g.pair; ++r) {
+            const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data(), r);
+            if (!ti.valid) continue;
+            if (n < capacity) {
+                int32_t *o = tiles_out + n * 8;
+                o[0] = ti.e;
+                o[1] = ti.mt;
+                o[2] = ti.nt;
+                o[3] = ti.s;
+                o[4] = ti.S;
+                o[5] = ti.kb0;
+                o[6] = ti.kb1;
+                o[7] = ti.ticket;
+            }
+            ++n;
+        }
     }
+    *count = n;
     return CAKE_GG_OK;
 }
 

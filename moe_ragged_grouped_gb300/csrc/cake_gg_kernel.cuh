@@ -41,6 +41,8 @@ constexpr int kStatusBadOffsets = 7;
 constexpr int kStatusTimeout = 8;
 constexpr uint32_t kABytes = kTileM * kTileK * 2;  // 16 KB: A tile of one stage
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;        // one 64 x 64 MN-major box
+constexpr size_t kSmemOptInLimit = 232448;        // opt-in dynamic shared memory per CTA (227 KB)
+constexpr uint32_t kStagingBytes = 4 * 32 * 128;   // epilogue: 32 rows x 128 B per epilogue warp
 
 struct KParams {
     const int32_t *offsets;
@@ -55,6 +57,7 @@ struct KParams {
     int32_t kchunk;
     int32_t det;
     int32_t tmem_cols;
+    int32_t tma_store;      // epilogue through shared memory + TMA tensor stores
     int32_t debug_flags;
     uint64_t timeout_ns;
 };
@@ -80,7 +83,7 @@ __host__ __device__ constexpr uint32_t stage_bytes_for(int bn) { return kABytes 
 
 __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages)
 {
-    return 1024 + size_t(stages) * stage_bytes_for(bn) + sizeof(Ctrl);
+    return 1024 + size_t(stages) * stage_bytes_for(bn) + kStagingBytes + sizeof(Ctrl);
 }
 
 // Bounded wait on one mbarrier phase, by every lane of the calling warp;
@@ -181,10 +184,10 @@ __device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
 
 // ---------------------------------------------------------------- kernel
 
-template <int MODE, bool SWAP, bool OUT_F32>
+template <int MODE, bool SWAP, bool OUT_F32, int PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     cake_gg_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                   const KParams p)
+                   const __grid_constant__ CUtensorMap mapOut, const KParams p)
 {
     constexpr bool A_MN = (MODE == kModeWgrad);
     constexpr bool B_MN = (MODE != kModeFwd);
@@ -194,13 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *ring = smem_raw + (ring_u32 - raw_u32);
     const uint32_t stage_bytes = stage_bytes_for(p.bn);
-    Ctrl *c = reinterpret_cast<Ctrl *>(ring + size_t(p.stages) * stage_bytes);
+    uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
+    Ctrl *c = reinterpret_cast<Ctrl *>(staging + kStagingBytes);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int E = p.E;
-    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk);
+    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR);
+    // a pair (cluster of 2) shares each unit; rank r computes m-tile 2 * unit + r
+    const int rank = PAIR == 2 ? int(cluster_ctarank()) : 0;
+    const int64_t unit0 = blockIdx.x / PAIR;
+    const int64_t unit_step = gridDim.x / PAIR;
+    constexpr uint16_t kPairMask = 0x3;
 
     // ---- setup: offsets, validation, walk tables (temporaries in the ring) ----
     int32_t *t_cnt = reinterpret_cast<int32_t *>(ring);
@@ -275,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_u32(&c->full[s]), 1);
-            mbar_init(smem_u32(&c->empty[s]), 1);
+            mbar_init(smem_u32(&c->empty[s]), PAIR);  // both CTAs' MMAs read a shared stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c->tfull[a]), 1);
@@ -288,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
+    if (PAIR == 2) cluster_sync_all();  // the peer's barriers exist before any multicast reaches them
     tc_fence_after_sync();
 
     const int64_t total = c->pref[E];
@@ -304,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref);
+            for (int64_t t = unit0; t < total && ok; t += unit_step) {
+                const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                     if (!thread_wait(smem_u32(&c->empty[stage]), phase ^ 1u, c, p, p.timeout_ns)) {
                         ok = false;
@@ -316,7 +326,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sb = sa + kABytes;
                     mbar_arrive_expect_tx(fb, tx);
                     const bool drop = (p.debug_flags & 1) && blockIdx.x == 0 && issued == 0;
-                    if (!drop) {
+                    if (!drop && PAIR == 2) {
+                        // own A; half of the shared B, multicast to both CTAs of the pair
+                        const int nb = p.bn / 64;
+                        if (MODE == kModeWgrad) {
+                            const int32_t r = ti.row0 + kb * kTileK;
+                            tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
+                            tma_load_2d(sa + kBoxBytes, &mapA, fb, ti.mt * kTileM + 64, r);
+                            for (int j = rank * nb / 2; j < (rank + 1) * nb / 2; ++j)
+                                tma_load_2d_mc(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j, r, kPairMask);
+                        } else if (MODE == kModeFwd) {
+                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
+                            tma_load_3d_mc(sb + uint32_t(rank) * uint32_t(p.bn / 2) * 128u, &mapB, fb, kb * kTileK,
+                                           ti.nt * p.bn + rank * (p.bn / 2), ti.e, kPairMask);
+                        } else {
+                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
+                            for (int j = rank * nb / 2; j < (rank + 1) * nb / 2; ++j)
+                                tma_load_3d_mc(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j, kb * kTileK,
+                                               ti.e, kPairMask);
+                        }
+                    } else if (!drop) {
                         if (MODE == kModeWgrad) {
                             const int32_t r = ti.row0 + kb * kTileK;
                             tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
@@ -359,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         bool any_mma = false;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref);
+        for (int64_t t = unit0; t < total && ok; t += unit_step, ++it) {
+            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
             const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
             if (!warp_wait(smem_u32(&c->tempty[acc]), acc_phase ^ 1u, c, p)) {
@@ -406,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : smem_desc_sw128(sb + ks * 32, 16, 1024);
                         umma_bf16(d_tmem, ad, bd, idesc, (kb > ti.kb0 || ks > 0) ? 1u : 0u);
                     }
-                    umma_commit(smem_u32(&c->empty[stage]));
+                    if (PAIR == 2) umma_commit_mc(smem_u32(&c->empty[stage]), kPairMask);
+                    else umma_commit(smem_u32(&c->empty[stage]));
                 }
                 any_mma = true;
                 __syncwarp();
@@ -432,8 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lrow = q * 32 + lane;    // tile row held by this thread
         const int etid = tid - 64;         // 0..127
         int it = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref);
+        for (int64_t t = unit0; t < total; t += unit_step, ++it) {
+            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
             const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
             bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
@@ -442,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
 
             const bool empty_tile = ti.kb1 <= ti.kb0;
-            const bool split = (MODE == kModeWgrad) && ti.S > 1;
+            const bool split = (MODE == kModeWgrad) && ti.S > 1 && ti.valid;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc) * acc_stride;
 
             // output geometry of this tile
@@ -481,7 +511,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : p.partials + int64_t(ti.ticket) * kTileM * p.bn;
             }
 
-            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+            // full 32-row slabs of a non-split, non-transposed tile go out through
+            // shared memory and TMA tensor stores (whole 128-byte lines); rows at
+            // an expert's end use the masked direct stores below
+            const bool tma_path = p.tma_store && ti.valid && !split && !(MODE == kModeWgrad && SWAP) &&
+                                  (MODE == kModeWgrad ? q * 32 < rows_valid : q * 32 + 32 <= rows_valid);
+            if (tma_path) {
+                constexpr int CW = OUT_F32 ? 32 : 64;  // columns per 128-byte row
+                uint8_t *stg = staging + q * 4096;
+                const uint32_t stg_u32 = smem_u32(stg);
+                for (int c0 = 0; c0 < p.bn; c0 += CW) {
+                    uint32_t w[32];
+                    if (empty_tile) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) w[j] = 0u;
+                    } else if (OUT_F32) {
+                        tmem_ld_32x32b_x32(t_row + uint32_t(c0), w);
+                        tmem_ld_wait();
+                    } else {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld_32x32b_x32(t_row + uint32_t(c0), r0);
+                        tmem_ld_32x32b_x32(t_row + uint32_t(c0 + 32), r1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            w[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+                            w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+                        }
+                    }
+                    if (lane == 0) bulk_wait_read_all();  // previous store has read the buffer
+                    __syncwarp();
+                    uint8_t *rowp = stg + lane * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4 *>(rowp + ((ch ^ (lane & 7)) << 4)) =
+                            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && c0 < cols_valid) {
+                        const int32_t x = ti.nt * p.bn + c0;
+                        if (MODE == kModeWgrad)
+                            tma_store_3d(&mapOut, stg_u32, x, ti.mt * kTileM + q * 32, ti.e);
+                        else
+                            tma_store_2d(&mapOut, stg_u32, x, ti.row0 + q * 32);
+                        bulk_commit_group();
+                    }
+                    __syncwarp();
+                }
+            }
+            for (int c0 = 0; c0 < p.bn && !tma_path; c0 += 32) {
                 float v[32];
                 if (empty_tile) {
 #pragma unroll
@@ -538,30 +616,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float *base0 = p.det ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
                                                : slot_ptr;
                     const int nsum = p.det ? ti.S : 1;
-                    for (int c4 = 0; c4 < p.bn / 4; ++c4) {
-                        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int s = 0; s < nsum; ++s) {
-                            const float4 b = ld_cg_f4(base0 + int64_t(s) * kTileM * p.bn +
-                                                      (int64_t(c4) * kTileM + lrow) * 4);
-                            if (s == 0) a = b;
-                            else {
-                                a.x += b.x;
-                                a.y += b.y;
-                                a.z += b.z;
-                                a.w += b.w;
+                    const int64_t slot_stride = int64_t(kTileM) * p.bn;
+                    // 4 float4 columns x up to 4 slots per batch: 16 independent loads in flight
+                    for (int c4 = 0; c4 < p.bn / 4; c4 += 4) {
+                        float4 acc[4];
+                        for (int s0 = 0; s0 < nsum; s0 += 4) {
+                            float4 b[4][4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    if (s0 + u < nsum)
+                                        b[u][j] = __ldcg(reinterpret_cast<const float4 *>(
+                                            base0 + (s0 + u) * slot_stride + (int64_t(c4 + j) * kTileM + lrow) * 4));
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                if (s0 + u < nsum) {
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        if (s0 + u == 0) acc[j] = b[u][j];
+                                        else {
+                                            acc[j].x += b[u][j].x;
+                                            acc[j].y += b[u][j].y;
+                                            acc[j].z += b[u][j].z;
+                                            acc[j].w += b[u][j].w;
+                                        }
+                                    }
+                                }
                             }
                         }
-                        const int col = c4 * 4;
-                        if (row_ok && col < cols_valid) {
-                            const float vv[4] = {a.x, a.y, a.z, a.w};
-                            if (MODE == kModeWgrad && SWAP) {
 #pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    store_scalar<OUT_F32>(p.out, out_base + int64_t(col + j) * ld + lrow, vv[j]);
-                            } else {
+                        for (int j = 0; j < 4; ++j) {
+                            const int col = (c4 + j) * 4;
+                            if (row_ok && col < cols_valid) {
+                                const float vv[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+                                if (MODE == kModeWgrad && SWAP) {
 #pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    store_scalar<OUT_F32>(p.out, out_base + int64_t(lrow) * ld + col + j, vv[j]);
+                                    for (int q4 = 0; q4 < 4; ++q4)
+                                        store_scalar<OUT_F32>(p.out, out_base + int64_t(col + q4) * ld + lrow, vv[q4]);
+                                } else if (OUT_F32) {
+                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + out_base +
+                                                                int64_t(lrow) * ld + col) = acc[j];
+                                } else {
+                                    uint2 pk;
+                                    pk.x = pack_bf16x2(vv[0], vv[1]);
+                                    pk.y = pack_bf16x2(vv[2], vv[3]);
+                                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + out_base +
+                                                               int64_t(lrow) * ld + col) = pk;
+                                }
                             }
                         }
                     }
@@ -570,10 +672,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (warp >= 2) {
+        if (lane == 0) bulk_wait_all();  // epilogue stores complete before the CTA retires
+        __syncwarp();
+    }
+
     // ---- teardown: every role is done; release TMEM ----
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
+    // no CTA leaves while its peer may still multicast into it or arrive on its barriers
+    if (PAIR == 2) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, uint32_t(p.tmem_cols));

@@ -9,23 +9,57 @@
 
 namespace cakegg {
 
-cudaError_t launch_fwd(bool out_f32, const CUtensorMap &a, const CUtensorMap &b, const KParams &p,
-                       int grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_dgrad(bool out_f32, const CUtensorMap &a, const CUtensorMap &b, const KParams &p,
-                         int grid, size_t smem, cudaStream_t stream);
-cudaError_t launch_wgrad(bool out_f32, bool swap, const CUtensorMap &a, const CUtensorMap &b,
+cudaError_t launch_fwd(bool out_f32, int pair, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                       const KParams &p, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_dgrad(bool out_f32, int pair, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
                          const KParams &p, int grid, size_t smem, cudaStream_t stream);
+cudaError_t launch_wgrad(bool out_f32, bool swap, int pair, const CUtensorMap &a, const CUtensorMap &b,
+                         const CUtensorMap &o, const KParams &p, int grid, size_t smem, cudaStream_t stream);
+
+template <int MODE, bool SWAP, bool OUT_F32, int PAIR>
+cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const KParams &p,
+                       int grid, size_t smem, cudaStream_t stream)
+{
+    auto kern = cake_gg_kernel<MODE, SWAP, OUT_F32, PAIR>;
+    // the opt-in shared-memory limit is raised once per device to the maximum,
+    // so later calls (including ones under stream capture) skip the attribute call
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemOptInLimit));
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    if (smem > kSmemOptInLimit) return cudaErrorInvalidValue;
+    if (PAIR == 1) {
+        kern<<<grid, kThreads, smem, stream>>>(a, b, o, p);
+        return cudaGetLastError();
+    }
+    if (grid % PAIR != 0) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, b, o, p);
+}
 
 template <int MODE, bool SWAP, bool OUT_F32>
-cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const KParams &p, int grid,
-                       size_t smem, cudaStream_t stream)
+cudaError_t launch_pair_or_single(int pair, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                                  const KParams &p, int grid, size_t smem, cudaStream_t stream)
 {
-    auto kern = cake_gg_kernel<MODE, SWAP, OUT_F32>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, smem, stream>>>(a, b, p);
-    return cudaGetLastError();
+    return pair == 2 ? launch_one<MODE, SWAP, OUT_F32, 2>(a, b, o, p, grid, smem, stream)
+                     : launch_one<MODE, SWAP, OUT_F32, 1>(a, b, o, p, grid, smem, stream);
 }
 
 }  // namespace cakegg

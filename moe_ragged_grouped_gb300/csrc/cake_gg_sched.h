@@ -12,6 +12,11 @@
 //    reduction may be split into chunks of `split_chunk` 64-row k-blocks; the
 //    number of splits of expert e, S_e, depends only on its row count.
 //
+// Pairs.  With pair = 2, two CTAs of a cluster take one unit together: rank r
+// computes m-tile 2 * m_unit + r (its own 128-row output tile) and both share
+// the unit's B operand (n-tile, k-range), each loading half of it for both.
+// A rank whose m-tile lies past the output computes masked garbage only.
+//
 // Order.  Experts are walked in a processing order and, inside an expert, in
 // m-tile-major order (n fastest, then split).  The weight gradient walks its
 // experts heaviest-first (most k-blocks per split first, ties by index) when
@@ -52,14 +57,16 @@ struct Geom {
     int32_t n_tiles;      // output column tiles
     int32_t m_tiles_w;    // weight gradient: output row tiles
     int32_t nkb;          // forward / data gradient: reduction k-blocks
+    int32_t pair;         // CTAs per unit (1, or 2 for a multicast pair)
 };
 
 CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
-                       int32_t swap, int32_t kchunk)
+                       int32_t swap, int32_t kchunk, int32_t pair = 1)
 {
     Geom g;
+    g.pair = pair;
     g.mode = mode;
     g.E = E;
     g.N = N;
@@ -94,11 +101,14 @@ CAKE_HD int32_t expert_splits(const Geom &g, int32_t rows)
     return nkb <= 0 ? 1 : ceil_div_i(nkb, g.kchunk);
 }
 
-// Tiles of one expert.
+// Output row tiles of the weight gradient taken per unit (pairs share a unit).
+CAKE_HD int32_t m_units_w(const Geom &g) { return ceil_div_i(g.m_tiles_w, g.pair); }
+
+// Units of one expert (a unit is one tile, or one tile per CTA of a pair).
 CAKE_HD int32_t expert_tiles(const Geom &g, int32_t rows)
 {
-    if (g.mode == kModeWgrad) return g.m_tiles_w * g.n_tiles * expert_splits(g, rows);
-    return ceil_div_i(rows, kTileM) * g.n_tiles;
+    if (g.mode == kModeWgrad) return m_units_w(g) * g.n_tiles * expert_splits(g, rows);
+    return ceil_div_i(rows, kTileM * g.pair) * g.n_tiles;
 }
 
 // Sort key of the heaviest-first walk: k-blocks in one split of the expert.
@@ -124,13 +134,14 @@ struct Tile {
     int32_t row_end;  // one past the expert's last row
     int32_t ticket;   // wgrad: output tile index e * (m_tiles_w * n_tiles) + mt * n_tiles + nt
     int64_t slot;     // wgrad split: partial slot of this split
+    bool valid;       // false for a pair rank whose tile lies past the output
 };
 
 // Tables: off[E+1] offsets; order[E] processing position -> expert;
 // pref[E+1] tile prefix in processing order; spref[E+1] split prefix by
 // expert id (weight gradient).
 CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int32_t *order,
-                         const int32_t *pref, const int32_t *spref)
+                         const int32_t *pref, const int32_t *spref, int32_t rank = 0)
 {
     // last position p with pref[p] <= t (positions of empty experts have
     // pref[p] == pref[p+1] and are never selected since t < pref[E])
@@ -152,7 +163,7 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         const int32_t s = local % S;
         const int32_t rest = local / S;
         ti.nt = rest % g.n_tiles;
-        ti.mt = rest / g.n_tiles;
+        ti.mt = (rest / g.n_tiles) * g.pair + rank;
         ti.s = s;
         ti.S = S;
         const int32_t chunk = S > 1 ? g.kchunk : nkb_e;
@@ -162,8 +173,9 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         ti.ticket = (e * g.m_tiles_w + ti.mt) * g.n_tiles + ti.nt;
         ti.slot = (static_cast<int64_t>(spref[e]) * g.m_tiles_w * g.n_tiles) +
                   static_cast<int64_t>(ti.mt * g.n_tiles + ti.nt) * S + s;
+        ti.valid = ti.mt < g.m_tiles_w;
     } else {
-        ti.mt = local / g.n_tiles;
+        ti.mt = (local / g.n_tiles) * g.pair + rank;
         ti.nt = local % g.n_tiles;
         ti.s = 0;
         ti.S = 1;
@@ -172,6 +184,7 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         ti.row0 = r0 + ti.mt * kTileM;
         ti.ticket = 0;
         ti.slot = 0;
+        ti.valid = ti.row0 < r1;
     }
     return ti;
 }

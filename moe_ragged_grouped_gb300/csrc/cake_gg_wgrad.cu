@@ -5,14 +5,15 @@
 
 namespace cakegg {
 
-cudaError_t launch_wgrad(bool out_f32, bool swap, const CUtensorMap &a, const CUtensorMap &b,
-                         const KParams &p, int grid, size_t smem, cudaStream_t stream)
+cudaError_t launch_wgrad(bool out_f32, bool swap, int pair, const CUtensorMap &a, const CUtensorMap &b,
+                         const CUtensorMap &o, const KParams &p, int grid, size_t smem, cudaStream_t stream)
 {
+    // the swapped (thin) weight gradient always runs unpaired
     if (swap)
-        return out_f32 ? launch_one<kModeWgrad, true, true>(a, b, p, grid, smem, stream)
-                       : launch_one<kModeWgrad, true, false>(a, b, p, grid, smem, stream);
-    return out_f32 ? launch_one<kModeWgrad, false, true>(a, b, p, grid, smem, stream)
-                   : launch_one<kModeWgrad, false, false>(a, b, p, grid, smem, stream);
+        return out_f32 ? launch_one<kModeWgrad, true, true, 1>(a, b, o, p, grid, smem, stream)
+                       : launch_one<kModeWgrad, true, false, 1>(a, b, o, p, grid, smem, stream);
+    return out_f32 ? launch_pair_or_single<kModeWgrad, false, true>(pair, a, b, o, p, grid, smem, stream)
+                   : launch_pair_or_single<kModeWgrad, false, false>(pair, a, b, o, p, grid, smem, stream);
 }
 
 }  // namespace cakegg
