@@ -1,0 +1,162 @@
+"""Parity at the full configured sizes, in the launch configuration the benchmark uses.
+
+Inputs are drawn on the GPU by a seeded generator (the benchmark's recipe) and
+copied to the host for the FP64 oracle, which evaluates sampled outputs one by
+one: uniform random elements plus every expert's first and last rows, tile
+edges, and (weight gradient) every expert including empty ones.  Each sample
+must satisfy the parity bound |gpu - ref| <= 2^-8 |ref| + 2^-18 L max|a| max|b|.
+
+Workloads (E experts, M routed rows, K, N):
+  dense projection   E=1, T=16384, d_in in {4096, 5120}, d_out in {48, 64, 512, 1024, 4096}
+  MoE gate_up        E=8, M=131072 balanced, K=4096, N=3072
+  MoE down           E=32, M=131072 multinomial (seed 0), K=1536, N=4096
+  skewed MoE         E=4, M=136064 Zipf(1.2) ascending with an empty expert, (K,N) = (4096,3072), (3072,4096)
+"""
+import numpy as np
+import pytest
+
+import oracle
+from moe_ragged_grouped_gb300 import build as gg_build
+from moe_ragged_grouped_gb300 import cake_gg as gg
+from moe_ragged_grouped_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    gg_build.build()
+    return gg.load_library()
+
+
+_cache = {}
+
+
+def inputs(wk):
+    """Device tensors and host bits of a workload (cached per module run)."""
+    import torch
+    if wk.name not in _cache:
+        _cache.clear()
+        torch.cuda.empty_cache()
+        X, W, G = wk.make_torch(seed=0, device="cuda")
+        bits = tuple(wl.torch_bf16_to_bits(t) for t in (X, W, G))
+        _cache[wk.name] = (X, W, G, bits)
+    return _cache[wk.name]
+
+
+def sample_rows_cols(off, n_out, rng, n=384):
+    M = int(off[-1])
+    rows = list(rng.integers(0, M, n))
+    for e in range(len(off) - 1):
+        if off[e + 1] > off[e]:
+            rows += [int(off[e]), int(off[e + 1]) - 1, min(int(off[e]) + 127, int(off[e + 1]) - 1),
+                     min(int(off[e]) + 128, int(off[e + 1]) - 1)]
+    rows = np.array(rows, np.int64)
+    cols = rng.integers(0, n_out, rows.shape[0])
+    edge = np.array([0, n_out - 1, min(63, n_out - 1), min(64, n_out - 1), min(255, n_out - 1),
+                     min(256, n_out - 1)], np.int64)
+    cols[:edge.shape[0]] = edge
+    return rows, cols
+
+
+def run_and_check(wk, pass_, out_dtype, det, rng, env=None, monkeypatch=None):
+    import torch
+    if env:
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+    X, W, G, (Xb, Wb, Gb) = inputs(wk)
+    off = wk.offsets
+    offs = torch.from_numpy(off).cuda()
+    a, b = {"fwd": (X, W), "dgrad": (G, W), "wgrad": (G, X)}[pass_]
+    out = gg.grouped_gemm(pass_, a, b, offs, out_dtype=out_dtype, deterministic=det)
+    torch.cuda.synchronize()
+    f = lambda t: float(np.abs(oracle.bf16_bits_to_f64(t)).max())
+    M = int(off[-1])
+    if pass_ == "wgrad":
+        sizes = np.diff(off)
+        es = list(rng.integers(0, wk.E, 384)) + list(range(wk.E)) * 4
+        es = np.array(es, np.int64)
+        ns = rng.integers(0, wk.N, es.shape[0])
+        ks = rng.integers(0, wk.K, es.shape[0])
+        ns[:4], ks[:4] = [0, wk.N - 1, 0, wk.N - 1], [0, wk.K - 1, wk.K - 1, 0]
+        ref = oracle.wgrad_at(Gb, Xb, off, wk.E, es, ns, ks)
+        idx = torch.from_numpy(es * wk.N * wk.K + ns * wk.K + ks).cuda()
+        got_t = out.view(-1)[idx]
+        L = sizes[es].astype(np.float64)
+        ma, mb = f(Gb[:M]), f(Xb[:M])
+    else:
+        n_out = wk.N if pass_ == "fwd" else wk.K
+        rows, cols = sample_rows_cols(off, n_out, rng)
+        if pass_ == "fwd":
+            ref = oracle.fwd_at(Xb, Wb, off, rows, cols)
+            ma, mb, L = f(Xb[:M]), f(Wb), float(wk.K)
+        else:
+            ref = oracle.dgrad_at(Gb, Wb, off, rows, cols)
+            ma, mb, L = f(Gb[:M]), f(Wb), float(wk.N)
+        idx = torch.from_numpy(rows * n_out + cols).cuda()
+        got_t = out.view(-1)[idx]
+    if got_t.dtype == torch.bfloat16:
+        got = oracle.bf16_bits_to_f64(wl.torch_bf16_to_bits(got_t))
+    else:
+        got = got_t.double().cpu().numpy()
+    tol = oracle.tolerance(ref, L, ma, mb)
+    bad = ~(np.abs(got - ref) <= tol)
+    assert not bad.any(), (f"{wk.name} {pass_} {out_dtype} det={det}: {int(bad.sum())}/{bad.size} samples "
+                           f"outside the bound; e.g. got {got[bad][:3]} ref {ref[bad][:3]}")
+    del out
+
+
+DENSE = [(4096, 48), (4096, 64), (5120, 48), (5120, 64), (4096, 512), (5120, 512),
+         (4096, 1024), (5120, 1024), (4096, 4096), (5120, 4096)]
+
+
+@pytest.mark.parametrize("d_in,d_out", DENSE)
+def test_dense_projection(d_in, d_out, monkeypatch):
+    wk = wl.dense_projection(d_in, d_out)
+    rng = np.random.default_rng(d_in + d_out)
+    run_and_check(wk, "wgrad", "fp32", 1, rng)
+    run_and_check(wk, "wgrad", "fp32", 0, rng)
+    run_and_check(wk, "fwd", "bf16", 1, rng)
+    run_and_check(wk, "dgrad", "bf16", 1, rng)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad", "wgrad"])
+def test_moe_gate_up(pass_):
+    run_and_check(wl.moe_gate_up(), pass_, "bf16", 1, np.random.default_rng(3))
+
+
+@pytest.mark.parametrize("out_dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("det,env", [(1, None), (0, None), (1, {"CAKE_GG_SPLIT_CHUNK": "16"}),
+                                     (0, {"CAKE_GG_SPLIT_CHUNK": "16"})])
+def test_moe_down_weight_gradient(out_dtype, det, env, monkeypatch):
+    run_and_check(wl.moe_down(), "wgrad", out_dtype, det, np.random.default_rng(4), env, monkeypatch)
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad", "wgrad"])
+def test_moe_skewed(transposed, pass_):
+    run_and_check(wl.moe_skewed(transposed), pass_, "bf16", 1, np.random.default_rng(5))
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad", "wgrad"])
+def test_skewed_deterministic_bitwise_runs_and_sm_caps(pass_):
+    """Deterministic mode on the skewed workload: 20 runs and 100 / 148 SM caps, all bitwise equal."""
+    import torch
+    wk = wl.moe_skewed(False)
+    X, W, G, _ = inputs(wk)
+    offs = torch.from_numpy(wk.offsets).cuda()
+    a, b = {"fwd": (X, W), "dgrad": (G, W), "wgrad": (G, X)}[pass_]
+    ref = gg.grouped_gemm(pass_, a, b, offs, out_dtype="bf16", deterministic=1)
+    M = int(wk.offsets[-1])
+    view = (lambda t: t[:M]) if pass_ != "wgrad" else (lambda t: t)
+    ref_v = view(ref).contiguous().view(torch.int16)
+    out = torch.empty_like(ref)
+    for i in range(20):
+        gg.grouped_gemm(pass_, a, b, offs, out_dtype="bf16", deterministic=1, out=out)
+        assert torch.equal(view(out).contiguous().view(torch.int16), ref_v), f"run {i}"
+    for cap in (100, 148):
+        gg.grouped_gemm(pass_, a, b, offs, out_dtype="bf16", deterministic=1, max_sms=cap, out=out)
+        assert torch.equal(view(out).contiguous().view(torch.int16), ref_v), f"max_sms={cap}"

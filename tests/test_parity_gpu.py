@@ -174,3 +174,34 @@ def test_device_detects_bad_offsets_and_recovers():
     assert ei.value.code == gg.CAKE_GG_ERR_BAD_OFFSETS
     # the context is still usable
     check_case("fwd", [100, 100], 64, 64, "bf16", 1, seed=8)
+
+
+def test_dgrad_equals_forward_with_transposed_weights():
+    """GPU vs GPU: dX = G W equals the forward pass with W'_e = W_e^T stored [E, K, N]."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs([300, 0, 200, 77], 192, 256, seed=13)
+    G, W = to_dev(Gb), to_dev(Wb)
+    Wt = W.transpose(1, 2).contiguous()
+    offs = torch.from_numpy(off).cuda()
+    dX = gg.grouped_gemm("dgrad", G, W, offs, out_dtype="fp32")
+    Yt = gg.grouped_gemm("fwd", G, Wt, offs, out_dtype="fp32")
+    M = int(off[-1])
+    a, b = dX[:M].double().cpu().numpy(), Yt[:M].double().cpu().numpy()
+    ma = float(np.abs(oracle.bf16_bits_to_f64(Gb[:M])).max())
+    mb = float(np.abs(oracle.bf16_bits_to_f64(Wb)).max())
+    assert (np.abs(a - b) <= oracle.tolerance(b, 192, ma, mb)).all()
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+def test_single_and_paired_ctas_agree_bitwise(pass_, monkeypatch):
+    """Pairing CTAs changes only how the B tile reaches shared memory, never a result bit."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs([0, 513, 1000, 130], 384, 512, seed=14)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    paired = run(pass_, X, W, G, off, "fp32", 1)
+    monkeypatch.setenv("CAKE_GG_PAIR", "0")
+    single = run(pass_, X, W, G, off, "fp32", 1)
+    M = int(off[-1])
+    if pass_ != "wgrad":
+        paired, single = paired[:M], single[:M]
+    assert torch.equal(paired.view(torch.int32), single.view(torch.int32))
