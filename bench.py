@@ -67,8 +67,9 @@ def get_workload(name):
     if name == "tiny":
         return wl.tiny()
     if name.startswith("dense_"):
-        d_in, d_out = (int(v) for v in name[len("dense_"):].split("to"))
-        return wl.dense_projection(d_in, d_out)
+        spec, _, t = name[len("dense_"):].partition("_T")
+        d_in, d_out = (int(v) for v in spec.split("to"))
+        return wl.dense_projection(d_in, d_out, int(t) if t else 16384)
     raise SystemExit(f"unknown workload {name}")
 
 

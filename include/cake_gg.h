@@ -27,17 +27,25 @@
  * data-gradient passes never split and are deterministic in both modes.
  *
  * Ownership: the caller owns every buffer (inputs, outputs, offsets,
- * workspace) and the plan.  The compute calls allocate nothing, free nothing
- * and never synchronise the host; they enqueue work on `stream` (a
- * cudaStream_t, NULL = the legacy default stream) and return.  The workspace
- * must stay allocated and unused by anyone else until the stream has run the
- * call; calls that share one workspace must be ordered on one stream.
+ * workspace) and the plan.  The compute calls allocate nothing, free nothing,
+ * launch nothing but their kernel and never synchronise the host; they
+ * enqueue work on `stream` (a cudaStream_t, NULL = the legacy default stream)
+ * and return.  The workspace must stay allocated and unused by anyone else
+ * until the stream has run the call; calls that share one workspace must be
+ * ordered on one stream.
+ *
+ * Workspace contents: fill the workspace with zeros once after allocating it
+ * (and again after a device-detected error).  Every call that ends without a
+ * device-detected error leaves it ready for the next call, so no call clears
+ * it.  Split-tile tickets are tagged with a per-call number and never need
+ * clearing.
  *
  * Errors: host-detected problems return a non-zero cake_gg_status_t and
  * enqueue nothing.  Problems only the GPU can see (bad offsets, a bounded wait
- * that expired) are written to the workspace's status word; the kernel then
- * skips its remaining work and returns (it never traps).  Output contents are
- * unspecified after any error.  cake_gg_check_status() reads the status word.
+ * that expired) are recorded in the workspace's status word, which keeps the
+ * first such error until cake_gg_check_status() reads and resets it; the
+ * kernel then skips its remaining work and returns (it never traps).  Output
+ * contents are unspecified after any error.
  */
 #ifndef CAKE_GG_H
 #define CAKE_GG_H
@@ -158,9 +166,9 @@ int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void
 int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
                           const int32_t *offsets, int out_dtype, int deterministic, void *stream);
 
-/* Synchronise `stream` and return the status word the last call that used
- * `workspace` left there (CAKE_GG_OK, _BAD_OFFSETS or _TIMEOUT), or
- * CAKE_GG_ERR_CUDA if the synchronisation itself failed. */
+/* Synchronise `stream`, return the status word of `workspace` (CAKE_GG_OK,
+ * or the first _BAD_OFFSETS / _TIMEOUT recorded by a call since the last
+ * check) and reset it to CAKE_GG_OK; CAKE_GG_ERR_CUDA if a CUDA call failed. */
 int cake_gg_check_status(const void *workspace, void *stream);
 
 /* Static, never-NULL description of a status code. */

@@ -229,9 +229,10 @@ def _torch_out_dtype(out_dtype):
 
 
 def make_workspace(plan, device):
+    """A zero-filled workspace of plan.workspace_bytes (the library expects zeros before first use)."""
     import torch
     n = max(int(plan.workspace_bytes), 256)
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def grouped_gemm(pass_, a, b, offsets, out_dtype="bf16", deterministic=True, max_sms=0, out=None,

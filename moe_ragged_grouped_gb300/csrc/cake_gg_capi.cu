@@ -1,6 +1,7 @@
 // cake_gg_capi.cu -- the C ABI of include/cake_gg.h: planning, argument
 // validation, TMA descriptor set-up and kernel launch.  Host code only.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -53,11 +54,13 @@ int env_int(const char *name, int dflt)
 // (expressed in k-block equivalents) -- returned as k-blocks per split
 // (0 = no split).  A pure function of the problem: never of the CTA count
 // a launch uses, so deterministic results do not depend on max_sms.
-int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn)
+int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn, int bk)
 {
     if (out_tiles <= 0 || kblocks_per_expert < 2 * kMinSplitChunk) return 0;
-    const double partial_kb = 2.0 * 2.0 * 1024.0 * bn / (16384.0 + 128.0 * bn);  // write + read, x2 margin
-    const double c_split = partial_kb + 4.0;
+    const double kps = bk / 64.0;
+    // partial-tile write + read (x2 margin) and the finish, in stage equivalents
+    const double partial_kb = 2.0 * 2.0 * 1024.0 * bn / ((16384.0 + 128.0 * bn) * kps);
+    const double c_split = partial_kb + 4.0 / kps;
     auto cost = [&](int64_t S) {
         const int64_t units = out_tiles * S;
         const int64_t waves = (units + kWaveCtas - 1) / kWaveCtas;
@@ -85,13 +88,26 @@ int tmem_cols_for(int bn)
 }
 
 // Byte layout of the workspace for a plan: header | tickets | partial tiles.
+// Tickets are epoch-tagged and need no clearing; the header (sticky status
+// word) and, in non-deterministic split plans, the FP32 accumulators must be
+// zero before a call, and every call that ends without a device-detected
+// error leaves them zero.
 struct WsLayout {
     uint64_t tickets_off, tickets_bytes;
     uint64_t partials_off, partials_bytes;
-    uint64_t clear_bytes;  // prefix cleared by every call
+    uint64_t zero_bytes;   // bytes from the start that must hold zeros before a call
     uint64_t total;
     bool ok;
 };
+
+std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch()
+{
+    uint32_t e = g_epoch.fetch_add(1) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1) + 1;
+    return e;
+}
 
 WsLayout ws_layout(const cake_gg_plan_t &pl)
 {
@@ -99,21 +115,22 @@ WsLayout ws_layout(const cake_gg_plan_t &pl)
     w.ok = true;
     w.tickets_off = kHeaderBytes;
     w.partials_off = kHeaderBytes;
-    w.clear_bytes = kHeaderBytes;
+    w.zero_bytes = kHeaderBytes;
     w.total = kHeaderBytes;
     if (pl.pass != CAKE_GG_WGRAD || pl.split_chunk <= 0) return w;
-    const Geom g = make_geom(kModeWgrad, pl.E, pl.N, pl.K, pl.M_max, pl.tile_n, pl.swap_ab, pl.split_chunk);
+    const Geom g = make_geom(kModeWgrad, pl.E, pl.N, pl.K, pl.M_max, pl.tile_n, pl.swap_ab, pl.split_chunk, pl.pair,
+                             pl.tile_k);
     const uint64_t tpe = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles);
     uint64_t n_tickets = 0, tile_bytes = 0, tmp = 0;
     w.ok &= mul_ok(tpe, uint64_t(pl.E), &n_tickets);
     w.ok &= mul_ok(uint64_t(kTileM) * 4u, uint64_t(pl.tile_n), &tile_bytes);
-    w.ok &= mul_ok(n_tickets, 4, &tmp);
+    w.ok &= mul_ok(n_tickets, 8, &tmp);
     w.tickets_bytes = align_up(tmp, 256);
     w.partials_off = w.tickets_off + w.tickets_bytes;
     uint64_t tiles = 0;
     if (pl.deterministic) {
         // sum over experts of ceil(rows_e / (64 * chunk)) is at most M_max / (64 * chunk) + E
-        const uint64_t splits = uint64_t(pl.M_max) / (uint64_t(kTileK) * uint64_t(pl.split_chunk)) +
+        const uint64_t splits = uint64_t(pl.M_max) / (uint64_t(pl.tile_k) * uint64_t(pl.split_chunk)) +
                                 uint64_t(pl.E) + 1;
         w.ok &= mul_ok(tpe, splits, &tiles);
     } else {
@@ -121,9 +138,9 @@ WsLayout ws_layout(const cake_gg_plan_t &pl)
     }
     w.ok &= mul_ok(tiles, tile_bytes, &w.partials_bytes);
     w.ok &= add_ok(w.partials_off, w.partials_bytes, &w.total);
-    // the deterministic partial slots are fully overwritten before they are read;
-    // the atomic accumulators must start at zero
-    w.clear_bytes = pl.deterministic ? w.partials_off : w.total;
+    // deterministic partial slots are written before they are read; the atomic
+    // accumulators must start at zero (each call's finishing CTA re-zeroes them)
+    w.zero_bytes = pl.deterministic ? kHeaderBytes : w.total;
     return w;
 }
 
@@ -189,6 +206,40 @@ int encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
     return r == CUDA_SUCCESS ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
 }
 
+// General BF16 map: dims[0] contiguous, byte strides of dims 1.. given (need not
+// increase), 128-byte swizzled boxes, zero fill outside the tensor.
+int encode_map_nd(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                  const uint32_t *box)
+{
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t bx[5], estride[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bx[i] = box[i];
+        estride[i] = 1;
+        if (i > 0) gstride[i - 1] = strides[i - 1];
+    }
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base), gdim,
+                          gstride, bx, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
+}
+
+// Atom-stacked view of a row-major [rows, width] BF16 matrix used MN-major:
+// dims {64, rows, width / 64} (the third dimension walks 64-wide atoms, 128 B
+// apart), so one box {64, 64 rows, natoms} fills natoms 8 KB atoms that lie
+// 8 KB apart in shared memory.  Needs width % 64 == 0 (no element of an atom
+// past the row's end).
+int encode_stacked(CUtensorMap *m, const void *base, uint64_t rows, uint64_t width, uint32_t box_rows,
+                   uint32_t natoms)
+{
+    if (width % 64 != 0) return CAKE_GG_ERR_UNSUPPORTED;
+    const uint64_t dims[3] = {64, rows, width / 64};
+    const uint64_t strides[2] = {width * 2, 128};
+    const uint32_t box[3] = {64, box_rows, natoms};
+    return encode_map_nd(m, base, 3, dims, strides, box);
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks shared by the three compute calls.
@@ -201,11 +252,12 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
     if (plan->E < 1 || plan->E > kMaxE || plan->N < 1 || plan->K < 1 || plan->M_max < 0 ||
         plan->M_max > INT32_MAX)
         return CAKE_GG_ERR_INVALID_ARG;
-    if (plan->tile_m != kTileM || plan->tile_k != kTileK || (plan->pair != 1 && plan->pair != 2) ||
+    if (plan->tile_m != kTileM || (plan->tile_k != 64 && plan->tile_k != 128 && plan->tile_k != 256) ||
+        (plan->tile_k != 64 && plan->pair != 1) || (plan->pair != 1 && plan->pair != 2) ||
         (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
         plan->tile_n < 64 || plan->tile_n > 256 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
-        smem_bytes_for(plan->tile_n, plan->stages) > kSmemLimit)
+        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64) > kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->N % 8 != 0 || plan->K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
     // operands with M_max rows may be null when there are no rows at all
@@ -237,7 +289,6 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     const WsLayout w = ws_layout(*plan);
     uint8_t *wsb = static_cast<uint8_t *>(ws);
 
-    if (cudaMemsetAsync(ws, 0, w.clear_bytes, stream) != cudaSuccess) return CAKE_GG_ERR_CUDA;
     if (M == 0) {
         // no rows at all: forward / data gradient write nothing, dW is zero
         if (mode == kModeWgrad) {
@@ -249,6 +300,11 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
 
     CUtensorMap ma, mb, mo;
     std::memset(&mo, 0, sizeof mo);
+    // MN-major operands through atom-stacked maps (one box per operand and stage)
+    const bool stack_ok = env_int("CAKE_GG_STACK", 1) != 0;
+    const int b_atoms = (bn / 64) / plan->pair;  // B atoms this CTA loads per stage
+    const int bk = plan->tile_k, kps = bk / 64;
+    bool stack_a = false, stack_b = false, chunk_a = false, chunk_b = false;
     const bool tma_store = env_int("CAKE_GG_TMA_STORE", 1) != 0 && !(mode == kModeWgrad && plan->swap_ab);
     if (tma_store) {
         // output boxes: 32 rows x 128 bytes (64 BF16 or 32 FP32 columns)
@@ -263,52 +319,95 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
         if (rc != CAKE_GG_OK) return rc;
     }
     if (mode == kModeFwd) {
-        const uint64_t dx[2] = {uint64_t(K), M};
-        const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
-        if ((rc = encode_map(&ma, opA, 2, dx, 64, kTileM)) != CAKE_GG_OK) return rc;
-        if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(plan->pair == 2 ? bn / 2 : bn))) != CAKE_GG_OK)
-            return rc;
+        if (kps > 1) {
+            // X as {64, M, K/64} and W as {64, N, K/64, E}: kps k-chunks per box
+            const uint64_t da[3] = {64, M, uint64_t(K) / 64};
+            const uint64_t sa_[2] = {uint64_t(K) * 2, 128};
+            const uint32_t ba[3] = {64, uint32_t(kTileM), uint32_t(kps)};
+            const uint64_t db[4] = {64, uint64_t(N), uint64_t(K) / 64, uint64_t(E)};
+            const uint64_t sb_[3] = {uint64_t(K) * 2, 128, uint64_t(N) * K * 2};
+            const uint32_t bb[4] = {64, uint32_t(bn), uint32_t(kps), 1};
+            if ((rc = encode_map_nd(&ma, opA, 3, da, sa_, ba)) != CAKE_GG_OK) return rc;
+            if ((rc = encode_map_nd(&mb, opB, 4, db, sb_, bb)) != CAKE_GG_OK) return rc;
+            chunk_a = chunk_b = true;
+        } else {
+            const uint64_t dx[2] = {uint64_t(K), M};
+            const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
+            if ((rc = encode_map(&ma, opA, 2, dx, 64, kTileM)) != CAKE_GG_OK) return rc;
+            if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(plan->pair == 2 ? bn / 2 : bn))) != CAKE_GG_OK)
+                return rc;
+        }
     } else if (mode == kModeDgrad) {
-        const uint64_t dg[2] = {uint64_t(N), M};
-        const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
-        if ((rc = encode_map(&ma, opA, 2, dg, 64, kTileM)) != CAKE_GG_OK) return rc;
-        if ((rc = encode_map(&mb, opB, 3, dw, 64, 64)) != CAKE_GG_OK) return rc;
+        if (kps > 1) {
+            // G as {64, M, N/64}: kps k-chunks per box
+            const uint64_t da[3] = {64, M, uint64_t(N) / 64};
+            const uint64_t sa_[2] = {uint64_t(N) * 2, 128};
+            const uint32_t ba[3] = {64, uint32_t(kTileM), uint32_t(kps)};
+            if ((rc = encode_map_nd(&ma, opA, 3, da, sa_, ba)) != CAKE_GG_OK) return rc;
+            chunk_a = true;
+        } else {
+            const uint64_t dg[2] = {uint64_t(N), M};
+            if ((rc = encode_map(&ma, opA, 2, dg, 64, kTileM)) != CAKE_GG_OK) return rc;
+        }
+        // W as {64, N, K/64, E}: this CTA's B atoms of a bk-row block in one box
+        if (stack_ok && K % 64 == 0) {
+            const uint64_t dims[4] = {64, uint64_t(N), uint64_t(K) / 64, uint64_t(E)};
+            const uint64_t strides[3] = {uint64_t(K) * 2, 128, uint64_t(N) * K * 2};
+            const uint32_t box[4] = {64, uint32_t(bk), uint32_t(b_atoms), 1};
+            stack_b = encode_map_nd(&mb, opB, 4, dims, strides, box) == CAKE_GG_OK;
+        }
+        if (!stack_b) {
+            const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
+            if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(bk))) != CAKE_GG_OK) return rc;
+        }
     } else {
         // opA = G [M, N], opB = X [M, K]; swapped operands put X on the MMA rows
-        const uint64_t dg[2] = {uint64_t(N), M};
-        const uint64_t dx[2] = {uint64_t(K), M};
         const void *pa = plan->swap_ab ? opB : opA;
         const void *pb = plan->swap_ab ? opA : opB;
-        if ((rc = encode_map(&ma, pa, 2, plan->swap_ab ? dx : dg, 64, 64)) != CAKE_GG_OK) return rc;
-        if ((rc = encode_map(&mb, pb, 2, plan->swap_ab ? dg : dx, 64, 64)) != CAKE_GG_OK) return rc;
+        const uint64_t wa = plan->swap_ab ? uint64_t(K) : uint64_t(N);
+        const uint64_t wb = plan->swap_ab ? uint64_t(N) : uint64_t(K);
+        if (stack_ok) {
+            stack_a = encode_stacked(&ma, pa, M, wa, uint32_t(bk), 2) == CAKE_GG_OK;
+            stack_b = encode_stacked(&mb, pb, M, wb, uint32_t(bk), uint32_t(b_atoms)) == CAKE_GG_OK;
+        }
+        const uint64_t da[2] = {wa, M};
+        const uint64_t db[2] = {wb, M};
+        if (!stack_a && (rc = encode_map(&ma, pa, 2, da, 64, uint32_t(bk))) != CAKE_GG_OK) return rc;
+        if (!stack_b && (rc = encode_map(&mb, pb, 2, db, 64, uint32_t(bk))) != CAKE_GG_OK) return rc;
     }
 
     KParams p{};
     p.offsets = offsets;
     p.out = out;
     p.status = reinterpret_cast<int32_t *>(wsb);
-    p.tickets = reinterpret_cast<int32_t *>(wsb + w.tickets_off);
+    p.tickets = reinterpret_cast<uint64_t *>(wsb + w.tickets_off);
     p.partials = reinterpret_cast<float *>(wsb + w.partials_off);
     p.M_max = plan->M_max;
     p.E = E;
     p.N = N;
     p.K = K;
     p.bn = bn;
+    p.bk = bk;
     p.stages = plan->stages;
     p.kchunk = mode == kModeWgrad ? plan->split_chunk : 0;
     p.det = plan->deterministic ? 1 : 0;
     p.tmem_cols = tmem_cols_for(bn);
     p.tma_store = tma_store ? 1 : 0;
+    p.epoch = next_epoch();
+    p.stack_a = stack_a ? 1 : 0;
+    p.stack_b = stack_b ? 1 : 0;
+    p.chunk_a = chunk_a ? 1 : 0;
+    p.chunk_b = chunk_b ? 1 : 0;
     p.debug_flags = plan->debug_flags;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
     const int P = plan->pair;
-    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P);
+    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk);
     uint64_t unit_bound;
     if (mode == kModeWgrad) {
         uint64_t splits = uint64_t(E);
-        if (p.kchunk > 0) splits = M / (uint64_t(kTileK) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
+        if (p.kchunk > 0) splits = M / (uint64_t(bk) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
         unit_bound = uint64_t(m_units_w(g)) * uint64_t(g.n_tiles) * splits;
     } else {
         unit_bound = (M / (uint64_t(kTileM) * P) + uint64_t(E) + 1) * uint64_t(g.n_tiles);
@@ -319,7 +418,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     grid -= grid % P;
     if (grid < P) grid = P;
 
-    const size_t smem = smem_bytes_for(bn, plan->stages);
+    const size_t smem = smem_bytes_for(bn, plan->stages, kps);
     cudaError_t err;
     if (mode == kModeFwd) err = launch_fwd(out_f32, P, ma, mb, mo, p, grid, smem, stream);
     else if (mode == kModeDgrad) err = launch_dgrad(out_f32, P, ma, mb, mo, p, grid, smem, stream);
@@ -376,7 +475,6 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->deterministic = deterministic ? 1 : 0;
     plan->max_sms = max_sms;
     plan->tile_m = kTileM;
-    plan->tile_k = kTileK;
     plan->pair = 1;
     plan->timeout_ns = kDefaultTimeoutNs;
 
@@ -399,9 +497,25 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->pair = (bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab)) ? 2 : 1;
     const int env_pair = env_int("CAKE_GG_PAIR", -1);
     if (env_pair == 0) plan->pair = 1;
+    // deeper stages (two 64-deep k-chunks) for the memory-bound thin shapes:
+    // one TMA box then moves 32 KB of the streamed operand, which a CTA pulls
+    // from HBM about twice as fast as 16 KB boxes
+    int32_t bk = 64;
+    if (plan->pair == 1) {
+        if (pass == CAKE_GG_FWD && N <= 64 && K % 64 == 0) bk = 128;
+        if (pass == CAKE_GG_WGRAD && plan->swap_ab) bk = 128;
+    }
+    const int env_bk = env_int("CAKE_GG_TILE_K", 0);
+    if ((env_bk == 64 || env_bk == 128 || env_bk == 256) && (plan->pair == 1 || env_bk == 64) &&
+        (env_bk == 64 || pass == CAKE_GG_WGRAD || (pass == CAKE_GG_FWD ? K : N) % 64 == 0))
+        bk = env_bk;
+    plan->tile_k = bk;
 
+    // deeper stages only while at least two of them fit
+    while (bk > 64 && smem_bytes_for(bn, 2, bk / 64) > kSmemLimit) bk /= 2;
+    plan->tile_k = bk;
     int stages = kMaxStages;
-    while (stages > 2 && smem_bytes_for(bn, stages) > kSmemLimit) --stages;
+    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64) > kSmemLimit) --stages;
     const int env_st = env_int("CAKE_GG_STAGES", 0);
     if (env_st >= 2 && env_st <= stages) stages = env_st;
     plan->stages = stages;
@@ -410,7 +524,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
         const int64_t tpe = int64_t(g.m_tiles_w) * g.n_tiles;
         if (tpe * E > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
-        plan->split_chunk = choose_split_chunk(tpe * E, (M_max / E + kTileK - 1) / kTileK, bn);
+        plan->split_chunk = choose_split_chunk(tpe * E, (M_max / E + bk - 1) / bk, bn, bk);
         const char *es = std::getenv("CAKE_GG_SPLIT_CHUNK");
         if (es && *es) {
             const int v = std::atoi(es);
@@ -460,6 +574,8 @@ int cake_gg_check_status(const void *workspace, void *stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(&st, workspace, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return CAKE_GG_ERR_CUDA;
+    // the word is sticky: reset it once read
+    if (cudaMemsetAsync(const_cast<void *>(workspace), 0, sizeof st, s) != cudaSuccess) return CAKE_GG_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return CAKE_GG_ERR_CUDA;
     return st;
 }
@@ -476,7 +592,7 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
         if (off[e + 1] < off[e]) return CAKE_GG_ERR_BAD_OFFSETS;
     const int mode = plan->pass == CAKE_GG_FWD ? kModeFwd : plan->pass == CAKE_GG_DGRAD ? kModeDgrad : kModeWgrad;
     const Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
-                             mode == kModeWgrad ? plan->split_chunk : 0, plan->pair);
+                             mode == kModeWgrad ? plan->split_chunk : 0, plan->pair, plan->tile_k);
     std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
     for (int e = 0; e < E; ++e) {
         cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
@@ -547,5 +663,9 @@ extern "C" int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, 
     int rc = check_call(plan, CAKE_GG_WGRAD, G, X, dW, offsets, out_dtype, deterministic, scratch,
                         CAKE_GG_NOALLOC_SCRATCH_BYTES);
     if (rc != CAKE_GG_OK) return rc;
+    // callers cannot reach the scratch, so each call clears what must start at zero
+    const WsLayout w = ws_layout(*plan);
+    if (cudaMemsetAsync(scratch, 0, w.zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CAKE_GG_ERR_CUDA;
     return run(plan, kModeWgrad, G, X, dW, offsets, scratch, static_cast<cudaStream_t>(stream));
 }

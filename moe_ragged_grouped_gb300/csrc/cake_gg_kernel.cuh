@@ -39,8 +39,8 @@ constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kStatusBadOffsets = 7;
 constexpr int kStatusTimeout = 8;
-constexpr uint32_t kABytes = kTileM * kTileK * 2;  // 16 KB: A tile of one stage
-constexpr uint32_t kBoxBytes = 64 * 64 * 2;        // one 64 x 64 MN-major box
+constexpr uint32_t kABytes = kTileM * kTileK * 2;  // 16 KB: A tile of one 64-deep k-chunk
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;        // one 64 x 64 MN-major box (8 KB)
 constexpr size_t kSmemOptInLimit = 232448;        // opt-in dynamic shared memory per CTA (227 KB)
 constexpr uint32_t kStagingBytes = 4 * 32 * 128;   // epilogue: 32 rows x 128 B per epilogue warp
 
@@ -48,16 +48,22 @@ struct KParams {
     const int32_t *offsets;
     void *out;
     int32_t *status;
-    int32_t *tickets;
+    uint64_t *tickets;      // per split output tile: (epoch << 32) | arrivals
     float *partials;
     int64_t M_max;
     int32_t E, N, K;
     int32_t bn;
+    int32_t bk;             // reduction elements per stage: 64 * k-chunks per stage
     int32_t stages;
     int32_t kchunk;
     int32_t det;
     int32_t tmem_cols;
     int32_t tma_store;      // epilogue through shared memory + TMA tensor stores
+    uint32_t epoch;         // per-call tag of the tickets (never 0)
+    int32_t stack_a;        // MN-major A through an atom-stacked map: one box per stage
+    int32_t stack_b;        // MN-major B likewise (all of this CTA's B atoms in one box)
+    int32_t chunk_a;        // K-major A through a {64, rows, K/64} map: one box per stage
+    int32_t chunk_b;        // K-major B (forward W) through a {64, N, K/64, E} map
     int32_t debug_flags;
     uint64_t timeout_ns;
 };
@@ -79,11 +85,15 @@ struct __align__(16) Ctrl {
     int32_t spref[kMaxE + 1];
 };
 
-__host__ __device__ constexpr uint32_t stage_bytes_for(int bn) { return kABytes + uint32_t(bn) * 128u; }
-
-__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages)
+// A stage holds kps = bk / 64 k-chunks of A (128 rows) and B (bn rows).
+__host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1)
 {
-    return 1024 + size_t(stages) * stage_bytes_for(bn) + kStagingBytes + sizeof(Ctrl);
+    return uint32_t(kps) * (kABytes + uint32_t(bn) * 128u);
+}
+
+__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps = 1)
+{
+    return 1024 + size_t(stages) * stage_bytes_for(bn, kps) + kStagingBytes + sizeof(Ctrl);
 }
 
 // Bounded wait on one mbarrier phase, by every lane of the calling warp;
@@ -134,6 +144,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     while (!mbar_try_wait(bar, parity)) {
         if (global_timer_ns() - t0 > limit_ns) return;
     }
+}
+
+// Ticket of a split output tile: returns how many splits of this call (epoch)
+// arrived before this one.  A ticket word left by an earlier call carries
+// another epoch and counts as zero, so tickets never need clearing.  At most
+// S concurrent updates race, so the CAS loop ends within S tries (bounded at
+// 64; on exhaustion the caller is told it is not last and the status word
+// records a timeout).
+__device__ __forceinline__ uint32_t ticket_arrive(uint64_t *t, uint32_t epoch, int32_t *status)
+{
+    uint64_t cur = *reinterpret_cast<volatile uint64_t *>(t);
+    for (int i = 0; i < 64; ++i) {
+        const bool same = uint32_t(cur >> 32) == epoch;
+        const uint64_t nxt = same ? cur + 1 : ((uint64_t(epoch) << 32) | 1ull);
+        const uint64_t prev = atomic_cas_acq_rel_gpu_u64(t, cur, nxt);
+        if (prev == cur) return same ? uint32_t(cur & 0xffffffffu) : 0u;
+        cur = prev;
+    }
+    atomicCAS(status, 0, kStatusTimeout);
+    return 0xffffffffu;
 }
 
 // ---------------------------------------------------------------- epilogue stores
@@ -196,7 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *ring = smem_raw + (ring_u32 - raw_u32);
-    const uint32_t stage_bytes = stage_bytes_for(p.bn);
+    const int kps = p.bk / kTileK;                 // k-chunks per stage
+    const uint32_t stage_bytes = stage_bytes_for(p.bn, kps);
+    const uint32_t a_bytes = uint32_t(kps) * kABytes;
+    const uint32_t atom_a = uint32_t(kps) * kBoxBytes;   // MN-major: 64 x bk atom
+    const uint32_t atom_b = atom_a;
+    const uint32_t chunk_b = uint32_t(p.bn) * 128u;      // K-major B: one 64-deep chunk of bn rows
     uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
     Ctrl *c = reinterpret_cast<Ctrl *>(staging + kStagingBytes);
 
@@ -204,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int E = p.E;
-    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR);
+    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk);
     // a pair (cluster of 2) shares each unit; rank r computes m-tile 2 * unit + r
     const int rank = PAIR == 2 ? int(cluster_ctarank()) : 0;
     const int64_t unit0 = blockIdx.x / PAIR;
@@ -323,43 +358,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t fb = smem_u32(&c->full[stage]);
                     const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
-                    const uint32_t sb = sa + kABytes;
+                    const uint32_t sb = sa + a_bytes;
                     mbar_arrive_expect_tx(fb, tx);
                     const bool drop = (p.debug_flags & 1) && blockIdx.x == 0 && issued == 0;
-                    if (!drop && PAIR == 2) {
-                        // own A; half of the shared B, multicast to both CTAs of the pair
+                    if (!drop) {
+                        // B atoms this CTA loads: all of them, or its half of a pair's (multicast)
                         const int nb = p.bn / 64;
+                        const int jb0 = PAIR == 2 ? rank * nb / 2 : 0;
+                        const int jb1 = PAIR == 2 ? (rank + 1) * nb / 2 : nb;
+                        const int32_t k0 = kb * p.bk;      // first reduction element of the stage
                         if (MODE == kModeWgrad) {
-                            const int32_t r = ti.row0 + kb * kTileK;
-                            tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
-                            tma_load_2d(sa + kBoxBytes, &mapA, fb, ti.mt * kTileM + 64, r);
-                            for (int j = rank * nb / 2; j < (rank + 1) * nb / 2; ++j)
-                                tma_load_2d_mc(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j, r, kPairMask);
-                        } else if (MODE == kModeFwd) {
-                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
-                            tma_load_3d_mc(sb + uint32_t(rank) * uint32_t(p.bn / 2) * 128u, &mapB, fb, kb * kTileK,
-                                           ti.nt * p.bn + rank * (p.bn / 2), ti.e, kPairMask);
+                            const int32_t r = ti.row0 + k0;
+                            // A: 128 MN x bk rows as two 64-wide atoms
+                            if (p.stack_a) {
+                                tma_load_3d(sa, &mapA, fb, 0, r, ti.mt * 2);
+                            } else {
+                                tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
+                                tma_load_2d(sa + atom_a, &mapA, fb, ti.mt * kTileM + 64, r);
+                            }
+                            if (p.stack_b) {
+                                if (PAIR == 2)
+                                    tma_load_3d_mc(sb + jb0 * atom_b, &mapB, fb, 0, r, ti.nt * nb + jb0, kPairMask);
+                                else
+                                    tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb);
+                            } else {
+                                for (int j = jb0; j < jb1; ++j) {
+                                    if (PAIR == 2)
+                                        tma_load_2d_mc(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, r, kPairMask);
+                                    else
+                                        tma_load_2d(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, r);
+                                }
+                            }
                         } else {
-                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
-                            for (int j = rank * nb / 2; j < (rank + 1) * nb / 2; ++j)
-                                tma_load_3d_mc(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j, kb * kTileK,
-                                               ti.e, kPairMask);
-                        }
-                    } else if (!drop) {
-                        if (MODE == kModeWgrad) {
-                            const int32_t r = ti.row0 + kb * kTileK;
-                            tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
-                            tma_load_2d(sa + kBoxBytes, &mapA, fb, ti.mt * kTileM + 64, r);
-                            for (int j = 0; j < p.bn / 64; ++j)
-                                tma_load_2d(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j, r);
-                        } else if (MODE == kModeFwd) {
-                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
-                            tma_load_3d(sb, &mapB, fb, kb * kTileK, ti.nt * p.bn, ti.e);
-                        } else {
-                            tma_load_2d(sa, &mapA, fb, kb * kTileK, ti.row0);
-                            for (int j = 0; j < p.bn / 64; ++j)
-                                tma_load_3d(sb + j * kBoxBytes, &mapB, fb, ti.nt * p.bn + 64 * j,
-                                            kb * kTileK, ti.e);
+                            // K-major A (X or G): all k-chunks of the stage in one box when chunked
+                            if (p.chunk_a) tma_load_3d(sa, &mapA, fb, 0, ti.row0, kb * kps);
+                            else tma_load_2d(sa, &mapA, fb, k0, ti.row0);
+                            if (MODE == kModeFwd) {
+                                if (PAIR == 2)
+                                    tma_load_3d_mc(sb + uint32_t(rank) * uint32_t(p.bn / 2) * 128u, &mapB, fb, k0,
+                                                   ti.nt * p.bn + rank * (p.bn / 2), ti.e, kPairMask);
+                                else if (p.chunk_b)
+                                    tma_load_4d(sb, &mapB, fb, 0, ti.nt * p.bn, kb * kps, ti.e);
+                                else
+                                    tma_load_3d(sb, &mapB, fb, k0, ti.nt * p.bn, ti.e);
+                            } else if (p.stack_b) {
+                                // W as {64, N, K/64, E}: this CTA's atoms of one bk-row block in one box
+                                if (PAIR == 2)
+                                    tma_load_4d_mc(sb + jb0 * atom_b, &mapB, fb, 0, k0, ti.nt * nb + jb0, ti.e,
+                                                   kPairMask);
+                                else
+                                    tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb, ti.e);
+                            } else {
+                                for (int j = jb0; j < jb1; ++j) {
+                                    if (PAIR == 2)
+                                        tma_load_3d_mc(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, k0, ti.e,
+                                                       kPairMask);
+                                    else
+                                        tma_load_3d(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, k0, ti.e);
+                                }
+                            }
                         }
                     }
                     ++issued;
@@ -404,21 +461,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
-                const uint32_t sb = sa + kABytes;
+                const uint32_t sb = sa + a_bytes;
                 if (MODE == kModeWgrad) {
-                    // rows of the last k-block past the expert's end belong to the
-                    // next expert (or lie beyond M_max): zero them in both operands
-                    const int32_t valid = ti.row_end - (ti.row0 + kb * kTileK);
-                    if (valid < kTileK) {
-                        const int nbox = 2 + p.bn / 64;
-                        const int nrow = kTileK - valid;
-                        const int chunks = nbox * nrow * 8;
+                    // rows of the expert's last stage past its end belong to the next
+                    // expert (or lie beyond M_max): zero them in every atom of A and B
+                    const int32_t valid = ti.row_end - (ti.row0 + kb * p.bk);
+                    if (valid < p.bk) {
+                        const int natoms = 2 + p.bn / 64;
+                        const int nrow = p.bk - valid;
+                        const int chunks = natoms * nrow * 8;
                         for (int i = lane; i < chunks; i += 32) {
-                            const int box = i / (nrow * 8);
-                            const int rem = i - box * nrow * 8;
+                            const int atom = i / (nrow * 8);
+                            const int rem = i - atom * nrow * 8;
                             const int row = valid + rem / 8;
                             const int ch = rem % 8;
-                            uint8_t *dst = ring + (sa - ring_u32) + box * kBoxBytes + row * 128 + ch * 16;
+                            const uint32_t base = atom < 2 ? sa + uint32_t(atom) * atom_a : sb + uint32_t(atom - 2) * atom_b;
+                            uint8_t *dst = ring + (base - ring_u32) + row * 128 + ch * 16;
                             *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
@@ -427,12 +485,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     tc_fence_after_sync();
-#pragma unroll
-                    for (int ks = 0; ks < kTileK / 16; ++ks) {
-                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + ks * 2048, kBoxBytes, 1024)
-                                                 : smem_desc_sw128(sa + ks * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + ks * 2048, kBoxBytes, 1024)
-                                                 : smem_desc_sw128(sb + ks * 32, 16, 1024);
+                    const int nks = p.bk / 16;
+                    for (int ks = 0; ks < nks; ++ks) {
+                        // MN-major: 16 rows further down each atom; K-major: 32 bytes along
+                        // a 128-byte row, k-chunk by k-chunk
+                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + ks * 2048, atom_a, 1024)
+                                                 : smem_desc_sw128(sa + (ks >> 2) * kABytes + (ks & 3) * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + ks * 2048, atom_b, 1024)
+                                                 : smem_desc_sw128(sb + (ks >> 2) * chunk_b + (ks & 3) * 32, 16, 1024);
                         umma_bf16(d_tmem, ad, bd, idesc, (kb > ti.kb0 || ks > 0) ? 1u : 0u);
                     }
                     if (PAIR == 2) umma_commit_mc(smem_u32(&c->empty[stage]), kPairMask);
@@ -604,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, 128);
                 if (etid == 0) {
                     __threadfence();
-                    const int old = atomic_add_acq_rel_gpu(p.tickets + ti.ticket, 1);
-                    c->last_flag = (old == ti.S - 1);
+                    const uint32_t before = ticket_arrive(p.tickets + ti.ticket, p.epoch, p.status);
+                    c->last_flag = (before == uint32_t(ti.S - 1));
                 }
                 __syncwarp();
                 named_bar_sync(1, 128);
@@ -613,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, 128);  // everyone read last_flag before the next tile rewrites it
                 if (last) {
                     __threadfence();
-                    const float *base0 = p.det ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
+                    float *base0 = p.det ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
                                                : slot_ptr;
                     const int nsum = p.det ? ti.S : 1;
                     const int64_t slot_stride = int64_t(kTileM) * p.bn;
@@ -629,6 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (s0 + u < nsum)
                                         b[u][j] = __ldcg(reinterpret_cast<const float4 *>(
                                             base0 + (s0 + u) * slot_stride + (int64_t(c4 + j) * kTileM + lrow) * 4));
+                            if (!p.det) {
+                                // the atomic accumulator is read only here: leave it zeroed for the next call
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    *reinterpret_cast<float4 *>(base0 + (int64_t(c4 + j) * kTileM + lrow) * 4) =
+                                        make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
                                 if (s0 + u < nsum) {

@@ -85,6 +85,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                               int32_t c0, int32_t c1, int32_t c2, int32_t c3, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(mask)
+        : "memory");
+}
+
 // Multicast variants: the box lands at the same shared-memory offset in every
 // CTA of `mask` (this cluster), each of whose mbarrier at `bar`'s offset gets
 // the complete-tx.
@@ -299,10 +319,12 @@ __device__ __forceinline__ void red_add_v4_f32(float *addr, float a, float b, fl
                  : "memory");
 }
 
-__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v)
+__device__ __forceinline__ uint64_t atomic_cas_acq_rel_gpu_u64(uint64_t *addr, uint64_t cmp, uint64_t val)
 {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+    uint64_t old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                 : "=l"(old)
+                 : "l"(addr), "l"(cmp), "l"(val)
                  : "memory");
     return old;
 }

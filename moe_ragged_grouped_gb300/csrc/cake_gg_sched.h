@@ -41,7 +41,7 @@ constexpr int kModeDgrad = 1;
 constexpr int kModeWgrad = 2;
 
 constexpr int kTileM = 128;     // MMA rows (TMEM lanes)
-constexpr int kTileK = 64;      // reduction elements per stage (one 128-byte swizzle row)
+constexpr int kTileK = 64;      // reduction elements of one k-chunk (one 128-byte swizzle row)
 constexpr int kMaxE = 1024;     // experts supported by the on-chip tables
 constexpr int kSortMaxE = 256;  // heaviest-first walk only up to this many experts
 
@@ -58,15 +58,17 @@ struct Geom {
     int32_t m_tiles_w;    // weight gradient: output row tiles
     int32_t nkb;          // forward / data gradient: reduction k-blocks
     int32_t pair;         // CTAs per unit (1, or 2 for a multicast pair)
+    int32_t bk;           // reduction elements per pipeline stage (64 * k-chunks per stage)
 };
 
 CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
-                       int32_t swap, int32_t kchunk, int32_t pair = 1)
+                       int32_t swap, int32_t kchunk, int32_t pair = 1, int32_t bk = kTileK)
 {
     Geom g;
     g.pair = pair;
+    g.bk = bk;
     g.mode = mode;
     g.E = E;
     g.N = N;
@@ -77,11 +79,11 @@ CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_
     g.kchunk = kchunk;
     if (mode == kModeFwd) {
         g.n_tiles = ceil_div_i(N, bn);
-        g.nkb = ceil_div_i(K, kTileK);
+        g.nkb = ceil_div_i(K, bk);
         g.m_tiles_w = 0;
     } else if (mode == kModeDgrad) {
         g.n_tiles = ceil_div_i(K, bn);
-        g.nkb = ceil_div_i(N, kTileK);
+        g.nkb = ceil_div_i(N, bk);
         g.m_tiles_w = 0;
     } else {
         const int32_t mdim = swap ? K : N;
@@ -97,7 +99,7 @@ CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_
 CAKE_HD int32_t expert_splits(const Geom &g, int32_t rows)
 {
     if (g.mode != kModeWgrad || g.kchunk <= 0) return 1;
-    const int32_t nkb = ceil_div_i(rows, kTileK);
+    const int32_t nkb = ceil_div_i(rows, g.bk);
     return nkb <= 0 ? 1 : ceil_div_i(nkb, g.kchunk);
 }
 
@@ -114,7 +116,7 @@ CAKE_HD int32_t expert_tiles(const Geom &g, int32_t rows)
 // Sort key of the heaviest-first walk: k-blocks in one split of the expert.
 CAKE_HD int32_t expert_cost(const Geom &g, int32_t rows)
 {
-    const int32_t nkb = ceil_div_i(rows, kTileK);
+    const int32_t nkb = ceil_div_i(rows, g.bk);
     const int32_t s = expert_splits(g, rows);
     return ceil_div_i(nkb, s);
 }
@@ -128,7 +130,7 @@ struct Tile {
     int32_t nt;       // output column tile
     int32_t s;        // split index
     int32_t S;        // splits of this output tile
-    int32_t kb0;      // first k-block (64 reduction elements each)
+    int32_t kb0;      // first k-block (g.bk reduction elements each)
     int32_t kb1;      // one past the last k-block
     int32_t row0;     // fwd/dgrad: first row of the tile; wgrad: first row of the expert
     int32_t row_end;  // one past the expert's last row
@@ -159,7 +161,7 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
     ti.row_end = r1;
     if (g.mode == kModeWgrad) {
         const int32_t S = expert_splits(g, r1 - r0);
-        const int32_t nkb_e = ceil_div_i(r1 - r0, kTileK);
+        const int32_t nkb_e = ceil_div_i(r1 - r0, g.bk);
         const int32_t s = local % S;
         const int32_t rest = local / S;
         ti.nt = rest % g.n_tiles;

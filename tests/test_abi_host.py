@@ -130,7 +130,7 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
             lst.sort()
             S = lst[0][1]
             assert [x[0] for x in lst] == list(range(S))
-            nkb = -(-(off[e + 1] - off[e]) // 64)
+            nkb = -(-(off[e + 1] - off[e]) // plan.tile_k)
             # contiguous partition of [0, nkb)
             assert lst[0][2] == 0 and lst[-1][3] == nkb
             for a, b in zip(lst, lst[1:]):
@@ -142,7 +142,7 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
         costs = []
         for e, mt, nt, s, S, kb0, kb1, _ in tiles:
             if not costs or costs[-1][0] != e:
-                costs.append((e, -(-(-(-(off[e + 1] - off[e]) // 64)) // S)))
+                costs.append((e, -(-(-(-(off[e + 1] - off[e]) // plan.tile_k)) // S)))
         seq = [c for _, c in costs]
         assert seq == sorted(seq, reverse=True)
     return plan, tiles

@@ -205,3 +205,21 @@ def test_single_and_paired_ctas_agree_bitwise(pass_, monkeypatch):
     if pass_ != "wgrad":
         paired, single = paired[:M], single[:M]
     assert torch.equal(paired.view(torch.int32), single.view(torch.int32))
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("tile_k", ["128", "256"])
+def test_deeper_stages(pass_, tile_k, monkeypatch):
+    """Stages holding two or four 64-deep k-chunks (single CTAs), on ragged groups with a NaN tail."""
+    monkeypatch.setenv("CAKE_GG_PAIR", "0")
+    monkeypatch.setenv("CAKE_GG_TILE_K", tile_k)
+    check_case(pass_, [0, 1, 129, 300, 0, 77], 192, 320, "fp32", 1, seed=15, extra_rows=9)
+    if pass_ == "wgrad":
+        monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "2")
+        check_case(pass_, [2000, 0, 517], 128, 256, "fp32", 1, seed=16, extra_rows=5)
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_thin_forward(out_dtype):
+    """Dense projection forward with d_out = 48: deeper stages, one 64-wide column tile."""
+    check_case("fwd", [1000], 48, 512, out_dtype, 1, seed=17, extra_rows=3)
