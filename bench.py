@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass-events", type=int, default=1,
+                    help="1: per-pass CUDA events inside the timed region; 0: none there (kernels back to "
+                         "back), per-pass times from a separate loop")
     ap.add_argument("--graph", action="store_true",
                     help="replay each pass from a captured CUDA graph (removes host launch overhead)")
     return ap.parse_args()
@@ -253,15 +256,25 @@ def run_ours(args, wk):
         sampler.mark_start()
     start.record(stream)
     for i in range(args.steps):
-        evs[i][0].record(stream)
+        if args.pass_events:
+            evs[i][0].record(stream)
         for j, p in enumerate(passes):
             run_pass(p)
-            evs[i][j + 1].record(stream)
+            if args.pass_events:
+                evs[i][j + 1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     if sampler:
         sampler.mark_end()
     elapsed_ms = start.elapsed_time(end)
+    if not args.pass_events:
+        # per-pass breakdown from a separate loop
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            for j, p in enumerate(passes):
+                run_pass(p)
+                evs[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
     per_pass_ms = {p: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                    for j, p in enumerate(passes)}
     if dist is not None:
@@ -344,7 +357,8 @@ def run_ours(args, wk):
                        "parallelism": f"replicas x{ws}",
                        "launch": "cuda-graph replay per pass" if args.graph else "eager",
                        "plans": {p: {k: v for k, v in plans[p].as_dict().items()
-                                     if k in ("tile_n", "stages", "swap_ab", "split_chunk")} for p in passes}},
+                                     if k in ("tile_n", "tile_k", "stages", "pair", "swap_ab", "split_chunk",
+                                              "staging_bufs")} for p in passes}},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": len(passes) * args.steps, "clocks": clocks}
     if dist is not None:

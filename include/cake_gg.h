@@ -102,7 +102,10 @@ typedef struct cake_gg_plan {
     int32_t debug_flags;     /* test-only fault injection; 0 in normal use          */
     uint64_t timeout_ns;     /* limit of every in-kernel wait (default 2 s)         */
     uint64_t workspace_bytes;/* bytes of workspace the compute call needs           */
-    int32_t reserved[8];
+    int32_t staging_bufs;    /* epilogue staging buffers per warp (1 or 2)          */
+    int32_t cluster_splits;  /* weight gradient: >0 = that many splits per tile run as
+                                one cluster and reduce on chip (no workspace partials) */
+    int32_t reserved[6];
 } cake_gg_plan_t;
 
 /* Debug flag (tests only): CTA 0 arms its first pipeline stage but issues no

@@ -62,7 +62,9 @@ class CakeGGPlan(ctypes.Structure):
         ("debug_flags", ctypes.c_int32),
         ("timeout_ns", ctypes.c_uint64),
         ("workspace_bytes", ctypes.c_uint64),
-        ("reserved", ctypes.c_int32 * 8),
+        ("staging_bufs", ctypes.c_int32),
+        ("cluster_splits", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
     def as_dict(self):

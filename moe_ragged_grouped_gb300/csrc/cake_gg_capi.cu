@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kWaveCtas = 152;              // GB300 SMs: the wave size the split model assumes
 constexpr int kMinSplitChunk = 4;           // k-blocks (256 rows) per split at least
+constexpr int kMaxClusterSplit = 8;         // portable cluster size
 constexpr size_t kSmemLimit = kSmemOptInLimit;
 constexpr uint64_t kHeaderBytes = 256;      // workspace: status word and padding
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -117,7 +118,7 @@ WsLayout ws_layout(const cake_gg_plan_t &pl)
     w.partials_off = kHeaderBytes;
     w.zero_bytes = kHeaderBytes;
     w.total = kHeaderBytes;
-    if (pl.pass != CAKE_GG_WGRAD || pl.split_chunk <= 0) return w;
+    if (pl.pass != CAKE_GG_WGRAD || pl.split_chunk <= 0 || pl.cluster_splits > 0) return w;
     const Geom g = make_geom(kModeWgrad, pl.E, pl.N, pl.K, pl.M_max, pl.tile_n, pl.swap_ab, pl.split_chunk, pl.pair,
                              pl.tile_k);
     const uint64_t tpe = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles);
@@ -253,11 +254,15 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         plan->M_max > INT32_MAX)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->tile_m != kTileM || (plan->tile_k != 64 && plan->tile_k != 128 && plan->tile_k != 256) ||
-        (plan->tile_k != 64 && plan->pair != 1) || (plan->pair != 1 && plan->pair != 2) ||
+        (plan->tile_k != 64 && plan->pair != 1 && pass == CAKE_GG_FWD) || (plan->pair != 1 && plan->pair != 2) ||
         (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
         plan->tile_n < 64 || plan->tile_n > 256 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
-        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64) > kSmemLimit)
+        (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
+        plan->cluster_splits > kMaxClusterSplit ||
+        (plan->cluster_splits > 0 && (pass != CAKE_GG_WGRAD || !plan->swap_ab || plan->pair != 1)) ||
+        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits) >
+            kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->N % 8 != 0 || plan->K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
     // operands with M_max rows may be null when there are no rows at all
@@ -398,12 +403,16 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.stack_b = stack_b ? 1 : 0;
     p.chunk_a = chunk_a ? 1 : 0;
     p.chunk_b = chunk_b ? 1 : 0;
+    p.pdl = env_int("CAKE_GG_PDL", 1) != 0 ? 1 : 0;
+    p.staging_bufs = plan->staging_bufs;
+    p.csplit = mode == kModeWgrad ? plan->cluster_splits : 0;
     p.debug_flags = plan->debug_flags;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
     const int P = plan->pair;
-    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk);
+    const int CL = p.csplit > 0 ? p.csplit : P;   // CTAs per cluster (one unit per cluster)
+    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk, p.csplit);
     uint64_t unit_bound;
     if (mode == kModeWgrad) {
         uint64_t splits = uint64_t(E);
@@ -414,11 +423,11 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     }
     int grid = dev.sms;
     if (plan->max_sms > 0 && plan->max_sms < grid) grid = plan->max_sms;
-    if (unit_bound * P < uint64_t(grid)) grid = int(unit_bound * P);
-    grid -= grid % P;
-    if (grid < P) grid = P;
+    if (unit_bound * CL < uint64_t(grid)) grid = int(unit_bound * CL);
+    grid -= grid % CL;
+    if (grid < CL) grid = CL;
 
-    const size_t smem = smem_bytes_for(bn, plan->stages, kps);
+    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs, p.csplit);
     cudaError_t err;
     if (mode == kModeFwd) err = launch_fwd(out_f32, P, ma, mb, mo, p, grid, smem, stream);
     else if (mode == kModeDgrad) err = launch_dgrad(out_f32, P, ma, mb, mo, p, grid, smem, stream);
@@ -506,7 +515,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         if (pass == CAKE_GG_WGRAD && plan->swap_ab) bk = 128;
     }
     const int env_bk = env_int("CAKE_GG_TILE_K", 0);
-    if ((env_bk == 64 || env_bk == 128 || env_bk == 256) && (plan->pair == 1 || env_bk == 64) &&
+    if ((env_bk == 64 || env_bk == 128 || env_bk == 256) && (plan->pair == 1 || env_bk == 64 || pass != CAKE_GG_FWD) &&
         (env_bk == 64 || pass == CAKE_GG_WGRAD || (pass == CAKE_GG_FWD ? K : N) % 64 == 0))
         bk = env_bk;
     plan->tile_k = bk;
@@ -514,12 +523,6 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // deeper stages only while at least two of them fit
     while (bk > 64 && smem_bytes_for(bn, 2, bk / 64) > kSmemLimit) bk /= 2;
     plan->tile_k = bk;
-    int stages = kMaxStages;
-    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64) > kSmemLimit) --stages;
-    const int env_st = env_int("CAKE_GG_STAGES", 0);
-    if (env_st >= 2 && env_st <= stages) stages = env_st;
-    plan->stages = stages;
-
     if (pass == CAKE_GG_WGRAD) {
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
         const int64_t tpe = int64_t(g.m_tiles_w) * g.n_tiles;
@@ -530,7 +533,48 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
             const int v = std::atoi(es);
             if (v >= 0) plan->split_chunk = v;
         }
+        // thin weight gradients reduce their splits on chip: the splits of a tile
+        // run as one cluster and sum their partials through distributed shared
+        // memory (no workspace partials, no tickets)
+        if (plan->swap_ab && plan->pair == 1 && plan->split_chunk > 0) {
+            const int64_t kbe = (M_max / E + bk - 1) / bk;
+            const int64_t S = (kbe + plan->split_chunk - 1) / plan->split_chunk;
+            if (S >= 2 && S <= kMaxClusterSplit) {
+                plan->cluster_splits = int32_t(S);
+                plan->split_chunk = 0;
+            }
+        }
+        const int env_cs = env_int("CAKE_GG_CSPLIT", -1);
+        if (env_cs == 0 && plan->cluster_splits > 0) {
+            plan->split_chunk = int32_t(((M_max / E + bk - 1) / bk + plan->cluster_splits - 1) / plan->cluster_splits);
+            plan->cluster_splits = 0;
+        } else if (env_cs >= 2 && env_cs <= kMaxClusterSplit && plan->swap_ab && plan->pair == 1) {
+            plan->cluster_splits = env_cs;
+            plan->split_chunk = 0;
+        }
     }
+    const int csp = plan->cluster_splits;
+    int stages = kMaxStages;
+    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64, 1, csp) > kSmemLimit) --stages;
+    // a short reduction per tile (thin data gradient / forward) makes the
+    // epilogue the critical path: trade ring depth for double-buffered staging
+    const int32_t red_len = pass == CAKE_GG_FWD ? K : pass == CAKE_GG_DGRAD ? N : 1 << 30;
+    int staging_bufs = 1;
+    if ((red_len + bk - 1) / bk <= 4) {
+        int st2 = stages;
+        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp) > kSmemLimit) --st2;
+        if (smem_bytes_for(bn, st2, bk / 64, 2, csp) <= kSmemLimit) {
+            staging_bufs = 2;
+            stages = st2;
+        }
+    }
+    const int env_sb = env_int("CAKE_GG_STAGING_BUFS", 0);
+    if (env_sb == 1) staging_bufs = 1;
+    plan->staging_bufs = staging_bufs;
+    const int env_st = env_int("CAKE_GG_STAGES", 0);
+    if (env_st >= 2 && env_st <= stages) stages = env_st;
+    plan->stages = stages;
+
     const WsLayout w = ws_layout(*plan);
     if (!w.ok) return CAKE_GG_ERR_OVERFLOW;
     plan->workspace_bytes = w.total;
@@ -592,7 +636,8 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
         if (off[e + 1] < off[e]) return CAKE_GG_ERR_BAD_OFFSETS;
     const int mode = plan->pass == CAKE_GG_FWD ? kModeFwd : plan->pass == CAKE_GG_DGRAD ? kModeDgrad : kModeWgrad;
     const Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
-                             mode == kModeWgrad ? plan->split_chunk : 0, plan->pair, plan->tile_k);
+                             mode == kModeWgrad ? plan->split_chunk : 0, plan->pair, plan->tile_k,
+                             mode == kModeWgrad ? plan->cluster_splits : 0);
     std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
     for (int e = 0; e < E; ++e) {
         cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
@@ -610,7 +655,8 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
     const int64_t units = pref[E];
     int64_t n = 0;
     for (int64_t t = 0; t < units; ++t) {
-        for (int r = 0; r < g.pair; ++r) {
+        const int ranks = g.csplit > 0 ? g.csplit : g.pair;
+        for (int r = 0; r < ranks; ++r) {
             const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data(), r);
             if (!ti.valid) continue;
             if (n < capacity) {

@@ -37,12 +37,13 @@ namespace cakegg {
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
+constexpr int kMaxCsplit = 8;   // largest cluster split (portable cluster size)
 constexpr int kStatusBadOffsets = 7;
 constexpr int kStatusTimeout = 8;
 constexpr uint32_t kABytes = kTileM * kTileK * 2;  // 16 KB: A tile of one 64-deep k-chunk
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;        // one 64 x 64 MN-major box (8 KB)
 constexpr size_t kSmemOptInLimit = 232448;        // opt-in dynamic shared memory per CTA (227 KB)
-constexpr uint32_t kStagingBytes = 4 * 32 * 128;   // epilogue: 32 rows x 128 B per epilogue warp
+constexpr uint32_t kStagingBytes = 4 * 32 * 128;   // epilogue: 32 rows x 128 B per epilogue warp and buffer
 
 struct KParams {
     const int32_t *offsets;
@@ -64,6 +65,9 @@ struct KParams {
     int32_t stack_b;        // MN-major B likewise (all of this CTA's B atoms in one box)
     int32_t chunk_a;        // K-major A through a {64, rows, K/64} map: one box per stage
     int32_t chunk_b;        // K-major B (forward W) through a {64, N, K/64, E} map
+    int32_t pdl;            // launched with programmatic stream serialization
+    int32_t staging_bufs;   // epilogue staging buffers per warp (1 or 2)
+    int32_t csplit;         // weight gradient: splits per tile reduced on chip by one cluster (0 = off)
     int32_t debug_flags;
     uint64_t timeout_ns;
 };
@@ -75,6 +79,8 @@ struct __align__(16) Ctrl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t red_ready;     // cluster split: all csplit partials of the current tile are in place
+    uint64_t red_consumed;  // cluster split: every peer has read this CTA's partial
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t bad;
@@ -91,9 +97,17 @@ __host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1)
     return uint32_t(kps) * (kABytes + uint32_t(bn) * 128u);
 }
 
-__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps = 1)
+// Cluster split: one FP32 partial tile (128 rows x bn) per CTA, read by its peers.
+__host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit)
 {
-    return 1024 + size_t(stages) * stage_bytes_for(bn, kps) + kStagingBytes + sizeof(Ctrl);
+    return csplit > 0 ? size_t(kTileM) * size_t(bn) * 4u : 0u;
+}
+
+__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps = 1, int staging_bufs = 1,
+                                                    int csplit = 0)
+{
+    return 1024 + size_t(stages) * stage_bytes_for(bn, kps) + size_t(staging_bufs) * kStagingBytes +
+           csplit_bytes_for(bn, csplit) + sizeof(Ctrl);
 }
 
 // Bounded wait on one mbarrier phase, by every lane of the calling warp;
@@ -106,6 +120,27 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctrl *c
         const uint64_t t0 = global_timer_ns();
         while (true) {
             for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait(bar, parity);
+            if (ok) break;
+            if (*reinterpret_cast<volatile int32_t *>(&c->abort_flag)) break;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                *reinterpret_cast<volatile int32_t *>(&c->abort_flag) = 1;
+                atomicCAS(p.status, 0, kStatusTimeout);
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded warp-uniform wait with cluster-scope acquire (barriers that peers
+// arrive on remotely).
+__device__ __forceinline__ bool cluster_wait(uint32_t bar, uint32_t parity, Ctrl *c, const KParams &p)
+{
+    bool ok = mbar_try_wait_cluster(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait_cluster(bar, parity);
             if (ok) break;
             if (*reinterpret_cast<volatile int32_t *>(&c->abort_flag)) break;
             if (global_timer_ns() - t0 > p.timeout_ns) {
@@ -212,6 +247,24 @@ __device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
     else static_cast<uint16_t *>(out)[idx] = f32_to_bf16_rn(v);
 }
 
+// All MMAs of one stage: 4 * KPS k-steps of 16.  Descriptors are built once
+// per stage and advanced by adding (byte offset >> 4) to the 14-bit start
+// address field (shared-memory addresses stay below 2^18, so no carry).
+// MN-major operands step 16 rows (2 KB) down their atoms; K-major operands
+// step 32 bytes along the 128-byte row, then to the next 64-deep k-chunk.
+template <int KPS, bool A_MN, bool B_MN>
+__device__ __forceinline__ void issue_stage_mmas(uint32_t d_tmem, uint64_t ad0, uint64_t bd0, uint32_t idesc,
+                                                 bool first, uint32_t chunk_b)
+{
+#pragma unroll
+    for (int ks = 0; ks < 4 * KPS; ++ks) {
+        const uint32_t aoff = A_MN ? uint32_t(ks) * 2048u : uint32_t(ks >> 2) * kABytes + uint32_t(ks & 3) * 32u;
+        const uint32_t boff = B_MN ? uint32_t(ks) * 2048u : uint32_t(ks >> 2) * chunk_b + uint32_t(ks & 3) * 32u;
+        umma_bf16(d_tmem, ad0 + uint64_t(aoff >> 4), bd0 + uint64_t(boff >> 4), idesc,
+                  (!first || ks > 0) ? 1u : 0u);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int MODE, bool SWAP, bool OUT_F32, int PAIR>
@@ -221,6 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     constexpr bool A_MN = (MODE == kModeWgrad);
     constexpr bool B_MN = (MODE != kModeFwd);
+
+    // previous kernels in the stream may still be finishing: touch no global
+    // memory before they complete; let the next kernel start launching now
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -233,90 +291,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t atom_b = atom_a;
     const uint32_t chunk_b = uint32_t(p.bn) * 128u;      // K-major B: one 64-deep chunk of bn rows
     uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
-    Ctrl *c = reinterpret_cast<Ctrl *>(staging + kStagingBytes);
+    float *red_buf = reinterpret_cast<float *>(staging + size_t(p.staging_bufs) * kStagingBytes);
+    Ctrl *c = reinterpret_cast<Ctrl *>(reinterpret_cast<uint8_t *>(red_buf) + csplit_bytes_for(p.bn, p.csplit));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int E = p.E;
-    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk);
-    // a pair (cluster of 2) shares each unit; rank r computes m-tile 2 * unit + r
-    const int rank = PAIR == 2 ? int(cluster_ctarank()) : 0;
-    const int64_t unit0 = blockIdx.x / PAIR;
-    const int64_t unit_step = gridDim.x / PAIR;
+    const int csplit = MODE == kModeWgrad ? p.csplit : 0;
+    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit);
+    // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + r
+    // with one B tile; a cluster split (csplit CTAs) computes one tile, rank r
+    // taking the r-th chunk of its reduction
+    const int cl = PAIR == 2 ? 2 : (csplit > 0 ? csplit : 1);
+    const int rank = cl > 1 ? int(cluster_ctarank()) : 0;
+    const int64_t unit0 = blockIdx.x / cl;
+    const int64_t unit_step = gridDim.x / cl;
     constexpr uint16_t kPairMask = 0x3;
 
-    // ---- setup: offsets, validation, walk tables (temporaries in the ring) ----
-    int32_t *t_cnt = reinterpret_cast<int32_t *>(ring);
-    int32_t *t_cost = t_cnt + kMaxE;
+    // ---- setup: offsets, validation, walk tables; TMEM and barriers in parallel ----
     if (tid == 0) {
         c->abort_flag = 0;
         c->bad = 0;
-    }
-    for (int i = tid; i <= E; i += kThreads) c->off[i] = p.offsets[i];
-    __syncthreads();
-    for (int e = tid; e < E; e += kThreads) {
-        const int32_t a = c->off[e], b = c->off[e + 1];
-        if ((e == 0 && a != 0) || b < a || (e == E - 1 && int64_t(b) > p.M_max)) c->bad = 1;
-        const int32_t rows = b - a;
-        t_cnt[e] = expert_tiles(g, rows < 0 ? 0 : rows);
-        t_cost[e] = expert_cost(g, rows < 0 ? 0 : rows);
-    }
-    __syncthreads();
-    if (c->bad) {
-        if (tid == 0) atomicCAS(p.status, 0, kStatusBadOffsets);
-        return;
-    }
-    if (walk_is_sorted(g)) {
-        for (int e = tid; e < E; e += kThreads) {
-            const int32_t ce = t_cost[e];
-            int32_t rank = 0;
-            for (int j = 0; j < E; ++j) {
-                const int32_t cj = t_cost[j];
-                rank += (cj > ce) || (cj == ce && j < e);
-            }
-            c->order[rank] = e;
-        }
-    } else {
-        for (int e = tid; e < E; e += kThreads) c->order[e] = e;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // exclusive prefix sums by one warp: tiles in processing order, splits by expert id
-        const int per = (E + 31) / 32;
-        const int b0 = lane * per;
-        int32_t sum_t = 0, sum_s = 0;
-        for (int i = b0; i < b0 + per && i < E; ++i) {
-            sum_t += t_cnt[c->order[i]];
-            sum_s += expert_splits(g, c->off[i + 1] - c->off[i]);
-        }
-        int32_t inc_t = sum_t, inc_s = sum_s;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int32_t ot = __shfl_up_sync(0xffffffffu, inc_t, d);
-            const int32_t os = __shfl_up_sync(0xffffffffu, inc_s, d);
-            if (lane >= d) {
-                inc_t += ot;
-                inc_s += os;
-            }
-        }
-        int32_t run_t = inc_t - sum_t, run_s = inc_s - sum_s;
-        for (int i = b0; i < b0 + per && i < E; ++i) {
-            c->pref[i] = run_t;
-            c->spref[i] = run_s;
-            run_t += t_cnt[c->order[i]];
-            run_s += expert_splits(g, c->off[i + 1] - c->off[i]);
-        }
-        if (lane == 31) {
-            c->pref[E] = inc_t;
-            c->spref[E] = inc_s;
-        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&c->tmem_base), uint32_t(p.tmem_cols));
         tmem_relinquish();
     }
-    if (tid == 0) {
+    if (tid == 64) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_u32(&c->full[s]), 1);
             mbar_init(smem_u32(&c->empty[s]), PAIR);  // both CTAs' MMAs read a shared stage
@@ -326,13 +328,136 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&c->tempty[a]), 4);
         }
         mbar_init(smem_u32(&c->drain), 1);
+        if (csplit > 0) {
+            mbar_init(smem_u32(&c->red_ready), uint32_t(csplit));
+            mbar_init(smem_u32(&c->red_consumed), uint32_t(csplit));
+        }
         fence_barrier_init();
+    }
+    if (E <= 32) {
+        // one warp builds every table: lane e holds expert e
+        if (warp == 0) {
+            const uint32_t full_mask = 0xffffffffu;
+            const int e = lane;
+            int32_t a = 0, b = 0;
+            if (e < E) {
+                a = p.offsets[e];
+                b = p.offsets[e + 1];
+            }
+            const bool badl = e < E && ((e == 0 && a != 0) || b < a || (e == E - 1 && int64_t(b) > p.M_max));
+            if (__any_sync(full_mask, badl) && lane == 0) c->bad = 1;
+            const int32_t rows = b - a > 0 ? b - a : 0;
+            const int32_t cnt = e < E ? expert_tiles(g, rows) : 0;
+            const int32_t cost = e < E ? expert_cost(g, rows) : 0;
+            const int32_t spl = e < E ? expert_splits(g, rows) : 0;
+            if (e < E) c->off[e] = a;
+            if (e == E - 1) c->off[E] = b;
+            int32_t rank = e;
+            if (walk_is_sorted(g)) {
+                rank = 0;
+                for (int j = 0; j < E; ++j) {
+                    const int32_t cj = __shfl_sync(full_mask, cost, j);
+                    rank += (cj > cost) || (cj == cost && j < e);
+                }
+            }
+            if (e < E) c->order[rank] = e;
+            __syncwarp();
+            const int32_t op = lane < E ? c->order[lane] : 0;
+            int32_t cnt_p = __shfl_sync(full_mask, cnt, op);
+            if (lane >= E) cnt_p = 0;
+            int32_t inc_t = cnt_p, inc_s = spl;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t ot = __shfl_up_sync(full_mask, inc_t, d);
+                const int32_t os = __shfl_up_sync(full_mask, inc_s, d);
+                if (lane >= d) {
+                    inc_t += ot;
+                    inc_s += os;
+                }
+            }
+            if (lane < E) {
+                c->pref[lane] = inc_t - cnt_p;
+                c->spref[lane] = inc_s - spl;
+            }
+            if (lane == 31) {
+                c->pref[E] = inc_t;
+                c->spref[E] = inc_s;
+            }
+        }
+    } else {
+        // block-wide build for many experts (temporaries in the ring)
+        int32_t *t_cnt = reinterpret_cast<int32_t *>(ring);
+        int32_t *t_cost = t_cnt + kMaxE;
+        for (int i = tid; i <= E; i += kThreads) c->off[i] = p.offsets[i];
+        __syncthreads();
+        for (int e = tid; e < E; e += kThreads) {
+            const int32_t a = c->off[e], b = c->off[e + 1];
+            if ((e == 0 && a != 0) || b < a || (e == E - 1 && int64_t(b) > p.M_max)) c->bad = 1;
+            const int32_t rows = b - a;
+            t_cnt[e] = expert_tiles(g, rows < 0 ? 0 : rows);
+            t_cost[e] = expert_cost(g, rows < 0 ? 0 : rows);
+        }
+        __syncthreads();
+        if (walk_is_sorted(g)) {
+            for (int e = tid; e < E; e += kThreads) {
+                const int32_t ce = t_cost[e];
+                int32_t rank = 0;
+                for (int j = 0; j < E; ++j) {
+                    const int32_t cj = t_cost[j];
+                    rank += (cj > ce) || (cj == ce && j < e);
+                }
+                c->order[rank] = e;
+            }
+        } else {
+            for (int e = tid; e < E; e += kThreads) c->order[e] = e;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive prefix sums by one warp: tiles in processing order, splits by expert id
+            const int per = (E + 31) / 32;
+            const int b0 = lane * per;
+            int32_t sum_t = 0, sum_s = 0;
+            for (int i = b0; i < b0 + per && i < E; ++i) {
+                sum_t += t_cnt[c->order[i]];
+                sum_s += expert_splits(g, c->off[i + 1] - c->off[i]);
+            }
+            int32_t inc_t = sum_t, inc_s = sum_s;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t ot = __shfl_up_sync(0xffffffffu, inc_t, d);
+                const int32_t os = __shfl_up_sync(0xffffffffu, inc_s, d);
+                if (lane >= d) {
+                    inc_t += ot;
+                    inc_s += os;
+                }
+            }
+            int32_t run_t = inc_t - sum_t, run_s = inc_s - sum_s;
+            for (int i = b0; i < b0 + per && i < E; ++i) {
+                c->pref[i] = run_t;
+                c->spref[i] = run_s;
+                run_t += t_cnt[c->order[i]];
+                run_s += expert_splits(g, c->off[i + 1] - c->off[i]);
+            }
+            if (lane == 31) {
+                c->pref[E] = inc_t;
+                c->spref[E] = inc_s;
+            }
+        }
     }
     // the set-up temporaries in the ring are overwritten by TMA (async proxy) later
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
-    if (PAIR == 2) cluster_sync_all();  // the peer's barriers exist before any multicast reaches them
+    if (c->bad) {
+        // every CTA (and every CTA of a cluster) sees the same offsets and leaves here
+        if (tid == 0) atomicCAS(p.status, 0, kStatusBadOffsets);
+        if (warp == 1) {
+            tc_fence_after_sync();
+            tmem_dealloc(c->tmem_base, uint32_t(p.tmem_cols));
+        }
+        return;
+    }
+    if (cl > 1) cluster_sync_all();  // peers' barriers exist before any multicast or remote arrive reaches them
     tc_fence_after_sync();
 
     const int64_t total = c->pref[E];
@@ -485,16 +610,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     tc_fence_after_sync();
-                    const int nks = p.bk / 16;
-                    for (int ks = 0; ks < nks; ++ks) {
-                        // MN-major: 16 rows further down each atom; K-major: 32 bytes along
-                        // a 128-byte row, k-chunk by k-chunk
-                        const uint64_t ad = A_MN ? smem_desc_sw128(sa + ks * 2048, atom_a, 1024)
-                                                 : smem_desc_sw128(sa + (ks >> 2) * kABytes + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bd = B_MN ? smem_desc_sw128(sb + ks * 2048, atom_b, 1024)
-                                                 : smem_desc_sw128(sb + (ks >> 2) * chunk_b + (ks & 3) * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb > ti.kb0 || ks > 0) ? 1u : 0u);
-                    }
+                    const uint64_t ad0 = A_MN ? smem_desc_sw128(sa, atom_a, 1024) : smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t bd0 = B_MN ? smem_desc_sw128(sb, atom_b, 1024) : smem_desc_sw128(sb, 16, 1024);
+                    const bool first = kb == ti.kb0;
+                    if (kps == 1) issue_stage_mmas<1, A_MN, B_MN>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                    else if (kps == 2) issue_stage_mmas<2, A_MN, B_MN>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                    else issue_stage_mmas<4, A_MN, B_MN>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                     if (PAIR == 2) umma_commit_mc(smem_u32(&c->empty[stage]), kPairMask);
                     else umma_commit(smem_u32(&c->empty[stage]));
                 }
@@ -522,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lrow = q * 32 + lane;    // tile row held by this thread
         const int etid = tid - 64;         // 0..127
         int it = 0;
+        int cs_it = 0;                     // cluster-split tiles reduced so far
         for (int64_t t = unit0; t < total; t += unit_step, ++it) {
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
@@ -565,6 +687,96 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (cols_valid > p.bn) cols_valid = p.bn;
             const bool row_ok = lrow < rows_valid;
 
+            if (csplit > 0) {
+                // ---- cluster split: partial in shared memory, reduced through DSMEM ----
+                // my previous partial must have been read by every peer
+                if (cs_it > 0) {
+                    bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t((cs_it - 1) & 1), c, p);
+                    if (!named_bar_and(1, 128, okc)) break;
+                }
+                for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                    float v[32];
+                    if (empty_tile) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                    } else {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_row + uint32_t(c0), r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    }
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        *reinterpret_cast<float4 *>(red_buf + (((c0 >> 2) + j4) * kTileM + lrow) * 4) =
+                            make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&c->tempty[acc]));
+                // publish: every peer may read my partial
+                named_bar_sync(1, 128);
+                if (etid == 0) {
+                    fence_acq_rel_cluster();
+                    for (int j = 0; j < csplit; ++j) mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), j));
+                }
+                bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
+                if (!named_bar_and(1, 128, okr)) break;
+                // my slice of float4 columns, summed over the splits in split order
+                const int nq = p.bn / 4;
+                const int per = (nq + csplit - 1) / csplit;
+                const int q0 = rank * per;
+                const int q1 = q0 + per < nq ? q0 + per : nq;
+                const uint32_t my_buf = smem_u32(red_buf);
+                // two float4 columns x up to kMaxCsplit splits in flight per batch
+                // (compile-time indices keep them in registers); then the splits are
+                // summed in order s = 0, 1, ..., csplit - 1
+                for (int qc = q0; qc < q1; qc += 2) {
+                    float4 b4[2][kMaxCsplit];
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                        for (int s_ = 0; s_ < kMaxCsplit; ++s_)
+                            if (s_ < csplit && qc + jj < q1)
+                                b4[jj][s_] = ld_shared_cluster_f4(map_to_cta(my_buf, uint32_t(s_)) +
+                                                                  uint32_t(((qc + jj) * kTileM + lrow) * 16));
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        if (qc + jj >= q1) continue;
+                        float4 acc = b4[jj][0];
+#pragma unroll
+                        for (int s_ = 1; s_ < kMaxCsplit; ++s_) {
+                            if (s_ < csplit) {
+                                acc.x += b4[jj][s_].x;
+                                acc.y += b4[jj][s_].y;
+                                acc.z += b4[jj][s_].z;
+                                acc.w += b4[jj][s_].w;
+                            }
+                        }
+                        const int col = (qc + jj) * 4;
+                        if (row_ok && col < cols_valid && ti.valid) {
+                            const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const int64_t idx = SWAP ? out_base + int64_t(col + q4) * ld + lrow
+                                                         : out_base + int64_t(lrow) * ld + col + q4;
+                                store_scalar<OUT_F32>(p.out, idx, vv[q4]);
+                            }
+                        }
+                    }
+                }
+                // done reading the peers' partials (a cluster's last unit needs no
+                // signal: the teardown cluster barrier keeps every peer alive)
+                if (t + unit_step < total) {
+                    named_bar_sync(1, 128);
+                    if (etid == 0)
+                        for (int j = 0; j < csplit; ++j)
+                            mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_consumed), j));
+                }
+                ++cs_it;
+                continue;
+            }
+
             float *slot_ptr = nullptr;
             if (split) {
                 slot_ptr = p.det ? p.partials + ti.slot * int64_t(kTileM) * p.bn
@@ -578,9 +790,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   (MODE == kModeWgrad ? q * 32 < rows_valid : q * 32 + 32 <= rows_valid);
             if (tma_path) {
                 constexpr int CW = OUT_F32 ? 32 : 64;  // columns per 128-byte row
-                uint8_t *stg = staging + q * 4096;
-                const uint32_t stg_u32 = smem_u32(stg);
+                int buf = 0;
                 for (int c0 = 0; c0 < p.bn; c0 += CW) {
+                    // this warp's staging buffers alternate when there are two
+                    uint8_t *stg = staging + (size_t(buf) * 4 + q) * 4096;
+                    const uint32_t stg_u32 = smem_u32(stg);
                     uint32_t w[32];
                     if (empty_tile) {
 #pragma unroll
@@ -599,7 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
                         }
                     }
-                    if (lane == 0) bulk_wait_read_all();  // previous store has read the buffer
+                    if (lane == 0) {
+                        // the store that last used this buffer has read it
+                        if (p.staging_bufs == 2) bulk_wait_read_but_one();
+                        else bulk_wait_read_all();
+                    }
                     __syncwarp();
                     uint8_t *rowp = stg + lane * 128;
 #pragma unroll
@@ -617,6 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_commit_group();
                     }
                     __syncwarp();
+                    if (p.staging_bufs == 2) buf ^= 1;
                 }
             }
             for (int c0 = 0; c0 < p.bn && !tma_path; c0 += 32) {
@@ -748,8 +967,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
-    // no CTA leaves while its peer may still multicast into it or arrive on its barriers
-    if (PAIR == 2) cluster_sync_all();
+    // no CTA leaves while a peer may still multicast into it, read its shared
+    // memory or arrive on its barriers
+    if (cl > 1) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, uint32_t(p.tmem_cols));

@@ -34,23 +34,32 @@ cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         attr_set[dev] = true;
     }
     if (smem > kSmemOptInLimit) return cudaErrorInvalidValue;
-    if (PAIR == 1) {
-        kern<<<grid, kThreads, smem, stream>>>(a, b, o, p);
-        return cudaGetLastError();
-    }
-    if (grid % PAIR != 0) return cudaErrorInvalidValue;
+    // clusters: a CTA pair, or the CTAs of a cluster split
+    const int cluster = PAIR == 2 ? 2 : (p.csplit > 0 ? p.csplit : 1);
+    if (grid % cluster != 0) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = PAIR;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (p.pdl) {
+        // programmatic dependent launch: this grid may start while the previous
+        // kernel in the stream finishes (the kernel waits before touching memory)
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, a, b, o, p);
 }
 

@@ -59,16 +59,19 @@ struct Geom {
     int32_t nkb;          // forward / data gradient: reduction k-blocks
     int32_t pair;         // CTAs per unit (1, or 2 for a multicast pair)
     int32_t bk;           // reduction elements per pipeline stage (64 * k-chunks per stage)
+    int32_t csplit;       // weight gradient: splits of a tile run by one cluster (0 = off)
 };
 
 CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
-                       int32_t swap, int32_t kchunk, int32_t pair = 1, int32_t bk = kTileK)
+                       int32_t swap, int32_t kchunk, int32_t pair = 1, int32_t bk = kTileK,
+                       int32_t csplit = 0)
 {
     Geom g;
     g.pair = pair;
     g.bk = bk;
+    g.csplit = csplit;
     g.mode = mode;
     g.E = E;
     g.N = N;
@@ -96,8 +99,11 @@ CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_
 }
 
 // Splits of an expert with `rows` rows (weight gradient); 1 when unsplit or empty.
+// With cluster splits every tile has csplit splits, one per CTA of a cluster,
+// walked as a single unit.
 CAKE_HD int32_t expert_splits(const Geom &g, int32_t rows)
 {
+    if (g.mode == kModeWgrad && g.csplit > 0) return g.csplit;
     if (g.mode != kModeWgrad || g.kchunk <= 0) return 1;
     const int32_t nkb = ceil_div_i(rows, g.bk);
     return nkb <= 0 ? 1 : ceil_div_i(nkb, g.kchunk);
@@ -109,7 +115,7 @@ CAKE_HD int32_t m_units_w(const Geom &g) { return ceil_div_i(g.m_tiles_w, g.pair
 // Units of one expert (a unit is one tile, or one tile per CTA of a pair).
 CAKE_HD int32_t expert_tiles(const Geom &g, int32_t rows)
 {
-    if (g.mode == kModeWgrad) return m_units_w(g) * g.n_tiles * expert_splits(g, rows);
+    if (g.mode == kModeWgrad) return m_units_w(g) * g.n_tiles * (g.csplit > 0 ? 1 : expert_splits(g, rows));
     return ceil_div_i(rows, kTileM * g.pair) * g.n_tiles;
 }
 
@@ -159,7 +165,23 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
     const int32_t r1 = off[e + 1];
     ti.e = e;
     ti.row_end = r1;
-    if (g.mode == kModeWgrad) {
+    if (g.mode == kModeWgrad && g.csplit > 0) {
+        // one unit per output tile; cluster rank r takes the r-th of csplit
+        // contiguous k-block chunks (possibly empty for a short expert)
+        const int32_t S = g.csplit;
+        const int32_t nkb_e = ceil_div_i(r1 - r0, g.bk);
+        const int32_t chunk = ceil_div_i(nkb_e, S);
+        ti.nt = local % g.n_tiles;
+        ti.mt = local / g.n_tiles;
+        ti.s = rank;
+        ti.S = S;
+        ti.kb0 = rank * chunk < nkb_e ? rank * chunk : nkb_e;
+        ti.kb1 = (rank + 1) * chunk < nkb_e ? (rank + 1) * chunk : nkb_e;
+        ti.row0 = r0;
+        ti.ticket = (e * g.m_tiles_w + ti.mt) * g.n_tiles + ti.nt;
+        ti.slot = 0;
+        ti.valid = ti.mt < g.m_tiles_w;
+    } else if (g.mode == kModeWgrad) {
         const int32_t S = expert_splits(g, r1 - r0);
         const int32_t nkb_e = ceil_div_i(r1 - r0, g.bk);
         const int32_t s = local % S;

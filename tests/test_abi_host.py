@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_plan_struct_layout_matches_header():
-    # 6 int32, int64, 10 int32, 2 uint64, 8 int32 reserved
+    # 6 int32, int64, 10 int32, 2 uint64, staging_bufs + 7 int32 reserved
     assert ctypes.sizeof(gg.CakeGGPlan) == 120
     assert gg.CakeGGPlan.M_max.offset == 24
     assert gg.CakeGGPlan.timeout_ns.offset == 72
@@ -94,7 +94,7 @@ def test_plan_choices_do_not_depend_on_max_sms(pass_, shape):
 
 def test_thin_weight_gradient_swaps_and_splits():
     p = gg.cake_gg_plan("wgrad", 1, 16384, 48, 4096, "fp32", 1)
-    assert p.swap_ab == 1 and p.tile_n == 64 and p.split_chunk > 0
+    assert p.swap_ab == 1 and p.tile_n == 64 and (p.split_chunk > 0 or p.cluster_splits > 1)
     q = gg.cake_gg_plan("wgrad", 8, 131072, 3072, 4096, "bf16", 1)
     assert q.swap_ab == 0 and q.split_chunk == 0 and q.workspace_bytes == 256
 
@@ -134,7 +134,8 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
             # contiguous partition of [0, nkb)
             assert lst[0][2] == 0 and lst[-1][3] == nkb
             for a, b in zip(lst, lst[1:]):
-                assert a[3] == b[2] and b[2] < b[3]
+                # cluster splits give every tile csplit ranks; trailing ones may be empty
+                assert a[3] == b[2] and (b[2] < b[3] or plan.cluster_splits > 0)
             assert len({x[4] for x in lst}) == 1
             cover[e, mt * bm:min((mt + 1) * bm, mdim), nt * bn:min((nt + 1) * bn, ndim)] += 1
         assert (cover == 1).all()
@@ -164,8 +165,13 @@ def test_tile_walk_split_partitions():
 
 def test_tile_walk_thin_swap():
     plan, tiles = _check_walk_coverage("wgrad", [16384], N=48, K=4096)
-    assert plan.swap_ab == 1
+    assert plan.swap_ab == 1 and plan.cluster_splits >= 2 and plan.workspace_bytes == 256
     assert len({(t[1], t[2]) for t in tiles}) == 32
+    assert len(tiles) == 32 * plan.cluster_splits
+
+
+def test_tile_walk_cluster_split_with_small_and_empty_experts():
+    _check_walk_coverage("wgrad", [0, 100, 3000, 65, 1], N=48, K=512, env={"CAKE_GG_CSPLIT": "4"})
 
 
 def test_tile_walk_rejects_bad_offsets():

@@ -223,3 +223,19 @@ def test_deeper_stages(pass_, tile_k, monkeypatch):
 def test_thin_forward(out_dtype):
     """Dense projection forward with d_out = 48: deeper stages, one 64-wide column tile."""
     check_case("fwd", [1000], 48, 512, out_dtype, 1, seed=17, extra_rows=3)
+
+
+@pytest.mark.parametrize("csplit", ["2", "5", "8"])
+@pytest.mark.parametrize("det,out_dtype", [(1, "fp32"), (0, "bf16")])
+def test_cluster_split_weight_gradient(csplit, det, out_dtype, monkeypatch):
+    """Thin weight gradient whose splits run as one cluster and reduce through distributed
+    shared memory: experts empty, shorter than one stage, and long."""
+    monkeypatch.setenv("CAKE_GG_CSPLIT", csplit)
+    check_case("wgrad", [0, 100, 3000, 65, 1], 48, 512, out_dtype, det, seed=18, extra_rows=6)
+
+
+@pytest.mark.parametrize("det", [1, 0])
+def test_thin_weight_gradient_through_workspace_slots(det, monkeypatch):
+    """The same thin shape with the cluster reduction disabled: partials through the workspace."""
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "0")
+    check_case("wgrad", [3000], 48, 512, "fp32", det, seed=3, extra_rows=5)
