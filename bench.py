@@ -254,20 +254,25 @@ def run_ours(args, wk):
     torch.cuda.synchronize(dev)
     if sampler:
         sampler.mark_start()
+    # one pass per step: the whole timed region is that kernel's launches, back
+    # to back; several passes: events between them (inside the timed region)
+    pass_events = args.pass_events and len(passes) > 1
     start.record(stream)
     for i in range(args.steps):
-        if args.pass_events:
+        if pass_events:
             evs[i][0].record(stream)
         for j, p in enumerate(passes):
             run_pass(p)
-            if args.pass_events:
+            if pass_events:
                 evs[i][j + 1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     if sampler:
         sampler.mark_end()
     elapsed_ms = start.elapsed_time(end)
-    if not args.pass_events:
+    if len(passes) == 1:
+        per_pass_ms = {passes[0]: elapsed_ms / args.steps}
+    elif not pass_events:
         # per-pass breakdown from a separate loop
         for i in range(args.steps):
             evs[i][0].record(stream)
@@ -275,8 +280,9 @@ def run_ours(args, wk):
                 run_pass(p)
                 evs[i][j + 1].record(stream)
         torch.cuda.synchronize(dev)
-    per_pass_ms = {p: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
-                   for j, p in enumerate(passes)}
+    if len(passes) > 1:
+        per_pass_ms = {p: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                       for j, p in enumerate(passes)}
     if dist is not None:
         dist.barrier()
         t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
@@ -333,14 +339,28 @@ def run_ours(args, wk):
     # ---- roofline of the dominant kernel ----
     peaks = measured_peaks()
     dom = max(per_pass_ms, key=per_pass_ms.get)
-    achieved = wk.flops(1) / (per_pass_ms[dom] * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
-    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic_for(wk.name, dom, od, det),
-                "kernel": f"cake_gg_kernel<{dom}>",
-                "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-                "per_pass_ms": {p: round(v, 4) for p, v in per_pass_ms.items()},
-                "per_pass_tflops": {p: round(wk.flops(1) / (v * 1e-3) / 1e12, 1) for p, v in per_pass_ms.items()}}
+    obytes = 4 if od == "fp32" else 2
+    dom_s = per_pass_ms[dom] * 1e-3
+    flop_pass, bytes_pass = wk.flops(1), wk.algorithmic_bytes(dom, obytes)
+    # the pass is memory-bound when its arithmetic intensity is below the measured ridge point
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    traffic = traffic_for(wk.name, dom, od, det)
+    if flop_pass / bytes_pass < ridge:
+        achieved, peak = bytes_pass / dom_s / 1e9, peaks["hbm_gbs"]
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "peak_source": f"{peaks['source']} hbm_gbs (copy)"}
+    else:
+        achieved, peak = flop_pass / dom_s / 1e12, peaks["bf16_tflops"]
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
+    roofline.update({"frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": int(bytes_pass), "flop": int(flop_pass),
+                     "kernel": f"cake_gg_kernel<{dom}>",
+                     "per_pass_ms": {p: round(v, 4) for p, v in per_pass_ms.items()},
+                     "per_pass_tflops": {p: round(flop_pass / (v * 1e-3) / 1e12, 1)
+                                         for p, v in per_pass_ms.items()},
+                     "per_pass_gbs": {p: round(wk.algorithmic_bytes(p, obytes) / (v * 1e-3) / 1e9, 1)
+                                      for p, v in per_pass_ms.items()}})
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -275,11 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool A_MN = (MODE == kModeWgrad);
     constexpr bool B_MN = (MODE != kModeFwd);
 
-    // previous kernels in the stream may still be finishing: touch no global
-    // memory before they complete; let the next kernel start launching now
-    grid_dependency_wait();
-    grid_launch_dependents();
-
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -309,10 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t unit_step = gridDim.x / cl;
     constexpr uint16_t kPairMask = 0x3;
 
-    // ---- setup: offsets, validation, walk tables; TMEM and barriers in parallel ----
+    // ---- setup, part 1: TMEM, barriers and tensor maps (no global loads) ----
+    // runs while the previous kernel in the stream may still be finishing; the
+    // offsets are only pulled into L2 (a prefetch returns no value, so it
+    // cannot observe them before that kernel's writes)
+    if (warp == 0 && lane * 32 <= E) prefetch_l2(p.offsets + lane * 32);
     if (tid == 0) {
         c->abort_flag = 0;
         c->bad = 0;
+        tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB);
+        if (p.tma_store) tma_prefetch_desc(&mapOut);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&c->tmem_base), uint32_t(p.tmem_cols));
@@ -334,6 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_barrier_init();
     }
+
+    // ---- setup, part 2: offsets, validation, walk tables ----
+    // the previous kernel's writes are visible from here on; the next kernel may
+    // start its own part 1
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (E <= 32) {
         // one warp builds every table: lane e holds expert e
         if (warp == 0) {
@@ -457,7 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return;
     }
-    if (cl > 1) cluster_sync_all();  // peers' barriers exist before any multicast or remote arrive reaches them
+    // peers' barriers must exist before a multicast or a remote arrive reaches
+    // them: warps that reach into peers (all of a pair; the epilogue of a
+    // cluster split) wait here, the others only at teardown
+    const bool early_wait = PAIR == 2 || warp >= 2;
+    if (cl > 1) {
+        cluster_arrive_relaxed();
+        if (early_wait) cluster_wait_acquire();
+    }
     tc_fence_after_sync();
 
     const int64_t total = c->pref[E];
@@ -467,8 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ======================= TMA producer =======================
         if (lane == 0) {
-            tma_prefetch_desc(&mapA);
-            tma_prefetch_desc(&mapB);
             const uint32_t tx = stage_bytes;
             int stage = 0;
             uint32_t phase = 0;
@@ -694,7 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t((cs_it - 1) & 1), c, p);
                     if (!named_bar_and(1, 128, okc)) break;
                 }
-                for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                // only the float4 columns that reach the output travel
+                const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
+                for (int c0 = 0; c0 < 4 * nq; c0 += 32) {
                     float v[32];
                     if (empty_tile) {
 #pragma unroll
@@ -714,17 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&c->tempty[acc]));
-                // publish: every peer may read my partial
+                // publish: every peer may read my partial (the epilogue barrier
+                // orders the other threads' stores before this thread's
+                // cluster-scope release arrivals)
                 named_bar_sync(1, 128);
-                if (etid == 0) {
-                    fence_acq_rel_cluster();
+                if (etid == 0)
                     for (int j = 0; j < csplit; ++j) mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), j));
-                }
                 bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
                 if (!named_bar_and(1, 128, okr)) break;
                 // my slice of float4 columns, summed over the splits in split order
-                const int nq = p.bn / 4;
-                const int per = (nq + csplit - 1) / csplit;
+                const int cs = csplit > 0 ? csplit : 1;  // (csplit > 0 here; keeps the division well-defined)
+                const int per = (nq + cs - 1) / cs;
                 const int q0 = rank * per;
                 const int q1 = q0 + per < nq ? q0 + per : nq;
                 const uint32_t my_buf = smem_u32(red_buf);
@@ -965,15 +980,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- teardown: every role is done; release TMEM ----
     __syncwarp();
+    if (cl > 1 && !early_wait) cluster_wait_acquire();  // the set-up barrier's second half
     tc_fence_before_sync();
     __syncthreads();
-    // no CTA leaves while a peer may still multicast into it, read its shared
-    // memory or arrive on its barriers
-    if (cl > 1) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, uint32_t(p.tmem_cols));
     }
+    // no CTA leaves while a peer may still multicast into it, read its shared
+    // memory or arrive on its barriers
+    if (cl > 1) cluster_sync_all();
 }
 
 }  // namespace cakegg

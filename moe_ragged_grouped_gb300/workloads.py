@@ -155,6 +155,22 @@ class Workload:
     def flops(self, npasses: int = 1) -> float:
         return 2.0 * self.M * self.N * self.K * npasses
 
+    def algorithmic_bytes(self, pass_: str, out_bytes: int = 2) -> float:
+        """Bytes one pass must move at least: each operand read once, the output written once.
+
+        fwd reads X [M,K] and W [E,N,K] and writes Y [M,N]; dgrad reads G and W and writes
+        dX [M,K]; wgrad reads G and X and writes dW [E,N,K] (BF16 inputs, ``out_bytes``
+        per output element).
+        """
+        M, N, K, E = self.M, self.N, self.K, self.E
+        if pass_ == "fwd":
+            return 2.0 * M * K + 2.0 * E * N * K + out_bytes * M * N
+        if pass_ == "dgrad":
+            return 2.0 * M * N + 2.0 * E * N * K + out_bytes * M * K
+        if pass_ == "wgrad":
+            return 2.0 * M * N + 2.0 * M * K + out_bytes * E * N * K
+        raise ValueError(pass_)
+
     def make_numpy(self, seed: int = 0, M_alloc: int | None = None):
         """(X, W, G) uint16 BF16 bits, generated in the order X, W, G.
 
