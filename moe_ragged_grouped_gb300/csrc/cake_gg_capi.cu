@@ -261,8 +261,8 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
         plan->cluster_splits > kMaxClusterSplit ||
         (plan->cluster_splits > 0 && (pass != CAKE_GG_WGRAD || !plan->swap_ab || plan->pair != 1)) ||
-        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits) >
-            kSmemLimit)
+        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits,
+                       plan->pair) > kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->N % 8 != 0 || plan->K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
     // operands with M_max rows may be null when there are no rows at all
@@ -427,7 +427,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     grid -= grid % CL;
     if (grid < CL) grid = CL;
 
-    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs, p.csplit);
+    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs, p.csplit, P);
     cudaError_t err;
     if (mode == kModeFwd) err = launch_fwd(out_f32, P, ma, mb, mo, p, grid, smem, stream);
     else if (mode == kModeDgrad) err = launch_dgrad(out_f32, P, ma, mb, mo, p, grid, smem, stream);
@@ -501,8 +501,8 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     const int env_bn = env_int("CAKE_GG_TILE_N", 0);
     if (env_bn >= 64 && env_bn <= 256 && env_bn % 64 == 0) bn = env_bn;
     plan->tile_n = bn;
-    // two CTAs share (multicast) the B tile when it is wide; swapped thin
-    // weight gradients stay single
+    // two CTAs compute a 256-row tile as one MMA (each holds half of the B
+    // tile) when it is wide; swapped thin weight gradients stay single
     plan->pair = (bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab)) ? 2 : 1;
     const int env_pair = env_int("CAKE_GG_PAIR", -1);
     if (env_pair == 0) plan->pair = 1;
@@ -521,7 +521,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->tile_k = bk;
 
     // deeper stages only while at least two of them fit
-    while (bk > 64 && smem_bytes_for(bn, 2, bk / 64) > kSmemLimit) bk /= 2;
+    while (bk > 64 && smem_bytes_for(bn, 2, bk / 64, 1, 0, plan->pair) > kSmemLimit) bk /= 2;
     plan->tile_k = bk;
     if (pass == CAKE_GG_WGRAD) {
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
@@ -555,15 +555,16 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     }
     const int csp = plan->cluster_splits;
     int stages = kMaxStages;
-    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64, 1, csp) > kSmemLimit) --stages;
+    const int pr = plan->pair;
+    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64, 1, csp, pr) > kSmemLimit) --stages;
     // a short reduction per tile (thin data gradient / forward) makes the
     // epilogue the critical path: trade ring depth for double-buffered staging
     const int32_t red_len = pass == CAKE_GG_FWD ? K : pass == CAKE_GG_DGRAD ? N : 1 << 30;
     int staging_bufs = 1;
     if ((red_len + bk - 1) / bk <= 4) {
         int st2 = stages;
-        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp) > kSmemLimit) --st2;
-        if (smem_bytes_for(bn, st2, bk / 64, 2, csp) <= kSmemLimit) {
+        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) > kSmemLimit) --st2;
+        if (smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) <= kSmemLimit) {
             staging_bufs = 2;
             stages = st2;
         }

@@ -92,9 +92,11 @@ struct __align__(16) Ctrl {
 };
 
 // A stage holds kps = bk / 64 k-chunks of A (128 rows) and B (bn rows).
-__host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1)
+// One ring stage: A (128 rows) and this CTA's rows of B (all bn of them, or
+// half of them in a 2-SM pair), kps 64-deep k-chunks each.
+__host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1, int pair = 1)
 {
-    return uint32_t(kps) * (kABytes + uint32_t(bn) * 128u);
+    return uint32_t(kps) * (kABytes + uint32_t(bn / pair) * 128u);
 }
 
 // Cluster split: one FP32 partial tile (128 rows x bn) per CTA, read by its peers.
@@ -104,9 +106,9 @@ __host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit)
 }
 
 __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps = 1, int staging_bufs = 1,
-                                                    int csplit = 0)
+                                                    int csplit = 0, int pair = 1)
 {
-    return 1024 + size_t(stages) * stage_bytes_for(bn, kps) + size_t(staging_bufs) * kStagingBytes +
+    return 1024 + size_t(stages) * stage_bytes_for(bn, kps, pair) + size_t(staging_bufs) * kStagingBytes +
            csplit_bytes_for(bn, csplit) + sizeof(Ctrl);
 }
 
@@ -252,7 +254,7 @@ __device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
 // address field (shared-memory addresses stay below 2^18, so no carry).
 // MN-major operands step 16 rows (2 KB) down their atoms; K-major operands
 // step 32 bytes along the 128-byte row, then to the next 64-deep k-chunk.
-template <int KPS, bool A_MN, bool B_MN>
+template <int KPS, bool A_MN, bool B_MN, int CG>
 __device__ __forceinline__ void issue_stage_mmas(uint32_t d_tmem, uint64_t ad0, uint64_t bd0, uint32_t idesc,
                                                  bool first, uint32_t chunk_b)
 {
@@ -260,8 +262,8 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d_tmem, uint64_t ad0, 
     for (int ks = 0; ks < 4 * KPS; ++ks) {
         const uint32_t aoff = A_MN ? uint32_t(ks) * 2048u : uint32_t(ks >> 2) * kABytes + uint32_t(ks & 3) * 32u;
         const uint32_t boff = B_MN ? uint32_t(ks) * 2048u : uint32_t(ks >> 2) * chunk_b + uint32_t(ks & 3) * 32u;
-        umma_bf16(d_tmem, ad0 + uint64_t(aoff >> 4), bd0 + uint64_t(boff >> 4), idesc,
-                  (!first || ks > 0) ? 1u : 0u);
+        umma_bf16<CG>(d_tmem, ad0 + uint64_t(aoff >> 4), bd0 + uint64_t(boff >> 4), idesc,
+                      (!first || ks > 0) ? 1u : 0u);
     }
 }
 
@@ -280,11 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *ring = smem_raw + (ring_u32 - raw_u32);
     const int kps = p.bk / kTileK;                 // k-chunks per stage
-    const uint32_t stage_bytes = stage_bytes_for(p.bn, kps);
+    const uint32_t stage_bytes = stage_bytes_for(p.bn, kps, PAIR);
     const uint32_t a_bytes = uint32_t(kps) * kABytes;
     const uint32_t atom_a = uint32_t(kps) * kBoxBytes;   // MN-major: 64 x bk atom
     const uint32_t atom_b = atom_a;
-    const uint32_t chunk_b = uint32_t(p.bn) * 128u;      // K-major B: one 64-deep chunk of bn rows
+    const uint32_t chunk_b = uint32_t(p.bn / PAIR) * 128u;  // K-major B: one 64-deep chunk of this CTA's rows
     uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
     float *red_buf = reinterpret_cast<float *>(staging + size_t(p.staging_bufs) * kStagingBytes);
     Ctrl *c = reinterpret_cast<Ctrl *>(reinterpret_cast<uint8_t *>(red_buf) + csplit_bytes_for(p.bn, p.csplit));
@@ -296,13 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int csplit = MODE == kModeWgrad ? p.csplit : 0;
     const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit);
     // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + r
-    // with one B tile; a cluster split (csplit CTAs) computes one tile, rank r
-    // taking the r-th chunk of its reduction
+    // as one 256-row MMA (the even CTA issues it; each CTA holds its A rows and
+    // half of the B tile); a cluster split (csplit CTAs) computes one tile,
+    // rank r taking the r-th chunk of its reduction
     const int cl = PAIR == 2 ? 2 : (csplit > 0 ? csplit : 1);
     const int rank = cl > 1 ? int(cluster_ctarank()) : 0;
     const int64_t unit0 = blockIdx.x / cl;
     const int64_t unit_step = gridDim.x / cl;
     constexpr uint16_t kPairMask = 0x3;
+    const bool leader = PAIR == 1 || rank == 0;     // issues the MMAs (and owns full / tempty)
 
     // ---- setup, part 1: TMEM, barriers and tensor maps (no global loads) ----
     // runs while the previous kernel in the stream may still be finishing; the
@@ -317,17 +321,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.tma_store) tma_prefetch_desc(&mapOut);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&c->tmem_base), uint32_t(p.tmem_cols));
-        tmem_relinquish();
+        tmem_alloc<PAIR>(smem_u32(&c->tmem_base), uint32_t(p.tmem_cols));
+        tmem_relinquish<PAIR>();
     }
     if (tid == 64) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(smem_u32(&c->full[s]), 1);
-            mbar_init(smem_u32(&c->empty[s]), PAIR);  // both CTAs' MMAs read a shared stage
+            // the even CTA of a pair also counts its peer's "stage loaded" relay
+            mbar_init(smem_u32(&c->full[s]), PAIR == 2 && rank == 0 ? 2u : 1u);
+            mbar_init(smem_u32(&c->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c->tfull[a]), 1);
-            mbar_init(smem_u32(&c->tempty[a]), 4);
+            mbar_init(smem_u32(&c->tempty[a]), 4u * PAIR);  // both CTAs' epilogue warps
         }
         mbar_init(smem_u32(&c->drain), 1);
         if (csplit > 0) {
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) atomicCAS(p.status, 0, kStatusBadOffsets);
         if (warp == 1) {
             tc_fence_after_sync();
-            tmem_dealloc(c->tmem_base, uint32_t(p.tmem_cols));
+            tmem_dealloc<PAIR>(c->tmem_base, uint32_t(p.tmem_cols));
         }
         return;
     }
@@ -500,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(fb, tx);
                     const bool drop = (p.debug_flags & 1) && blockIdx.x == 0 && issued == 0;
                     if (!drop) {
-                        // B atoms this CTA loads: all of them, or its half of a pair's (multicast)
+                        // B atoms this CTA loads: all of them, or its half of a pair's
                         const int nb = p.bn / 64;
                         const int jb0 = PAIR == 2 ? rank * nb / 2 : 0;
                         const int jb1 = PAIR == 2 ? (rank + 1) * nb / 2 : nb;
@@ -515,17 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_2d(sa + atom_a, &mapA, fb, ti.mt * kTileM + 64, r);
                             }
                             if (p.stack_b) {
-                                if (PAIR == 2)
-                                    tma_load_3d_mc(sb + jb0 * atom_b, &mapB, fb, 0, r, ti.nt * nb + jb0, kPairMask);
-                                else
-                                    tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb);
+                                tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + jb0);
                             } else {
-                                for (int j = jb0; j < jb1; ++j) {
-                                    if (PAIR == 2)
-                                        tma_load_2d_mc(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, r, kPairMask);
-                                    else
-                                        tma_load_2d(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, r);
-                                }
+                                for (int j = jb0; j < jb1; ++j)
+                                    tma_load_2d(sb + (j - jb0) * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, r);
                             }
                         } else {
                             // K-major A (X or G): all k-chunks of the stage in one box when chunked
@@ -533,27 +531,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else tma_load_2d(sa, &mapA, fb, k0, ti.row0);
                             if (MODE == kModeFwd) {
                                 if (PAIR == 2)
-                                    tma_load_3d_mc(sb + uint32_t(rank) * uint32_t(p.bn / 2) * 128u, &mapB, fb, k0,
-                                                   ti.nt * p.bn + rank * (p.bn / 2), ti.e, kPairMask);
+                                    tma_load_3d(sb, &mapB, fb, k0, ti.nt * p.bn + rank * (p.bn / 2), ti.e);
                                 else if (p.chunk_b)
                                     tma_load_4d(sb, &mapB, fb, 0, ti.nt * p.bn, kb * kps, ti.e);
                                 else
                                     tma_load_3d(sb, &mapB, fb, k0, ti.nt * p.bn, ti.e);
                             } else if (p.stack_b) {
                                 // W as {64, N, K/64, E}: this CTA's atoms of one bk-row block in one box
-                                if (PAIR == 2)
-                                    tma_load_4d_mc(sb + jb0 * atom_b, &mapB, fb, 0, k0, ti.nt * nb + jb0, ti.e,
-                                                   kPairMask);
-                                else
-                                    tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb, ti.e);
+                                tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb + jb0, ti.e);
                             } else {
-                                for (int j = jb0; j < jb1; ++j) {
-                                    if (PAIR == 2)
-                                        tma_load_3d_mc(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, k0, ti.e,
-                                                       kPairMask);
-                                    else
-                                        tma_load_3d(sb + j * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, k0, ti.e);
-                                }
+                                for (int j = jb0; j < jb1; ++j)
+                                    tma_load_3d(sb + (j - jb0) * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, k0, ti.e);
                             }
                         }
                     }
@@ -577,7 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ======================= MMA issuer =======================
-        const uint32_t idesc = idesc_bf16_f32(kTileM, uint32_t(p.bn), A_MN, B_MN);
+        // (the odd CTA of a pair issues none: it zeroes its stale rows of each
+        // loaded stage and relays "stage loaded" to the even CTA's full barrier)
+        const uint32_t idesc = idesc_bf16_f32(kTileM * PAIR, uint32_t(p.bn), A_MN, B_MN);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -587,13 +577,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
             const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
-            if (!warp_wait(smem_u32(&c->tempty[acc]), acc_phase ^ 1u, c, p)) {
-                ok = false;
-                break;
+            if (leader) {
+                // every epilogue warp (of both CTAs of a pair) released this buffer
+                if (!warp_wait(smem_u32(&c->tempty[acc]), acc_phase ^ 1u, c, p)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
             }
-            tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + uint32_t(acc) * acc_stride;
             for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                // (the even CTA's full barrier also counts the peer's relay)
                 if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
                     ok = false;
                     break;
@@ -602,10 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sb = sa + a_bytes;
                 if (MODE == kModeWgrad) {
                     // rows of the expert's last stage past its end belong to the next
-                    // expert (or lie beyond M_max): zero them in every atom of A and B
+                    // expert (or lie beyond M_max): zero them in every atom of this
+                    // CTA's A and B
                     const int32_t valid = ti.row_end - (ti.row0 + kb * p.bk);
                     if (valid < p.bk) {
-                        const int natoms = 2 + p.bn / 64;
+                        const int natoms = 2 + p.bn / 64 / PAIR;
                         const int nrow = p.bk - valid;
                         const int chunks = natoms * nrow * 8;
                         for (int i = lane; i < chunks; i += 32) {
@@ -621,18 +616,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    tc_fence_after_sync();
-                    const uint64_t ad0 = A_MN ? smem_desc_sw128(sa, atom_a, 1024) : smem_desc_sw128(sa, 16, 1024);
-                    const uint64_t bd0 = B_MN ? smem_desc_sw128(sb, atom_b, 1024) : smem_desc_sw128(sb, 16, 1024);
-                    const bool first = kb == ti.kb0;
-                    if (kps == 1) issue_stage_mmas<1, A_MN, B_MN>(d_tmem, ad0, bd0, idesc, first, chunk_b);
-                    else if (kps == 2) issue_stage_mmas<2, A_MN, B_MN>(d_tmem, ad0, bd0, idesc, first, chunk_b);
-                    else issue_stage_mmas<4, A_MN, B_MN>(d_tmem, ad0, bd0, idesc, first, chunk_b);
-                    if (PAIR == 2) umma_commit_mc(smem_u32(&c->empty[stage]), kPairMask);
-                    else umma_commit(smem_u32(&c->empty[stage]));
+                if (leader) {
+                    if (lane == 0) {
+                        tc_fence_after_sync();
+                        const uint64_t ad0 = A_MN ? smem_desc_sw128(sa, atom_a, 1024) : smem_desc_sw128(sa, 16, 1024);
+                        const uint64_t bd0 = B_MN ? smem_desc_sw128(sb, atom_b, 1024) : smem_desc_sw128(sb, 16, 1024);
+                        const bool first = kb == ti.kb0;
+                        if (kps == 1) issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                        else if (kps == 2) issue_stage_mmas<2, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                        else issue_stage_mmas<4, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                        // the stage is free again in both CTAs once these MMAs complete
+                        if (PAIR == 2) umma_commit_mc<2>(smem_u32(&c->empty[stage]), kPairMask);
+                        else umma_commit<1>(smem_u32(&c->empty[stage]));
+                    }
+                    any_mma = true;
+                } else if (lane == 0) {
+                    mbar_arrive_remote(map_to_cta(smem_u32(&c->full[stage]), 0));
                 }
-                any_mma = true;
                 __syncwarp();
                 if (++stage == p.stages) {
                     stage = 0;
@@ -640,12 +640,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            if (lane == 0) umma_commit(smem_u32(&c->tfull[acc]));
+            if (leader && lane == 0) {
+                if (PAIR == 2) umma_commit_mc<2>(smem_u32(&c->tfull[acc]), kPairMask);
+                else umma_commit<1>(smem_u32(&c->tfull[acc]));
+            }
             __syncwarp();
         }
         if (!ok && any_mma) {
             if (lane == 0) {
-                umma_commit(smem_u32(&c->drain));
+                umma_commit<PAIR>(smem_u32(&c->drain));
                 drain_wait(smem_u32(&c->drain), 0, 20000000ull);
             }
             __syncwarp();
@@ -661,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
             const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
+            // (in a pair the even CTA's MMA commit arrives on both CTAs' tfull)
             bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
             ok = named_bar_and(1, 128, ok);
             if (!ok) break;
@@ -887,10 +891,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // accumulator buffer free for the MMA warp
+            // accumulator buffer free for the MMA warp (of the even CTA of a pair)
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&c->tempty[acc]));
+            if (lane == 0) {
+                if (leader) mbar_arrive(smem_u32(&c->tempty[acc]));
+                else mbar_arrive_remote(map_to_cta(smem_u32(&c->tempty[acc]), 0));
+            }
 
             if (split) {
                 // ticket: the last split of this output tile to arrive finishes it
@@ -983,13 +990,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (cl > 1 && !early_wait) cluster_wait_acquire();  // the set-up barrier's second half
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 1 && PAIR == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, uint32_t(p.tmem_cols));
+        tmem_dealloc<1>(tmem_base, uint32_t(p.tmem_cols));
     }
-    // no CTA leaves while a peer may still multicast into it, read its shared
-    // memory or arrive on its barriers
+    // no CTA leaves while a peer may still read its shared memory, write its
+    // TMEM or arrive on its barriers
     if (cl > 1) cluster_sync_all();
+    if (warp == 1 && PAIR == 2) {
+        // both CTAs free the pair's columns together
+        tc_fence_after_sync();
+        tmem_dealloc<2>(tmem_base, uint32_t(p.tmem_cols));
+    }
 }
 
 }  // namespace cakegg

@@ -186,8 +186,10 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         const int32_t nkb_e = ceil_div_i(r1 - r0, g.bk);
         const int32_t s = local % S;
         const int32_t rest = local / S;
-        ti.nt = rest % g.n_tiles;
-        ti.mt = (rest / g.n_tiles) * g.pair + rank;
+        // m-units fastest: the units of a wave share the wide operand's columns
+        // (fewer L2 misses than walking the n-tiles first)
+        ti.nt = rest / m_units_w(g);
+        ti.mt = (rest % m_units_w(g)) * g.pair + rank;
         ti.s = s;
         ti.S = S;
         const int32_t chunk = S > 1 ? g.kchunk : nkb_e;
