@@ -12,6 +12,13 @@ output, deterministic mode.  Operands (2.1 GB per step) are larger than the
 Prints one JSON line (rank 0).  ``--impl reference`` times the FP64 CPU
 oracle on the host cores instead (a bounded sample of the same workload per
 step).  Under torchrun each rank runs an independent replica (weak scaling).
+
+    python bench.py --grid pages [--grid-filter TEXT] [--grid-reps R]
+
+times the GB300 rows of flashinfer PR #8269's per-row latency table (weight
+gradient, checkpointed forward + backward, and the same with early stop) the
+way that table was measured: one call, cold L2, median over repetitions.  It
+prints one JSON line per row and a summary line.
 """
 from __future__ import annotations
 
@@ -51,6 +58,10 @@ def parse_args():
                          "back), per-pass times from a separate loop")
     ap.add_argument("--graph", action="store_true",
                     help="replay each pass from a captured CUDA graph (removes host launch overhead)")
+    ap.add_argument("--grid", default="", choices=["", "pages"],
+                    help="pages: time the GB300 rows of the pages' per-row latency table")
+    ap.add_argument("--grid-filter", default="", help="only rows whose 'shape op' contains this text")
+    ap.add_argument("--grid-reps", type=int, default=7)
     return ap.parse_args()
 
 
@@ -516,8 +527,84 @@ def run_reference(args, wk):
     print(json.dumps(line), flush=True)
 
 
+def run_pages_grid(args):
+    """One call per repetition, L2 flushed before it, CUDA events around it."""
+    import torch
+    from moe_ragged_grouped_gb300 import cake_gg as gg
+    from moe_ragged_grouped_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gg.load_library()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # twice the L2
+    stream = torch.cuda.current_stream(dev)
+    rows = [r for r in wl.PAGES_GB300_ROWS if args.grid_filter in f"{r[0]} {r[1]}"]
+    cur_shape, tensors = None, None
+    ratios = {}
+    for shape, op, det_ms, sota_ms, sota_key, nd_ms in rows:
+        wk, od_dw = wl.pages_workload(shape)
+        if shape != cur_shape:
+            tensors = None
+            torch.cuda.empty_cache()
+            X, W, G = wk.make_torch(seed=0, device=dev)
+            offs = torch.from_numpy(wk.offsets).to(dev)
+            tensors = (X, W, G, offs)
+            cur_shape = shape
+        X, W, G, offs = tensors
+        passes = wl.PAGES_OPS[op]
+        od = od_dw if op == "dW" else "bf16"
+        tdt = torch.float32 if od == "fp32" else torch.bfloat16
+        outs = {"fwd": torch.empty((wk.M, wk.N), dtype=tdt, device=dev),
+                "dgrad": torch.empty((wk.M, wk.K), dtype=tdt, device=dev) if "dgrad" in passes else None,
+                "wgrad": torch.empty((wk.E, wk.N, wk.K), dtype=tdt, device=dev)}
+        plans = {p: gg.cake_gg_plan(p, wk.E, wk.M, wk.N, wk.K, od, 1) for p in set(passes)}
+        wss = {p: gg.make_workspace(plans[p], dev) for p in plans}
+        ops = {"fwd": (gg.cake_gg_fwd, X, W), "dgrad": (gg.cake_gg_dgrad, G, W), "wgrad": (gg.cake_gg_wgrad, G, X)}
+
+        def call():
+            for p in passes:
+                fn, a, b = ops[p]
+                rc = fn(plans[p], a, b, outs[p], offs, od, 1, wss[p], stream=stream.cuda_stream)
+                if rc != 0:
+                    raise gg.CakeGGError(rc, p)
+
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize(dev)
+        for p in plans:
+            st = gg.cake_gg_check_status(wss[p], stream.cuda_stream)
+            if st != 0:
+                raise gg.CakeGGError(st, f"{shape} {p} device status")
+        times = []
+        for _ in range(args.grid_reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        line = {"grid": "pages_gb300", "shape": shape, "op": op, "out_dtype": od, "deterministic": True,
+                "ms": round(ms, 4), "tflops": round(wk.flops(len(passes)) / (ms * 1e-3) / 1e12, 1),
+                "ms_min_max": [round(min(times), 4), round(max(times), 4)],
+                "pages_det_ms": det_ms, "vs_pages_det": round(det_ms / ms, 4),
+                "pages_nondet_ms": nd_ms, "vs_pages_nondet": round(nd_ms / ms, 4),
+                "pages_sota_ms": sota_ms, "pages_sota": sota_key, "vs_pages_sota": round(sota_ms / ms, 4)}
+        print(json.dumps(line), flush=True)
+        for k in ("det", "nondet", "sota"):
+            ratios.setdefault((op, k), []).append(line[f"vs_pages_{k}"])
+        del outs, wss
+    summary = {"grid": "pages_gb300", "summary": "geomean of (pages' latency / ours) per operation", "rows": len(rows)}
+    for (op, k), v in sorted(ratios.items()):
+        summary[f"{op} vs {k}"] = round(math.exp(sum(math.log(x) for x in v) / len(v)), 4)
+    print(json.dumps(summary), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.grid == "pages":
+        run_pages_grid(args)
+        return
     wk = get_workload(args.workload)
     if args.workload != "moe_gate_up" and "wgrad" in args.passes and wk.passes == ("wgrad",):
         args.passes = "wgrad"

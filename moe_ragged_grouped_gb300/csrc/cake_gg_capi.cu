@@ -407,6 +407,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.staging_bufs = plan->staging_bufs;
     p.csplit = mode == kModeWgrad ? plan->cluster_splits : 0;
     p.debug_flags = plan->debug_flags;
+    p.prefetch = mode == kModeWgrad && !plan->swap_ab ? env_int("CAKE_GG_PREFETCH", 0) : 0;
+    if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles

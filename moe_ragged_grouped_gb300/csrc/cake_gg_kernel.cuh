@@ -69,6 +69,7 @@ struct KParams {
     int32_t staging_bufs;   // epilogue staging buffers per warp (1 or 2)
     int32_t csplit;         // weight gradient: splits per tile reduced on chip by one cluster (0 = off)
     int32_t debug_flags;
+    int32_t prefetch;       // weight gradient: L2 prefetch distance in stages (0 = off)
     uint64_t timeout_ns;
 };
 
@@ -265,6 +266,29 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d_tmem, uint64_t ad0, 
         umma_bf16<CG>(d_tmem, ad0 + uint64_t(aoff >> 4), bd0 + uint64_t(boff >> 4), idesc,
                       (!first || ks > 0) ? 1u : 0u);
     }
+}
+
+// Weight gradient: rows [valid, bk) of a stage lie past the expert's end (the
+// next expert's rows, or beyond M_max); zero them in every 64-wide atom of
+// this CTA's A (2 atoms) and B (natoms - 2 atoms) before the MMAs read the
+// stage.  Kept out of line: inlined, it slows the MMA warp's loop on every
+// stage although it runs at most once per tile.
+static __device__ __noinline__ void zero_stale_rows(uint8_t *ring, uint32_t ring_u32, uint32_t sa, uint32_t sb,
+                                             uint32_t atom_a, uint32_t atom_b, int valid, int bk, int natoms,
+                                             int lane)
+{
+    const int nrow = bk - valid;
+    const int chunks = natoms * nrow * 8;
+    for (int i = lane; i < chunks; i += 32) {
+        const int atom = i / (nrow * 8);
+        const int rem = i - atom * nrow * 8;
+        const int row = valid + rem / 8;
+        const int ch = rem % 8;
+        const uint32_t base = atom < 2 ? sa + uint32_t(atom) * atom_a : sb + uint32_t(atom - 2) * atom_b;
+        uint8_t *dst = ring + (base - ring_u32) + row * 128 + ch * 16;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
 }
 
 // ---------------------------------------------------------------- kernel
@@ -512,6 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t k0 = kb * p.bk;      // first reduction element of the stage
                         if (MODE == kModeWgrad) {
                             const int32_t r = ti.row0 + k0;
+                            // both operands stream once per unit from rows far apart in
+                            // time across the grid: pull the stage `prefetch` ahead into
+                            // L2 so that its real load hits
+                            if (p.prefetch > 0 && kb + p.prefetch < ti.kb1 && p.stack_a && p.stack_b) {
+                                const int32_t rp = r + p.prefetch * p.bk;
+                                tma_prefetch_l2_3d(&mapA, 0, rp, ti.mt * 2);
+                                tma_prefetch_l2_3d(&mapB, 0, rp, ti.nt * nb + jb0);
+                            }
                             // A: 128 MN x bk rows as two 64-wide atoms
                             if (p.stack_a) {
                                 tma_load_3d(sa, &mapA, fb, 0, r, ti.mt * 2);
@@ -586,6 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
             }
             const uint32_t d_tmem = tmem_base + uint32_t(acc) * acc_stride;
+            // weight gradient: the one k-block of this unit whose stage reaches past
+            // the expert's end (none when the expert's rows are a multiple of bk)
+            int zero_kb = -1, zero_valid = 0;
+            if (MODE == kModeWgrad && ti.kb1 > ti.kb0) {
+                const int32_t v = ti.row_end - (ti.row0 + (ti.kb1 - 1) * p.bk);
+                if (v < p.bk) {
+                    zero_kb = ti.kb1 - 1;
+                    zero_valid = v;
+                }
+            }
             for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                 // (the even CTA's full barrier also counts the peer's relay)
                 if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
@@ -594,27 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
                 const uint32_t sb = sa + a_bytes;
-                if (MODE == kModeWgrad) {
-                    // rows of the expert's last stage past its end belong to the next
-                    // expert (or lie beyond M_max): zero them in every atom of this
-                    // CTA's A and B
-                    const int32_t valid = ti.row_end - (ti.row0 + kb * p.bk);
-                    if (valid < p.bk) {
-                        const int natoms = 2 + p.bn / 64 / PAIR;
-                        const int nrow = p.bk - valid;
-                        const int chunks = natoms * nrow * 8;
-                        for (int i = lane; i < chunks; i += 32) {
-                            const int atom = i / (nrow * 8);
-                            const int rem = i - atom * nrow * 8;
-                            const int row = valid + rem / 8;
-                            const int ch = rem % 8;
-                            const uint32_t base = atom < 2 ? sa + uint32_t(atom) * atom_a : sb + uint32_t(atom - 2) * atom_b;
-                            uint8_t *dst = ring + (base - ring_u32) + row * 128 + ch * 16;
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                }
+                if (MODE == kModeWgrad && kb == zero_kb)
+                    zero_stale_rows(ring, ring_u32, sa, sb, atom_a, atom_b, zero_valid, p.bk, 2 + p.bn / 64 / PAIR,
+                                    lane);
                 __syncwarp();
                 if (leader) {
                     if (lane == 0) {

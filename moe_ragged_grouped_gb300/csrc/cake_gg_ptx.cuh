@@ -116,6 +116,24 @@ __device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap *
         : "memory");
 }
 
+// Pull a box of a tensor into L2 only (no shared memory, no barrier): issued
+// some stages ahead of the real load so that its data is an L2 hit.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Multicast variants: the box lands at the same shared-memory offset in every
 // CTA of `mask` (this cluster), each of whose mbarrier at `bar`'s offset gets
 // the complete-tx.

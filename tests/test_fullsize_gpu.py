@@ -11,6 +11,8 @@ Workloads (E experts, M routed rows, K, N):
   MoE gate_up        E=8, M=131072 balanced, K=4096, N=3072
   MoE down           E=32, M=131072 multinomial (seed 0), K=1536, N=4096
   skewed MoE         E=4, M=136064 Zipf(1.2) ascending with an empty expert, (K,N) = (4096,3072), (3072,4096)
+  the pages' grid    gate_up N=4096 K=6144 and down N=6144 K=2048 with balanced, Zipf-skewed,
+                     one-empty and lognormal group sizes (a few representative rows)
 """
 import numpy as np
 import pytest
@@ -160,3 +162,19 @@ def test_skewed_deterministic_bitwise_runs_and_sm_caps(pass_):
     for cap in (100, 148):
         gg.grouped_gemm(pass_, a, b, offs, out_dtype="bf16", deterministic=1, max_sms=cap, out=out)
         assert torch.equal(view(out).contiguous().view(torch.int16), ref_v), f"max_sms={cap}"
+
+
+@pytest.mark.parametrize("shape,passes", [
+    ("gate_up E4 M136064 1-empty asc", ("wgrad", "fwd", "dgrad")),
+    ("gate_up E4 M112576 skew", ("wgrad",)),
+    ("gate_up E32 M131072 random", ("wgrad",)),
+    ("down E4 M112576 bal fp32", ("wgrad",)),
+    ("down E8 M131072 random", ("wgrad", "fwd", "dgrad")),
+])
+def test_pages_grid_rows(shape, passes):
+    """Shapes of the pages' GB300 latency table (weight gradient in its stated output dtype;
+    the checkpointed rows' forward and data gradient in BF16)."""
+    wk, od = wl.pages_workload(shape)
+    rng = np.random.default_rng(7)
+    for p in passes:
+        run_and_check(wk, p, od if p == "wgrad" else "bf16", 1, rng)
