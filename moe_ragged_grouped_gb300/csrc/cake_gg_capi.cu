@@ -254,7 +254,7 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         plan->M_max > INT32_MAX)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->tile_m != kTileM || (plan->tile_k != 64 && plan->tile_k != 128 && plan->tile_k != 256) ||
-        (plan->tile_k != 64 && plan->pair != 1 && pass == CAKE_GG_FWD) || (plan->pair != 1 && plan->pair != 2) ||
+        (plan->pair != 1 && plan->pair != 2) ||
         (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
         plan->tile_n < 64 || plan->tile_n > 256 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
@@ -331,7 +331,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
             const uint32_t ba[3] = {64, uint32_t(kTileM), uint32_t(kps)};
             const uint64_t db[4] = {64, uint64_t(N), uint64_t(K) / 64, uint64_t(E)};
             const uint64_t sb_[3] = {uint64_t(K) * 2, 128, uint64_t(N) * K * 2};
-            const uint32_t bb[4] = {64, uint32_t(bn), uint32_t(kps), 1};
+            const uint32_t bb[4] = {64, uint32_t(bn / plan->pair), uint32_t(kps), 1};
             if ((rc = encode_map_nd(&ma, opA, 3, da, sa_, ba)) != CAKE_GG_OK) return rc;
             if ((rc = encode_map_nd(&mb, opB, 4, db, sb_, bb)) != CAKE_GG_OK) return rc;
             chunk_a = chunk_b = true;
@@ -511,15 +511,20 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // deeper stages (two 64-deep k-chunks) for the memory-bound thin shapes:
     // one TMA box then moves 32 KB of the streamed operand, which a CTA pulls
     // from HBM about twice as fast as 16 KB boxes
+    // 2-SM pairs: 128-deep stages (8 MMAs and two 32 KB boxes per stage) halve
+    // the per-stage barrier, commit and copy overhead of 64-deep ones; short
+    // reductions keep 64-deep stages (a deeper ring for their few k-blocks)
     int32_t bk = 64;
+    const bool chunkable = pass == CAKE_GG_WGRAD || (pass == CAKE_GG_FWD ? K : N) % 64 == 0;
+    const int64_t red_per_unit = pass == CAKE_GG_FWD ? K : pass == CAKE_GG_DGRAD ? N : M_max / E;
     if (plan->pair == 1) {
         if (pass == CAKE_GG_FWD && N <= 64 && K % 64 == 0) bk = 128;
         if (pass == CAKE_GG_WGRAD && plan->swap_ab) bk = 128;
+    } else if (chunkable && red_per_unit >= 2048) {
+        bk = 128;
     }
     const int env_bk = env_int("CAKE_GG_TILE_K", 0);
-    if ((env_bk == 64 || env_bk == 128 || env_bk == 256) && (plan->pair == 1 || env_bk == 64 || pass != CAKE_GG_FWD) &&
-        (env_bk == 64 || pass == CAKE_GG_WGRAD || (pass == CAKE_GG_FWD ? K : N) % 64 == 0))
-        bk = env_bk;
+    if ((env_bk == 64 || env_bk == 128 || env_bk == 256) && (env_bk == 64 || chunkable)) bk = env_bk;
     plan->tile_k = bk;
 
     // deeper stages only while at least two of them fit
@@ -573,6 +578,14 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     }
     const int env_sb = env_int("CAKE_GG_STAGING_BUFS", 0);
     if (env_sb == 1) staging_bufs = 1;
+    if (env_sb == 2 && staging_bufs == 1) {
+        int st2 = stages;
+        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) > kSmemLimit) --st2;
+        if (smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) <= kSmemLimit) {
+            staging_bufs = 2;
+            stages = st2;
+        }
+    }
     plan->staging_bufs = staging_bufs;
     const int env_st = env_int("CAKE_GG_STAGES", 0);
     if (env_st >= 2 && env_st <= stages) stages = env_st;

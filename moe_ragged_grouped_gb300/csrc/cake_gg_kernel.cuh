@@ -562,12 +562,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (p.chunk_a) tma_load_3d(sa, &mapA, fb, 0, ti.row0, kb * kps);
                             else tma_load_2d(sa, &mapA, fb, k0, ti.row0);
                             if (MODE == kModeFwd) {
-                                if (PAIR == 2)
-                                    tma_load_3d(sb, &mapB, fb, k0, ti.nt * p.bn + rank * (p.bn / 2), ti.e);
-                                else if (p.chunk_b)
-                                    tma_load_4d(sb, &mapB, fb, 0, ti.nt * p.bn, kb * kps, ti.e);
+                                // this CTA's rows of the W tile: all bn, or its half of a pair's
+                                const int32_t wrow = ti.nt * p.bn + rank * (p.bn / PAIR);
+                                if (p.chunk_b)
+                                    tma_load_4d(sb, &mapB, fb, 0, wrow, kb * kps, ti.e);
                                 else
-                                    tma_load_3d(sb, &mapB, fb, k0, ti.nt * p.bn, ti.e);
+                                    tma_load_3d(sb, &mapB, fb, k0, wrow, ti.e);
                             } else if (p.stack_b) {
                                 // W as {64, N, K/64, E}: this CTA's atoms of one bk-row block in one box
                                 tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb + jb0, ti.e);
@@ -834,7 +834,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tma_path) {
                 constexpr int CW = OUT_F32 ? 32 : 64;  // columns per 128-byte row
                 int buf = 0;
-                for (int c0 = 0; c0 < p.bn; c0 += CW) {
+                // only chunks that exist: every staging write must be followed by its
+                // committed store, or the alternating-buffer wait (all groups but the
+                // newest have read their buffers) would let a write overtake a store
+                for (int c0 = 0; c0 < p.bn && c0 < cols_valid; c0 += CW) {
                     // this warp's staging buffers alternate when there are two
                     uint8_t *stg = staging + (size_t(buf) * 4 + q) * 4096;
                     const uint32_t stg_u32 = smem_u32(stg);
@@ -869,7 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0 && c0 < cols_valid) {
+                    if (lane == 0) {
                         const int32_t x = ti.nt * p.bn + c0;
                         if (MODE == kModeWgrad)
                             tma_store_3d(&mapOut, stg_u32, x, ti.mt * kTileM + q * 32, ti.e);

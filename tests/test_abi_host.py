@@ -160,7 +160,7 @@ def test_tile_walk_split_partitions():
     plan, tiles = _check_walk_coverage("wgrad", [0, 3000, 700, 64], N=128, K=256,
                                        env={"CAKE_GG_SPLIT_CHUNK": "4"})
     assert plan.split_chunk == 4
-    assert max(t[4] for t in tiles) == -(-(-(-3000 // 64)) // 4)
+    assert max(t[4] for t in tiles) == -(-(-(-3000 // plan.tile_k)) // 4)
 
 
 def test_tile_walk_thin_swap():

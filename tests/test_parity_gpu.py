@@ -239,3 +239,25 @@ def test_thin_weight_gradient_through_workspace_slots(det, monkeypatch):
     """The same thin shape with the cluster reduction disabled: partials through the workspace."""
     monkeypatch.setenv("CAKE_GG_CSPLIT", "0")
     check_case("wgrad", [3000], 48, 512, "fp32", det, seed=3, extra_rows=5)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("max_sms", [2, 0])
+def test_double_staging_partial_last_tile(pass_, out_dtype, max_sms, monkeypatch):
+    """Two alternating staging buffers per epilogue warp, an output width that leaves the last
+    column tile partial (384 = 256 + 128), and one CTA pair running every tile in turn: each
+    staging write must be followed by its own committed store."""
+    monkeypatch.setenv("CAKE_GG_STAGING_BUFS", "2")
+    N, K = (384, 512) if pass_ == "fwd" else (512, 384)
+    check_case(pass_, [0, 777, 2048, 301], N, K, out_dtype, 1, seed=19, extra_rows=4, max_sms=max_sms)
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("tile_k", ["64", "128"])
+def test_pairs_at_both_stage_depths_and_few_ctas(pass_, tile_k, monkeypatch):
+    """2-SM pairs with 64- and 128-deep stages, on a grid of one and three pairs (many tiles per
+    CTA, ring and accumulator phases carried across tiles), ragged groups with a NaN tail."""
+    monkeypatch.setenv("CAKE_GG_TILE_K", tile_k)
+    for cap in (2, 6):
+        check_case(pass_, [0, 777, 2048, 301], 384, 512, "fp32", 1, seed=20, extra_rows=5, max_sms=cap)
