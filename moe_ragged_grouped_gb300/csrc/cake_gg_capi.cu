@@ -23,7 +23,8 @@ constexpr int kWaveCtas = 152;              // GB300 SMs: the wave size the spli
 constexpr int kMinSplitChunk = 4;           // k-blocks (256 rows) per split at least
 constexpr int kMaxClusterSplit = 8;         // portable cluster size
 constexpr size_t kSmemLimit = kSmemOptInLimit;
-constexpr uint64_t kHeaderBytes = 256;      // workspace: status word and padding
+constexpr uint64_t kHeaderBytes = 256;      // workspace: status word, unit scheduler words, padding
+constexpr uint64_t kSchedOffset = 64;       // next-unit counter; CTAs-retired counter 128 bytes further
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 bool mul_ok(uint64_t a, uint64_t b, uint64_t *out)
@@ -408,6 +409,11 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.csplit = mode == kModeWgrad ? plan->cluster_splits : 0;
     p.debug_flags = plan->debug_flags;
     p.prefetch = mode == kModeWgrad && !plan->swap_ab ? env_int("CAKE_GG_PREFETCH", 0) : 0;
+    // weight-gradient units differ in length (skewed experts): take them from a
+    // global counter in heaviest-first order (the cluster split keeps its
+    // static one-unit-per-cluster walk)
+    p.dyn = mode == kModeWgrad && plan->cluster_splits == 0 && env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
+    p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
     if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 

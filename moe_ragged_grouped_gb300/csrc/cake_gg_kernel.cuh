@@ -70,8 +70,12 @@ struct KParams {
     int32_t csplit;         // weight gradient: splits per tile reduced on chip by one cluster (0 = off)
     int32_t debug_flags;
     int32_t prefetch;       // weight gradient: L2 prefetch distance in stages (0 = off)
+    int32_t dyn;            // units fetched from a global counter (else a static stride)
+    int32_t *sched;         // [0]: next unit, [32]: CTAs retired (zero between calls)
     uint64_t timeout_ns;
 };
+
+constexpr int kUQ = 4;      // depth of the queue that passes fetched units to every role
 
 // Control block after the operand ring.
 struct __align__(16) Ctrl {
@@ -82,6 +86,9 @@ struct __align__(16) Ctrl {
     uint64_t drain;
     uint64_t red_ready;     // cluster split: all csplit partials of the current tile are in place
     uint64_t red_consumed;  // cluster split: every peer has read this CTA's partial
+    uint64_t uq_full[kUQ];  // unit queue slot written (by the even CTA's producer)
+    uint64_t uq_empty[kUQ]; // (even CTA) every role of the cluster has read the slot
+    int64_t uq[kUQ];        // unit ids, -1 = no more
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t bad;
@@ -184,6 +191,61 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
+// Single-thread bounded wait with cluster-scope acquire.
+__device__ __forceinline__ bool thread_wait_cluster(uint32_t bar, uint32_t parity, Ctrl *c, const KParams &p)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int32_t *>(&c->abort_flag)) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            *reinterpret_cast<volatile int32_t *>(&c->abort_flag) = 1;
+            atomicCAS(p.status, 0, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// The units a CTA (pair) processes: a static stride over the walk, or, when
+// p.dyn, units taken from a global counter in walk order (heaviest first) by
+// the even CTA's producer -- greedy list scheduling, so skewed experts
+// balance -- and passed to every role of both CTAs through the unit queue.
+// Results do not depend on which CTA computes a unit.
+struct UnitSeq {
+    int64_t t;
+    int64_t pos;
+};
+
+// A consuming warp (MMA / relay, epilogue) takes the next unit; false = none
+// left (or abort: ok = false).
+__device__ __forceinline__ bool warp_next_unit(UnitSeq &u, int64_t unit0, int64_t unit_step, int64_t total,
+                                               bool leader, int lane, Ctrl *c, const KParams &p, bool &ok)
+{
+    if (!p.dyn) {
+        u.t = u.pos == 0 ? unit0 : u.t + unit_step;
+        ++u.pos;
+        return u.t < total;
+    }
+    const int slot = int(u.pos % kUQ);
+    const uint32_t par = uint32_t((u.pos / kUQ) & 1);
+    const bool w = leader ? warp_wait(smem_u32(&c->uq_full[slot]), par, c, p)
+                          : cluster_wait(smem_u32(&c->uq_full[slot]), par, c, p);
+    if (!w) {
+        ok = false;
+        return false;
+    }
+    u.t = *reinterpret_cast<volatile int64_t *>(&c->uq[slot]);
+    __syncwarp();
+    if (lane == 0) {
+        if (leader) mbar_arrive(smem_u32(&c->uq_empty[slot]));
+        else mbar_arrive_cluster(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
+    }
+    ++u.pos;
+    return u.t >= 0;
+}
+
 // Ticket of a split output tile: returns how many splits of this call (epoch)
 // arrived before this one.  A ticket word left by an earlier call carries
 // another epoch and counts as zero, so tickets never need clearing.  At most
@@ -274,19 +336,16 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d_tmem, uint64_t ad0, 
 // stage.  Kept out of line: inlined, it slows the MMA warp's loop on every
 // stage although it runs at most once per tile.
 static __device__ __noinline__ void zero_stale_rows(uint8_t *ring, uint32_t ring_u32, uint32_t sa, uint32_t sb,
-                                             uint32_t atom_a, uint32_t atom_b, int valid, int bk, int natoms,
-                                             int lane)
+                                                    uint32_t atom_a, uint32_t atom_b, int valid, int bk, int natoms,
+                                                    int lane)
 {
-    const int nrow = bk - valid;
-    const int chunks = natoms * nrow * 8;
-    for (int i = lane; i < chunks; i += 32) {
-        const int atom = i / (nrow * 8);
-        const int rem = i - atom * nrow * 8;
-        const int row = valid + rem / 8;
-        const int ch = rem % 8;
+    // a warp pass covers 4 rows x 8 16-byte chunks of one atom
+    const int ch = lane & 7;
+    for (int atom = 0; atom < natoms; ++atom) {
         const uint32_t base = atom < 2 ? sa + uint32_t(atom) * atom_a : sb + uint32_t(atom - 2) * atom_b;
-        uint8_t *dst = ring + (base - ring_u32) + row * 128 + ch * 16;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        uint8_t *a = ring + (base - ring_u32) + ch * 16;
+        for (int row = valid + (lane >> 3); row < bk; row += 4)
+            *reinterpret_cast<uint4 *>(a + row * 128) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
 }
@@ -359,6 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&c->tempty[a]), 4u * PAIR);  // both CTAs' epilogue warps
         }
         mbar_init(smem_u32(&c->drain), 1);
+        for (int i = 0; i < kUQ; ++i) {
+            mbar_init(smem_u32(&c->uq_full[i]), 1);
+            // readers of a slot: MMA (or relay) warp, 4 epilogue warps, and the
+            // odd CTA's producer in a pair
+            mbar_init(smem_u32(&c->uq_empty[i]), PAIR == 2 ? 11u : 5u);
+        }
         if (csplit > 0) {
             mbar_init(smem_u32(&c->red_ready), uint32_t(csplit));
             mbar_init(smem_u32(&c->red_consumed), uint32_t(csplit));
@@ -516,7 +581,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = unit0; t < total && ok; t += unit_step) {
+            UnitSeq us{0, 0};
+            int32_t nxt = 0;
+            if (p.dyn && leader) nxt = atomicAdd(p.sched, 1);
+            while (ok) {
+                int64_t t;
+                if (!p.dyn) {
+                    t = us.pos == 0 ? unit0 : us.t + unit_step;
+                    us.t = t;
+                    ++us.pos;
+                    if (t >= total) break;
+                } else if (leader) {
+                    // fetch: publish the unit to every role of the cluster
+                    const int slot = int(us.pos % kUQ);
+                    if (us.pos >= kUQ && !thread_wait_cluster(smem_u32(&c->uq_empty[slot]),
+                                                              uint32_t(((us.pos / kUQ) - 1) & 1), c, p)) {
+                        ok = false;
+                        break;
+                    }
+                    t = int64_t(nxt) < total ? int64_t(nxt) : -1;
+                    c->uq[slot] = t;
+                    if (PAIR == 2) st_shared_cluster_b64(map_to_cta(smem_u32(&c->uq[slot]), 1), t);
+                    mbar_arrive(smem_u32(&c->uq_full[slot]));
+                    if (PAIR == 2) mbar_arrive_cluster(map_to_cta(smem_u32(&c->uq_full[slot]), 1));
+                    ++us.pos;
+                    if (t < 0) break;
+                    nxt = atomicAdd(p.sched, 1);  // in flight while this unit's copies go out
+                } else {
+                    // the odd CTA's producer reads the queue like every other role
+                    const int slot = int(us.pos % kUQ);
+                    if (!thread_wait_cluster(smem_u32(&c->uq_full[slot]), uint32_t((us.pos / kUQ) & 1), c, p)) {
+                        ok = false;
+                        break;
+                    }
+                    t = *reinterpret_cast<volatile int64_t *>(&c->uq[slot]);
+                    mbar_arrive_cluster(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
+                    ++us.pos;
+                    if (t < 0) break;
+                }
                 const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                     if (!thread_wait(smem_u32(&c->empty[stage]), phase ^ 1u, c, p, p.timeout_ns)) {
@@ -605,7 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         bool any_mma = false;
-        for (int64_t t = unit0; t < total && ok; t += unit_step, ++it) {
+        for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, ok); ++it) {
+            const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
             const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
@@ -684,7 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int etid = tid - 64;         // 0..127
         int it = 0;
         int cs_it = 0;                     // cluster-split tiles reduced so far
-        for (int64_t t = unit0; t < total; t += unit_step, ++it) {
+        bool qok = true;
+        for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, qok); ++it) {
+            const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
             const int acc = it & 1;
             const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
@@ -1028,6 +1133,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both CTAs free the pair's columns together
         tc_fence_after_sync();
         tmem_dealloc<2>(tmem_base, uint32_t(p.tmem_cols));
+    }
+    if (p.dyn && tid == 0) {
+        // the last CTA to retire leaves the unit counter at zero for the next
+        // call (every CTA's fetches are done when it counts itself)
+        __threadfence();
+        if (atomicAdd(p.sched + 32, 1) == int32_t(gridDim.x) - 1) {
+            atomicExch(p.sched, 0);
+            atomicExch(p.sched + 32, 0);
+        }
     }
 }
 

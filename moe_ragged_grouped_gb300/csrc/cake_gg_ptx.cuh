@@ -171,6 +171,12 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// 8-byte store into a peer CTA's shared memory (address from mapa).
+__device__ __forceinline__ void st_shared_cluster_b64(uint32_t cluster_addr, int64_t v)
+{
+    asm volatile("st.shared::cluster.b64 [%0], %1;" ::"r"(cluster_addr), "l"(v) : "memory");
+}
+
 // Arrive on an mbarrier of a peer CTA with the default (CTA-scope release)
 // semantics: a cheap count for pipeline signals whose data is tracked by the
 // barrier itself (TMA bytes, tensor-core commits) rather than by generic

@@ -261,3 +261,39 @@ def test_pairs_at_both_stage_depths_and_few_ctas(pass_, tile_k, monkeypatch):
     monkeypatch.setenv("CAKE_GG_TILE_K", tile_k)
     for cap in (2, 6):
         check_case(pass_, [0, 777, 2048, 301], 384, 512, "fp32", 1, seed=20, extra_rows=5, max_sms=cap)
+
+
+@pytest.mark.parametrize("sizes,N,K", [([0, 5000, 1900, 33, 0, 777], 384, 512), ([3000, 200, 17], 256, 128)])
+@pytest.mark.parametrize("max_sms", [0, 6])
+def test_dynamic_and_static_unit_order_agree_bitwise(sizes, N, K, max_sms, monkeypatch):
+    """Weight-gradient units taken from a global counter (heaviest first) give the same bits as the
+    static stride: a tile's arithmetic never depends on the CTA that computes it."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs(sizes, N, K, seed=21, extra_rows=3)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    dyn = run("wgrad", X, W, G, off, "fp32", 1, max_sms=max_sms)
+    monkeypatch.setenv("CAKE_GG_DYN", "0")
+    stat = run("wgrad", X, W, G, off, "fp32", 1, max_sms=max_sms)
+    assert torch.equal(dyn.view(torch.int32), stat.view(torch.int32))
+
+
+def test_scheduler_words_return_to_zero():
+    """The unit counter and the retired-CTA counter in the workspace header are zero after every
+    call, so the workspace needs no clearing between calls."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs([700, 0, 1300], 256, 512, seed=22)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    E, M = 3, Xb.shape[0]
+    plans = [gg.cake_gg_plan("wgrad", E, M, 256, 512, od, 1, cap) for od in ("bf16", "fp32") for cap in (0, 4)]
+    ws = torch.zeros(max(int(pl.workspace_bytes) for pl in plans), dtype=torch.uint8, device="cuda")
+    offs = torch.from_numpy(off).cuda()
+    for cap in (0, 4, 0):
+        plan = gg.cake_gg_plan("wgrad", E, M, 256, 512, "bf16", 1, cap)
+        gg.grouped_gemm("wgrad", G, X, offs, out_dtype="bf16", plan=plan, workspace=ws)
+        torch.cuda.synchronize()
+        head = ws[:256].view(torch.int32).cpu().numpy()
+        assert (head == 0).all(), head.nonzero()
+    ref = reference("wgrad", Xb, Wb, Gb, off)
+    out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", plan=gg.cake_gg_plan("wgrad", E, M, 256, 512, "fp32", 1),
+                          workspace=ws)
+    assert_parity("wgrad", out_to_f64(out), ref, Xb, Wb, Gb, off, "after reuse")
