@@ -94,9 +94,10 @@ typedef struct cake_gg_plan {
     /* chosen by cake_gg_plan() */
     int32_t tile_m;          /* MMA rows per tile (128)                             */
     int32_t tile_n;          /* MMA columns per tile (64 .. 256)                    */
-    int32_t tile_k;          /* reduction elements per pipeline stage (64)          */
+    int32_t tile_k;          /* reduction elements per pipeline stage (64, 128, 256) */
     int32_t stages;          /* shared-memory ring depth                            */
-    int32_t pair;            /* CTAs per cluster sharing one B tile by multicast (1 or 2) */
+    int32_t pair;            /* 2: two CTAs compute a 256-row tile as one tcgen05 MMA,
+                                each holding half of the B tile; 1: single CTAs      */
     int32_t swap_ab;         /* weight gradient: 1 = MMA rows run over K (thin N)   */
     int32_t split_chunk;     /* weight gradient: k-blocks per split, 0 = no split   */
     int32_t debug_flags;     /* test-only fault injection; 0 in normal use          */
@@ -105,7 +106,10 @@ typedef struct cake_gg_plan {
     int32_t staging_bufs;    /* epilogue staging buffers per warp (1 or 2)          */
     int32_t cluster_splits;  /* weight gradient: >0 = that many splits per tile run as
                                 one cluster and reduce on chip (no workspace partials) */
-    int32_t reserved[6];
+    int32_t tail_units;      /* weight gradient: the last tail_units units of the walk */
+    int32_t tail_splits;     /* are each split into tail_splits pieces whose FP32
+                                partials are summed in split order (0 = no tail split) */
+    int32_t reserved[4];
 } cake_gg_plan_t;
 
 /* Debug flag (tests only): CTA 0 arms its first pipeline stage but issues no
@@ -165,7 +169,7 @@ int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void
  *    order them on one stream.
  *  - Device-detected errors are written to the scratch's status word, which
  *    callers cannot read; outputs are unspecified after such an error. */
-#define CAKE_GG_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define CAKE_GG_NOALLOC_SCRATCH_BYTES (32u << 20)
 int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
                           const int32_t *offsets, int out_dtype, int deterministic, void *stream);
 

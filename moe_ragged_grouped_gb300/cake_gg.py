@@ -27,7 +27,7 @@ CAKE_GG_ERR_CUDA = 6
 CAKE_GG_ERR_BAD_OFFSETS = 7
 CAKE_GG_ERR_TIMEOUT = 8
 CAKE_GG_ERR_SCRATCH_LIMIT = 9
-CAKE_GG_NOALLOC_SCRATCH_BYTES = 16 << 20
+CAKE_GG_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 CAKE_GG_FWD, CAKE_GG_DGRAD, CAKE_GG_WGRAD = 0, 1, 2
 CAKE_GG_BF16, CAKE_GG_FP32 = 0, 1
@@ -64,7 +64,9 @@ class CakeGGPlan(ctypes.Structure):
         ("workspace_bytes", ctypes.c_uint64),
         ("staging_bufs", ctypes.c_int32),
         ("cluster_splits", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("tail_units", ctypes.c_int32),
+        ("tail_splits", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
     def as_dict(self):

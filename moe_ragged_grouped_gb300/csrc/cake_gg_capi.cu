@@ -25,6 +25,7 @@ constexpr int kMaxClusterSplit = 8;         // portable cluster size
 constexpr size_t kSmemLimit = kSmemOptInLimit;
 constexpr uint64_t kHeaderBytes = 256;      // workspace: status word, unit scheduler words, padding
 constexpr uint64_t kSchedOffset = 64;       // next-unit counter; CTAs-retired counter 128 bytes further
+constexpr int kMaxTailSplits = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 bool mul_ok(uint64_t a, uint64_t b, uint64_t *out)
@@ -119,11 +120,27 @@ WsLayout ws_layout(const cake_gg_plan_t &pl)
     w.partials_off = kHeaderBytes;
     w.zero_bytes = kHeaderBytes;
     w.total = kHeaderBytes;
-    if (pl.pass != CAKE_GG_WGRAD || pl.split_chunk <= 0 || pl.cluster_splits > 0) return w;
+    const bool tail = pl.pass == CAKE_GG_WGRAD && pl.tail_splits > 1 && pl.tail_units > 0;
+    if (pl.pass != CAKE_GG_WGRAD || (pl.split_chunk <= 0 && !tail) || pl.cluster_splits > 0) return w;
     const Geom g = make_geom(kModeWgrad, pl.E, pl.N, pl.K, pl.M_max, pl.tile_n, pl.swap_ab, pl.split_chunk, pl.pair,
                              pl.tile_k);
     const uint64_t tpe = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles);
     uint64_t n_tickets = 0, tile_bytes = 0, tmp = 0;
+    if (tail) {
+        // tickets for every output tile; FP32 partial slots per (tail unit, pair
+        // rank, piece), written before they are read
+        w.ok &= mul_ok(tpe, uint64_t(pl.E), &n_tickets);
+        w.ok &= mul_ok(uint64_t(kTileM) * 4u, uint64_t(pl.tile_n), &tile_bytes);
+        w.ok &= mul_ok(n_tickets, 8, &tmp);
+        w.tickets_bytes = align_up(tmp, 256);
+        w.partials_off = w.tickets_off + w.tickets_bytes;
+        uint64_t slots = 0;
+        w.ok &= mul_ok(uint64_t(pl.tail_units) * uint64_t(pl.pair), uint64_t(pl.tail_splits), &slots);
+        w.ok &= mul_ok(slots, tile_bytes, &w.partials_bytes);
+        w.ok &= add_ok(w.partials_off, w.partials_bytes, &w.total);
+        w.zero_bytes = kHeaderBytes;
+        return w;
+    }
     w.ok &= mul_ok(tpe, uint64_t(pl.E), &n_tickets);
     w.ok &= mul_ok(uint64_t(kTileM) * 4u, uint64_t(pl.tile_n), &tile_bytes);
     w.ok &= mul_ok(n_tickets, 8, &tmp);
@@ -262,6 +279,9 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
         plan->cluster_splits > kMaxClusterSplit ||
         (plan->cluster_splits > 0 && (pass != CAKE_GG_WGRAD || !plan->swap_ab || plan->pair != 1)) ||
+        plan->tail_units < 0 || plan->tail_splits < 0 || plan->tail_splits == 1 || plan->tail_splits > kMaxTailSplits ||
+        (plan->tail_splits > 1 && (pass != CAKE_GG_WGRAD || plan->swap_ab || plan->split_chunk > 0 ||
+                                   plan->cluster_splits > 0)) ||
         smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits,
                        plan->pair) > kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
@@ -414,6 +434,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     // static one-unit-per-cluster walk)
     p.dyn = mode == kModeWgrad && plan->cluster_splits == 0 && env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
     p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
+    p.tail = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_units : 0;
+    p.tail_s = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_splits : 0;
     if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 
@@ -425,7 +447,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     if (mode == kModeWgrad) {
         uint64_t splits = uint64_t(E);
         if (p.kchunk > 0) splits = M / (uint64_t(bk) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
-        unit_bound = uint64_t(m_units_w(g)) * uint64_t(g.n_tiles) * splits;
+        unit_bound = uint64_t(m_units_w(g)) * uint64_t(g.n_tiles) * splits +
+                     uint64_t(p.tail) * uint64_t(p.tail_s > 1 ? p.tail_s - 1 : 0);
     } else {
         unit_bound = (M / (uint64_t(kTileM) * P) + uint64_t(E) + 1) * uint64_t(g.n_tiles);
     }
@@ -566,6 +589,29 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
             plan->split_chunk = 0;
         }
     }
+    // split tail: the last partial wave of equal-length weight-gradient units
+    // (U mod P units for P = 152 CTAs / pair, a fixed wave so the plan never
+    // depends on max_sms) runs as S pieces each, filling about one more wave
+    // of 1/S length instead of a whole wave with few units
+    if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->split_chunk == 0 && plan->cluster_splits == 0 &&
+        env_int("CAKE_GG_TAIL", 1) != 0) {
+        const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, 0, 0, plan->pair, bk);
+        const int64_t units = int64_t(E) * m_units_w(g) * g.n_tiles;
+        const int64_t P = kWaveCtas / plan->pair;
+        const int64_t T = units % P;
+        const int64_t kb_per_unit = (M_max / E) / bk;
+        // long units only: on short ones the pieces' partial-sum finish costs
+        // about what the shorter last wave saves
+        if (units > P && T > 0 && 2 * T <= P && kb_per_unit >= 64) {
+            int64_t S = P / T;
+            if (S > kMaxTailSplits) S = kMaxTailSplits;
+            while (S > 1 && kb_per_unit < 4 * S) --S;   // pieces of at least ~4 stages
+            if (S >= 2) {
+                plan->tail_units = int32_t(T);
+                plan->tail_splits = int32_t(S);
+            }
+        }
+    }
     const int csp = plan->cluster_splits;
     int stages = kMaxStages;
     const int pr = plan->pair;
@@ -657,9 +703,11 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
     for (int e = 0; e < E; ++e)
         if (off[e + 1] < off[e]) return CAKE_GG_ERR_BAD_OFFSETS;
     const int mode = plan->pass == CAKE_GG_FWD ? kModeFwd : plan->pass == CAKE_GG_DGRAD ? kModeDgrad : kModeWgrad;
-    const Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
+    const bool tail = mode == kModeWgrad && plan->tail_splits > 1;
+    Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
                              mode == kModeWgrad ? plan->split_chunk : 0, plan->pair, plan->tile_k,
-                             mode == kModeWgrad ? plan->cluster_splits : 0);
+                             mode == kModeWgrad ? plan->cluster_splits : 0, tail ? plan->tail_units : 0,
+                             tail ? plan->tail_splits : 0);
     std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
     for (int e = 0; e < E; ++e) {
         cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
@@ -674,7 +722,9 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
         pref[i + 1] = pref[i] + cnt[order[i]];
         spref[i + 1] = spref[i] + expert_splits(g, off[i + 1] - off[i]);
     }
-    const int64_t units = pref[E];
+    std::vector<int32_t> off_v(off, off + E + 1);
+    if (g.tail > 0 && !tail_active(g, off_v.data(), order.data())) g.tail = g.tail_s = 0;
+    const int64_t units = walk_length(g, pref[E]);
     int64_t n = 0;
     for (int64_t t = 0; t < units; ++t) {
         const int ranks = g.csplit > 0 ? g.csplit : g.pair;

@@ -71,6 +71,8 @@ struct KParams {
     int32_t debug_flags;
     int32_t prefetch;       // weight gradient: L2 prefetch distance in stages (0 = off)
     int32_t dyn;            // units fetched from a global counter (else a static stride)
+    int32_t tail;           // weight gradient: split tail units ...
+    int32_t tail_s;         // ... and pieces per tail unit (0 = none)
     int32_t *sched;         // [0]: next unit, [32]: CTAs retired (zero between calls)
     uint64_t timeout_ns;
 };
@@ -379,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
     const int E = p.E;
     const int csplit = MODE == kModeWgrad ? p.csplit : 0;
-    const Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit);
+    Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit,
+                       MODE == kModeWgrad ? p.tail : 0, MODE == kModeWgrad ? p.tail_s : 0);
     // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + r
     // as one 256-row MMA (the even CTA issues it; each CTA holds its A rows and
     // half of the B tile); a cluster split (csplit CTAs) computes one tile,
@@ -569,7 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after_sync();
 
-    const int64_t total = c->pref[E];
+    if (MODE == kModeWgrad && g.tail > 0 && !tail_active(g, c->off, c->order)) g.tail = g.tail_s = 0;
+    const int64_t total = walk_length(g, c->pref[E]);
     const uint32_t tmem_base = c->tmem_base;
     const uint32_t acc_stride = uint32_t(p.tmem_cols) / 2;
 
@@ -925,9 +929,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 
+            // partial slots per split (deterministic mode and tail pieces), or one
+            // accumulator per output tile (non-deterministic global splits)
+            const bool slots = p.det || ti.tail;
             float *slot_ptr = nullptr;
             if (split) {
-                slot_ptr = p.det ? p.partials + ti.slot * int64_t(kTileM) * p.bn
+                slot_ptr = slots ? p.partials + ti.slot * int64_t(kTileM) * p.bn
                                  : p.partials + int64_t(ti.ticket) * kTileM * p.bn;
             }
 
@@ -1006,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         float *dst = slot_ptr + (int64_t((c0 >> 2) + j4) * kTileM + lrow) * 4;
-                        if (p.det)
+                        if (slots)
                             *reinterpret_cast<float4 *>(dst) =
                                 make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
                         else
@@ -1046,9 +1053,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, 128);  // everyone read last_flag before the next tile rewrites it
                 if (last) {
                     __threadfence();
-                    float *base0 = p.det ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
+                    float *base0 = slots ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
                                                : slot_ptr;
-                    const int nsum = p.det ? ti.S : 1;
+                    const int nsum = slots ? ti.S : 1;
                     const int64_t slot_stride = int64_t(kTileM) * p.bn;
                     // 4 float4 columns x up to 4 slots per batch: 16 independent loads in flight
                     for (int c4 = 0; c4 < p.bn / 4; c4 += 4) {
@@ -1062,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (s0 + u < nsum)
                                         b[u][j] = __ldcg(reinterpret_cast<const float4 *>(
                                             base0 + (s0 + u) * slot_stride + (int64_t(c4 + j) * kTileM + lrow) * 4));
-                            if (!p.det) {
+                            if (!slots) {
                                 // the atomic accumulator is read only here: leave it zeroed for the next call
 #pragma unroll
                                 for (int j = 0; j < 4; ++j)

@@ -60,15 +60,19 @@ struct Geom {
     int32_t pair;         // CTAs per unit (1, or 2 for a multicast pair)
     int32_t bk;           // reduction elements per pipeline stage (64 * k-chunks per stage)
     int32_t csplit;       // weight gradient: splits of a tile run by one cluster (0 = off)
+    int32_t tail;         // weight gradient: the last `tail` units of the walk are split ...
+    int32_t tail_s;       // ... into tail_s pieces each (0 = no tail split)
 };
 
 CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
                        int32_t swap, int32_t kchunk, int32_t pair = 1, int32_t bk = kTileK,
-                       int32_t csplit = 0)
+                       int32_t csplit = 0, int32_t tail = 0, int32_t tail_s = 0)
 {
     Geom g;
+    g.tail = tail_s > 1 ? tail : 0;
+    g.tail_s = tail_s > 1 ? tail_s : 0;
     g.pair = pair;
     g.bk = bk;
     g.csplit = csplit;
@@ -143,7 +147,29 @@ struct Tile {
     int32_t ticket;   // wgrad: output tile index e * (m_tiles_w * n_tiles) + mt * n_tiles + nt
     int64_t slot;     // wgrad split: partial slot of this split
     bool valid;       // false for a pair rank whose tile lies past the output
+    bool tail;        // a piece of a split tail unit (partials in slots, also when non-deterministic)
 };
+
+// A split tail pays only when the walk's last units are full length: with
+// skewed experts the last units (the lightest expert's, heaviest-first order)
+// are short already.  On: the lightest expert costs at least 80% of the
+// heaviest.  A function of the offsets alone, so every CTA (and the host
+// walk) decides alike.
+CAKE_HD bool tail_active(const Geom &g, const int32_t *off, const int32_t *order)
+{
+    if (g.mode != kModeWgrad || g.tail <= 0) return false;
+    const int32_t e_hi = order[0], e_lo = order[g.E - 1];
+    const int64_t c_hi = expert_cost(g, off[e_hi + 1] - off[e_hi]);
+    const int64_t c_lo = expert_cost(g, off[e_lo + 1] - off[e_lo]);
+    return 5 * c_lo >= 4 * c_hi;
+}
+
+// Positions in the walk: the weight gradient's last g.tail units each take
+// g.tail_s positions (one per piece).
+CAKE_HD int64_t walk_length(const Geom &g, int64_t units)
+{
+    return units + int64_t(g.tail) * (g.tail_s > 1 ? g.tail_s - 1 : 0);
+}
 
 // Tables: off[E+1] offsets; order[E] processing position -> expert;
 // pref[E+1] tile prefix in processing order; spref[E+1] split prefix by
@@ -151,6 +177,18 @@ struct Tile {
 CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int32_t *order,
                          const int32_t *pref, const int32_t *spref, int32_t rank = 0)
 {
+    // a piece of a split tail unit: position -> (unit, piece)
+    int32_t tail_piece = -1;
+    int64_t tail_unit = 0;
+    if (g.mode == kModeWgrad && g.tail > 0) {
+        const int64_t main_units = int64_t(pref[g.E]) - g.tail;
+        if (t >= main_units) {
+            const int64_t j = t - main_units;
+            tail_unit = j / g.tail_s;
+            tail_piece = int32_t(j - tail_unit * g.tail_s);
+            t = main_units + tail_unit;
+        }
+    }
     // last position p with pref[p] <= t (positions of empty experts have
     // pref[p] == pref[p+1] and are never selected since t < pref[E])
     int32_t lo = 0, hi = g.E - 1;
@@ -159,6 +197,7 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         if (static_cast<int64_t>(pref[mid]) <= t) lo = mid; else hi = mid - 1;
     }
     Tile ti;
+    ti.tail = false;
     const int32_t e = order[lo];
     const int32_t local = static_cast<int32_t>(t - pref[lo]);
     const int32_t r0 = off[e];
@@ -200,6 +239,17 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         ti.slot = (static_cast<int64_t>(spref[e]) * g.m_tiles_w * g.n_tiles) +
                   static_cast<int64_t>(ti.mt * g.n_tiles + ti.nt) * S + s;
         ti.valid = ti.mt < g.m_tiles_w;
+        if (tail_piece >= 0) {
+            // piece `tail_piece` of the expert's k-blocks, split into g.tail_s
+            // contiguous chunks; slots per (tail unit, pair rank, piece)
+            const int32_t ch = ceil_div_i(nkb_e, g.tail_s);
+            ti.s = tail_piece;
+            ti.S = g.tail_s;
+            ti.kb0 = tail_piece * ch < nkb_e ? tail_piece * ch : nkb_e;
+            ti.kb1 = (tail_piece + 1) * ch < nkb_e ? (tail_piece + 1) * ch : nkb_e;
+            ti.slot = (tail_unit * g.pair + rank) * g.tail_s + tail_piece;
+            ti.tail = true;
+        }
     } else {
         ti.mt = (local / g.n_tiles) * g.pair + rank;
         ti.nt = local % g.n_tiles;

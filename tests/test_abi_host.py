@@ -96,7 +96,11 @@ def test_thin_weight_gradient_swaps_and_splits():
     p = gg.cake_gg_plan("wgrad", 1, 16384, 48, 4096, "fp32", 1)
     assert p.swap_ab == 1 and p.tile_n == 64 and (p.split_chunk > 0 or p.cluster_splits > 1)
     q = gg.cake_gg_plan("wgrad", 8, 131072, 3072, 4096, "bf16", 1)
-    assert q.swap_ab == 0 and q.split_chunk == 0 and q.workspace_bytes == 256
+    assert q.swap_ab == 0 and q.split_chunk == 0
+    # 1536 pair units = 20 waves of 76 pairs + 16: those 16 run as 4 pieces each, through
+    # FP32 partial slots (16 units x 2 CTAs x 4 pieces x 128 x 256 floats) and per-tile tickets
+    assert (q.tail_units, q.tail_splits) == (16, 4)
+    assert q.workspace_bytes >= 256 + 16 * 2 * 4 * 128 * 256 * 4
 
 
 def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
@@ -134,8 +138,9 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
             # contiguous partition of [0, nkb)
             assert lst[0][2] == 0 and lst[-1][3] == nkb
             for a, b in zip(lst, lst[1:]):
-                # cluster splits give every tile csplit ranks; trailing ones may be empty
-                assert a[3] == b[2] and (b[2] < b[3] or plan.cluster_splits > 0)
+                # cluster splits and split tails give every tile a fixed piece count;
+                # trailing pieces of a short expert may be empty
+                assert a[3] == b[2] and (b[2] < b[3] or plan.cluster_splits > 0 or plan.tail_splits > 0)
             assert len({x[4] for x in lst}) == 1
             cover[e, mt * bm:min((mt + 1) * bm, mdim), nt * bn:min((nt + 1) * bn, ndim)] += 1
         assert (cover == 1).all()
@@ -199,3 +204,22 @@ def test_compute_calls_reject_bad_arguments_before_any_cuda_call():
     wplan = gg.cake_gg_plan("wgrad", 1, 16384, 48, 4096, "fp32", 1)
     assert gg.cake_gg_wgrad(wplan, good, good, good, good, "fp32", 1, good,
                             wplan.workspace_bytes - 1, 0) == gg.CAKE_GG_ERR_WORKSPACE
+
+
+def test_tile_walk_split_tail():
+    """The last partial wave of weight-gradient units runs as pieces: every output element is still
+    covered once, each tail tile's pieces partition its expert's k-blocks, the rest stay whole."""
+    plan, tiles = _check_walk_coverage("wgrad", [16384] * 8, N=3072, K=4096)
+    assert plan.tail_units == 16 and plan.tail_splits == 4
+    pieces = [t for t in tiles if t[4] > 1]
+    assert len(pieces) == plan.tail_units * plan.pair * plan.tail_splits
+    assert len(tiles) - len(pieces) == (8 * 12 * 16 - plan.tail_units) * plan.pair
+    # nearly balanced experts: the pieces belong to the lightest expert, walked last
+    plan, tiles = _check_walk_coverage("wgrad", [8300, 8200, 8192, 8100], N=3072, K=4096)
+    assert (plan.tail_units, plan.tail_splits) == (8, 8)
+    assert {t[0] for t in tiles if t[4] > 1} == {3}
+    # skewed experts (lightest below 80% of the heaviest): the plan reserves a tail, the walk
+    # keeps every unit whole (its last units are short already)
+    plan, tiles = _check_walk_coverage("wgrad", [59491, 25895, 15919, 11271], N=6144, K=2048)
+    assert plan.tail_splits > 1
+    assert not [t for t in tiles if t[4] > 1]

@@ -178,3 +178,25 @@ def test_pages_grid_rows(shape, passes):
     rng = np.random.default_rng(7)
     for p in passes:
         run_and_check(wk, p, od if p == "wgrad" else "bf16", 1, rng)
+
+
+TAIL = wl.Workload("tail_E4_M32792_K4096_N3072", 4, 3072, 4096, [8300, 8200, 8192, 8100])
+
+
+@pytest.mark.parametrize("det,out_dtype", [(1, "fp32"), (0, "bf16"), (1, "bf16")])
+def test_split_tail(det, out_dtype):
+    """768 pair units = 10 waves of 76 + 8: the last 8 (the lightest expert's, 8100 rows, its last
+    k-block partial) run as 8 pieces each; sampled outputs against the oracle."""
+    plan = gg.cake_gg_plan("wgrad", TAIL.E, TAIL.M, TAIL.N, TAIL.K, out_dtype, det)
+    assert (plan.tail_units, plan.tail_splits) == (8, 8)
+    run_and_check(TAIL, "wgrad", out_dtype, det, np.random.default_rng(8))
+
+
+def test_split_tail_bitwise_across_sm_caps():
+    import torch
+    X, W, G, _ = inputs(TAIL)
+    offs = torch.from_numpy(TAIL.offsets).cuda()
+    ref = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1)
+    for cap in (100, 148, 7, 0):
+        out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1, max_sms=cap)
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"max_sms={cap}"
