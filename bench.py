@@ -70,8 +70,11 @@ def get_workload(name):
     if name == "moe_gate_up":
         return wl.moe_gate_up()
     if name == "moe_gate_up_m16k":
-        w = wl.moe_gate_up()
         return wl.Workload("moe_gate_up_E8_M16384_K4096_N3072", 8, 3072, 4096, wl.balanced_sizes(8, 16384))
+    if name == "moe_gate_up_e2":
+        # two gate_up experts of 16384 rows: the per-expert working set of the full
+        # step (above the L2) at a quarter of its device memory, for profiling
+        return wl.Workload("moe_gate_up_E2_M32768_K4096_N3072", 2, 3072, 4096, wl.balanced_sizes(2, 32768))
     if name == "moe_down":
         return wl.moe_down()
     if name == "moe_skew":
