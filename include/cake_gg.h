@@ -19,8 +19,10 @@
  * Deterministic mode (PR #8258: "bitwise reproducible from run to run"): every
  * output element is computed by a fixed sequence of FP32 operations that
  * depends only on (pass, E, M_max, N, K, out_dtype) and the offsets -- never on
- * max_sms, on which CTA runs a tile, or on arrival order.  Split reductions
- * add FP32 partials in split order and round once.  Non-deterministic mode
+ * max_sms, on which CTA runs a tile, or on arrival order (the weight
+ * gradient takes its tiles from a counter at run time; the results are the
+ * same bits whichever CTA computes a tile).  Split reductions add FP32
+ * partials in split order and round once.  Non-deterministic mode
  * (PR #8258: tail partial tiles added "into a shared FP32 sum with atomic
  * reductions", last CTA per tile found by a "per-tile ticket") may change the
  * order of the weight gradient's split sums from run to run.  The forward and
@@ -38,7 +40,8 @@
  * (and again after a device-detected error).  Every call that ends without a
  * device-detected error leaves it ready for the next call, so no call clears
  * it.  Split-tile tickets are tagged with a per-call number and never need
- * clearing.
+ * clearing; the weight gradient's tile counter (workspace header) is zeroed
+ * by the last CTA of each call.
  *
  * Errors: host-detected problems return a non-zero cake_gg_status_t and
  * enqueue nothing.  Problems only the GPU can see (bad offsets, a bounded wait
@@ -184,8 +187,9 @@ const char *cake_gg_strerror(int code);
 /* Host-side replica of the kernel's tile walk, for testing the scheduler on
  * any machine.  Given host offsets[E+1], writes up to `capacity` tiles, each
  * as 8 int32 {expert, m_tile, n_tile, split, n_splits, kblock_begin,
- * kblock_end, ticket}, in the order the persistent CTAs take them, and stores
- * the total tile count in *count.  Returns CAKE_GG_ERR_BAD_OFFSETS for offsets
+ * kblock_end, ticket}, in walk order (heaviest expert first for the weight
+ * gradient; the order in which the CTAs take them from the tile counter, or
+ * by a fixed stride), and stores the total tile count in *count.  Returns CAKE_GG_ERR_BAD_OFFSETS for offsets
  * the kernel would reject. */
 int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *offsets_host,
                       int64_t capacity, int32_t *tiles_out, int64_t *count);
