@@ -97,6 +97,16 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, dist, device):
+    """The largest value over the ranks (a timing is the slowest rank's); `dist` None = one rank."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -299,9 +309,7 @@ def run_ours(args, wk):
                        for j, p in enumerate(passes)}
     if dist is not None:
         dist.barrier()
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     clocks = sampler.finish() if sampler else None
 
     flop_step = wk.flops(len(passes))
@@ -341,11 +349,7 @@ def run_ours(args, wk):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b)
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
         e2e = {"value": flop_step * args.e2e_steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms / args.e2e_steps}

@@ -83,6 +83,29 @@ def test_noalloc_matches_workspace_entry_point(sizes, N, K, env, out_dtype, det,
                                ref.view(torch.int16 if out_dtype == "bf16" else torch.int32)), f"call {call}"
 
 
+@pytest.mark.parametrize("out_dtype,det", [("bf16", 1), ("fp32", 0)])
+def test_noalloc_with_a_split_tail_matches_bitwise(out_dtype, det):
+    """A plan whose last partial wave runs as split pieces (16 MB of partial slots inside the
+    fixed scratch): two calls in a row give the workspace entry point's bits (tail pieces are
+    summed in piece order in both modes)."""
+    import torch
+    sizes, N, K = [8300, 8200, 8192, 8100], 3072, 4096
+    Xb, Gb, off = _inputs(sizes, N, K, seed=23)
+    E, M = len(sizes), Xb.shape[0]
+    X, G = wl.to_torch_bf16(Xb, "cuda"), wl.to_torch_bf16(Gb, "cuda")
+    offs = torch.from_numpy(off).cuda()
+    plan = gg.cake_gg_plan("wgrad", E, M, N, K, out_dtype, det)
+    assert plan.tail_splits == 8 and plan.workspace_bytes <= gg.CAKE_GG_NOALLOC_SCRATCH_BYTES
+    ref = gg.grouped_gemm("wgrad", G, X, offs, out_dtype=out_dtype, deterministic=det, plan=plan)
+    iv = torch.int16 if out_dtype == "bf16" else torch.int32
+    for call in range(2):
+        dW = torch.full_like(ref, float("nan"))
+        rc = gg.cake_gg_wgrad_noalloc(plan, G, X, dW, offs, out_dtype, det)
+        assert rc == gg.CAKE_GG_OK, gg.cake_gg_strerror(rc)
+        torch.cuda.synchronize()
+        assert torch.equal(dW.view(iv), ref.view(iv)), f"call {call}"
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     import torch
     # T = 2^20 rows of a thin projection needs far more partial-tile scratch than the fixed maximum
