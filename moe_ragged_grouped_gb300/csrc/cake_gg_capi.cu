@@ -85,6 +85,7 @@ int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn
 
 int tmem_cols_for(int bn)
 {
+    if (bn > 256) return 512;  // one 512-column accumulator
     int cols = 32;
     while (cols < 2 * bn) cols <<= 1;
     return cols;
@@ -274,7 +275,9 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
     if (plan->tile_m != kTileM || (plan->tile_k != 64 && plan->tile_k != 128 && plan->tile_k != 256) ||
         (plan->pair != 1 && plan->pair != 2) ||
         (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
-        plan->tile_n < 64 || plan->tile_n > 256 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
+        plan->tile_n < 64 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
+        (plan->tile_n > 256 && (plan->tile_n != 512 || pass != CAKE_GG_WGRAD || plan->pair != 2 || plan->swap_ab ||
+                                plan->tile_k != 64 || plan->cluster_splits > 0)) ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
         (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
         plan->cluster_splits > kMaxClusterSplit ||
@@ -328,7 +331,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     std::memset(&mo, 0, sizeof mo);
     // MN-major operands through atom-stacked maps (one box per operand and stage)
     const bool stack_ok = env_int("CAKE_GG_STACK", 1) != 0;
-    const int b_atoms = (bn / 64) / plan->pair;  // B atoms this CTA loads per stage
+    // B atoms per box: this CTA's share of the tile (of each 256-column half of a 512-wide one)
+    const int b_atoms = (bn > 256 ? 256 / 64 : bn / 64) / plan->pair;
     const int bk = plan->tile_k, kps = bk / 64;
     bool stack_a = false, stack_b = false, chunk_a = false, chunk_b = false;
     const bool tma_store = env_int("CAKE_GG_TMA_STORE", 1) != 0 && !(mode == kModeWgrad && plan->swap_ab);
@@ -401,6 +405,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
         if (!stack_a && (rc = encode_map(&ma, pa, 2, da, 64, uint32_t(bk))) != CAKE_GG_OK) return rc;
         if (!stack_b && (rc = encode_map(&mb, pb, 2, db, 64, uint32_t(bk))) != CAKE_GG_OK) return rc;
     }
+
+    if (bn > 256 && !stack_b) return CAKE_GG_ERR_UNSUPPORTED;  // wide tiles load B through stacked maps
 
     KParams p{};
     p.offsets = offsets;
@@ -537,6 +543,16 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->pair = (bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab)) ? 2 : 1;
     const int env_pair = env_int("CAKE_GG_PAIR", -1);
     if (env_pair == 0) plan->pair = 1;
+    // long weight-gradient units: a pair takes a 256 x 512 tile (two N = 256
+    // MMAs sharing each A stage; TMEM holds one accumulator): a quarter fewer
+    // operand bytes per flop, and a wave covers twice an expert's tile area
+    bool wide = false;
+    if (pass == CAKE_GG_WGRAD && plan->pair == 2 && !plan->swap_ab && bn == 256 && K >= 1024 &&
+        M_max / E >= 8192 && env_int("CAKE_GG_WIDE", 1) != 0) {
+        bn = 512;
+        plan->tile_n = bn;
+        wide = true;
+    }
     // deeper stages (two 64-deep k-chunks) for the memory-bound thin shapes:
     // one TMA box then moves 32 KB of the streamed operand, which a CTA pulls
     // from HBM about twice as fast as 16 KB boxes
@@ -554,6 +570,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     }
     const int env_bk = env_int("CAKE_GG_TILE_K", 0);
     if ((env_bk == 64 || env_bk == 128 || env_bk == 256) && (env_bk == 64 || chunkable)) bk = env_bk;
+    if (wide) bk = 64;  // 48 KB stages, four deep
     plan->tile_k = bk;
 
     // deeper stages only while at least two of them fit
@@ -606,6 +623,9 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
             int64_t S = P / T;
             if (S > kMaxTailSplits) S = kMaxTailSplits;
             while (S > 1 && kb_per_unit < 4 * S) --S;   // pieces of at least ~4 stages
+            // partial slots of at most 16 MiB (T units x pair x S pieces x one FP32 tile)
+            const int64_t tile_bytes = int64_t(kTileM) * bn * 4;
+            while (S > 1 && T * plan->pair * S * tile_bytes > (int64_t(16) << 20)) --S;
             if (S >= 2) {
                 plan->tail_units = int32_t(T);
                 plan->tail_splits = int32_t(S);

@@ -576,6 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t total = walk_length(g, c->pref[E]);
     const uint32_t tmem_base = c->tmem_base;
     const uint32_t acc_stride = uint32_t(p.tmem_cols) / 2;
+    // a 512-wide tile fills TMEM: one accumulator, released before the next unit
+    const int nacc = p.bn > 256 ? 1 : 2;
 
     if (warp == 0) {
         // ======================= TMA producer =======================
@@ -657,7 +659,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
                                 tma_load_2d(sa + atom_a, &mapA, fb, ti.mt * kTileM + 64, r);
                             }
-                            if (p.stack_b) {
+                            if (p.stack_b && p.bn > 256) {
+                                // a 512-wide tile: this CTA's half of each 256-column MMA tile
+                                const int hb = 256 / 64 / PAIR;   // atoms per half per CTA
+                                tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + rank * hb);
+                                tma_load_3d(sb + uint32_t(hb) * atom_b, &mapB, fb, 0, r, ti.nt * nb + 4 + rank * hb);
+                            } else if (p.stack_b) {
                                 tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + jb0);
                             } else {
                                 for (int j = jb0; j < jb1; ++j)
@@ -705,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ======================= MMA issuer =======================
         // (the odd CTA of a pair issues none: it zeroes its stale rows of each
         // loaded stage and relays "stage loaded" to the even CTA's full barrier)
-        const uint32_t idesc = idesc_bf16_f32(kTileM * PAIR, uint32_t(p.bn), A_MN, B_MN);
+        // (a 512-wide tile is two MMAs of N = 256 per k-step, into TMEM columns 0 and 256)
+        const uint32_t idesc = idesc_bf16_f32(kTileM * PAIR, uint32_t(p.bn > 256 ? 256 : p.bn), A_MN, B_MN);
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -714,8 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, ok); ++it) {
             const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
-            const int acc = it & 1;
-            const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
+            const int acc = nacc == 2 ? (it & 1) : 0;
+            const uint32_t acc_phase = nacc == 2 ? (uint32_t(it >> 1) & 1u) : (uint32_t(it) & 1u);
             if (leader) {
                 // every epilogue warp (of both CTAs of a pair) released this buffer
                 if (!warp_wait(smem_u32(&c->tempty[acc]), acc_phase ^ 1u, c, p)) {
@@ -753,7 +761,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t ad0 = A_MN ? smem_desc_sw128(sa, atom_a, 1024) : smem_desc_sw128(sa, 16, 1024);
                         const uint64_t bd0 = B_MN ? smem_desc_sw128(sb, atom_b, 1024) : smem_desc_sw128(sb, 16, 1024);
                         const bool first = kb == ti.kb0;
-                        if (kps == 1) issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                        if (p.bn > 256) {
+                            // this CTA's halves of the two 256-column B tiles sit 2 * (128 / PAIR / 64) atoms apart
+                            const uint32_t half = uint32_t(256 / 64 / PAIR) * atom_b;
+                            const uint64_t bd1 = smem_desc_sw128(sb + half, atom_b, 1024);
+                            issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                            issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem + 256u, ad0, bd1, idesc, first, chunk_b);
+                        } else if (kps == 1)
+                            issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                         else if (kps == 2) issue_stage_mmas<2, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                         else issue_stage_mmas<4, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                         // the stage is free again in both CTAs once these MMAs complete
@@ -795,8 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, qok); ++it) {
             const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
-            const int acc = it & 1;
-            const uint32_t acc_phase = uint32_t(it >> 1) & 1u;
+            const int acc = nacc == 2 ? (it & 1) : 0;
+            const uint32_t acc_phase = nacc == 2 ? (uint32_t(it >> 1) & 1u) : (uint32_t(it) & 1u);
             // (in a pair the even CTA's MMA commit arrives on both CTAs' tfull)
             bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
             ok = named_bar_and(1, 128, ok);

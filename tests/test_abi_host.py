@@ -89,7 +89,7 @@ def test_plan_choices_do_not_depend_on_max_sms(pass_, shape):
     for p in plans[1:]:
         for key in ("tile_m", "tile_n", "tile_k", "stages", "swap_ab", "split_chunk", "workspace_bytes"):
             assert p[key] == plans[0][key]
-    assert plans[0]["tile_n"] % 64 == 0 and 64 <= plans[0]["tile_n"] <= 256
+    assert plans[0]["tile_n"] % 64 == 0 and (64 <= plans[0]["tile_n"] <= 256 or plans[0]["tile_n"] == 512)
 
 
 def test_thin_weight_gradient_swaps_and_splits():
@@ -97,10 +97,11 @@ def test_thin_weight_gradient_swaps_and_splits():
     assert p.swap_ab == 1 and p.tile_n == 64 and (p.split_chunk > 0 or p.cluster_splits > 1)
     q = gg.cake_gg_plan("wgrad", 8, 131072, 3072, 4096, "bf16", 1)
     assert q.swap_ab == 0 and q.split_chunk == 0
-    # 1536 pair units = 20 waves of 76 pairs + 16: those 16 run as 4 pieces each, through
-    # FP32 partial slots (16 units x 2 CTAs x 4 pieces x 128 x 256 floats) and per-tile tickets
-    assert (q.tail_units, q.tail_splits) == (16, 4)
-    assert q.workspace_bytes >= 256 + 16 * 2 * 4 * 128 * 256 * 4
+    # long units: 256 x 512 pair tiles, 768 units = 10 waves of 76 pairs + 8; those 8 run as 4
+    # pieces each through FP32 partial slots (8 units x 2 CTAs x 4 pieces x 128 x 512 floats)
+    assert q.tile_n == 512 and q.tile_k == 64
+    assert (q.tail_units, q.tail_splits) == (8, 4)
+    assert q.workspace_bytes >= 256 + 8 * 2 * 4 * 128 * 512 * 4
 
 
 def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
@@ -210,13 +211,13 @@ def test_tile_walk_split_tail():
     """The last partial wave of weight-gradient units runs as pieces: every output element is still
     covered once, each tail tile's pieces partition its expert's k-blocks, the rest stay whole."""
     plan, tiles = _check_walk_coverage("wgrad", [16384] * 8, N=3072, K=4096)
-    assert plan.tail_units == 16 and plan.tail_splits == 4
+    assert plan.tile_n == 512 and plan.tail_units == 8 and plan.tail_splits == 4
     pieces = [t for t in tiles if t[4] > 1]
     assert len(pieces) == plan.tail_units * plan.pair * plan.tail_splits
-    assert len(tiles) - len(pieces) == (8 * 12 * 16 - plan.tail_units) * plan.pair
+    assert len(tiles) - len(pieces) == (8 * 12 * 8 - plan.tail_units) * plan.pair
     # nearly balanced experts: the pieces belong to the lightest expert, walked last
     plan, tiles = _check_walk_coverage("wgrad", [8300, 8200, 8192, 8100], N=3072, K=4096)
-    assert (plan.tail_units, plan.tail_splits) == (8, 8)
+    assert (plan.tile_n, plan.tail_units, plan.tail_splits) == (512, 4, 8)
     assert {t[0] for t in tiles if t[4] > 1} == {3}
     # skewed experts (lightest below 80% of the heaviest): the plan reserves a tail, the walk
     # keeps every unit whole (its last units are short already)

@@ -185,10 +185,10 @@ TAIL = wl.Workload("tail_E4_M32792_K4096_N3072", 4, 3072, 4096, [8300, 8200, 819
 
 @pytest.mark.parametrize("det,out_dtype", [(1, "fp32"), (0, "bf16"), (1, "bf16")])
 def test_split_tail(det, out_dtype):
-    """768 pair units = 10 waves of 76 + 8: the last 8 (the lightest expert's, 8100 rows, its last
-    k-block partial) run as 8 pieces each; sampled outputs against the oracle."""
+    """384 pair units of 256 x 512 = 5 waves of 76 + 4: the last 4 (the lightest expert's, 8100
+    rows, its last k-block partial) run as 8 pieces each; sampled outputs against the oracle."""
     plan = gg.cake_gg_plan("wgrad", TAIL.E, TAIL.M, TAIL.N, TAIL.K, out_dtype, det)
-    assert (plan.tail_units, plan.tail_splits) == (8, 8)
+    assert (plan.tile_n, plan.tail_units, plan.tail_splits) == (512, 4, 8)
     run_and_check(TAIL, "wgrad", out_dtype, det, np.random.default_rng(8))
 
 

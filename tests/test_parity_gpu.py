@@ -297,3 +297,28 @@ def test_scheduler_words_return_to_zero():
     out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", plan=gg.cake_gg_plan("wgrad", E, M, 256, 512, "fp32", 1),
                           workspace=ws)
     assert_parity("wgrad", out_to_f64(out), ref, Xb, Wb, Gb, off, "after reuse")
+
+
+@pytest.mark.parametrize("det,out_dtype", [(1, "fp32"), (0, "bf16"), (1, "bf16")])
+def test_wide_weight_gradient_tiles(det, out_dtype):
+    """256 x 512 pair tiles (two N = 256 MMAs per k-step into one 512-column accumulator):
+    an empty expert, a last column tile of 64 (K = 1088), a last pair whose odd CTA lies past
+    N = 384, NaN rows past the last offset."""
+    import torch
+    from moe_ragged_grouped_gb300 import cake_gg as gg_
+    plan = gg_.cake_gg_plan("wgrad", 3, 25004, 384, 1088, out_dtype, det)
+    assert plan.tile_n == 512 and plan.pair == 2
+    check_case("wgrad", [12000, 0, 13000], 384, 1088, out_dtype, det, seed=24, extra_rows=4)
+
+
+def test_wide_tiles_bitwise_equal_to_256_wide(monkeypatch):
+    """Unsplit plans (a split's boundaries depend on the stage depth): every output element sees
+    the same sequence of K = 16 MMA steps in both tile widths."""
+    import torch
+    monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "0")
+    Xb, Wb, Gb, off = make_inputs([12000, 0, 13000], 384, 1088, seed=25)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    wide = run("wgrad", X, W, G, off, "fp32", 1)
+    monkeypatch.setenv("CAKE_GG_WIDE", "0")
+    narrow = run("wgrad", X, W, G, off, "fp32", 1)
+    assert torch.equal(wide.view(torch.int32), narrow.view(torch.int32))
