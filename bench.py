@@ -58,6 +58,9 @@ def parse_args():
                          "back), per-pass times from a separate loop")
     ap.add_argument("--graph", action="store_true",
                     help="replay each pass from a captured CUDA graph (removes host launch overhead)")
+    ap.add_argument("--corun", default="",
+                    help="comma list of SM counts (e.g. 8,16,32): after the timed region, time the same "
+                         "steps again while a spinner on another stream holds that many SMs")
     ap.add_argument("--grid", default="", choices=["", "pages"],
                     help="pages: time the GB300 rows of the pages' per-row latency table")
     ap.add_argument("--grid-filter", default="", help="only rows whose 'shape op' contains this text")
@@ -380,6 +383,33 @@ def run_ours(args, wk):
                      "per_pass_gbs": {p: round(wk.algorithmic_bytes(p, obytes) / (v * 1e-3) / 1e9, 1)
                                       for p, v in per_pass_ms.items()}})
 
+    corun = None
+    if args.corun:
+        # co-run robustness: a bounded spinner holds n SMs for 60 % of the
+        # plain timed region; ideal extra time = the SM-time it takes away
+        corun = {"sms": [], "ms_per_step": [], "slowdown": [], "ideal_slowdown": [], "spin_ms": []}
+        side = torch.cuda.Stream(dev)
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        spin_ms = 0.6 * elapsed_ms
+        for n in (int(v) for v in args.corun.split(",") if v):
+            torch.cuda.synchronize(dev)
+            rc = gg.cake_gg_corun_spinner(n, int(spin_ms * 1e6), side.cuda_stream)
+            if rc != 0:
+                raise gg.CakeGGError(rc, "corun spinner")
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                for p in passes:
+                    run_pass(p)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            t = a.elapsed_time(b)
+            corun["sms"].append(n)
+            corun["ms_per_step"].append(round(t / args.steps, 4))
+            corun["slowdown"].append(round(t / elapsed_ms - 1.0, 4))
+            corun["ideal_slowdown"].append(round(n * spin_ms / nsm / elapsed_ms, 4))
+            corun["spin_ms"].append(round(spin_ms, 3))
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wk, X, W, G, passes, args.cpu_seconds)
@@ -398,6 +428,7 @@ def run_ours(args, wk):
                                      if k in ("tile_n", "tile_k", "stages", "pair", "swap_ab", "split_chunk",
                                               "staging_bufs")} for p in passes}},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            **({"corun": corun} if corun else {}),
             "gpu_launches": len(passes) * args.steps, "clocks": clocks}
     if dist is not None:
         dist.barrier()

@@ -115,8 +115,9 @@ typedef struct cake_gg_plan {
     int32_t reserved[4];
 } cake_gg_plan_t;
 
-/* Debug flag (tests only): CTA 0 arms its first pipeline stage but issues no
- * copy into it, so the consumer's bounded wait expires and the call reports
+/* Debug flag (tests only): the CTA that takes the walk's first unit (its even
+ * CTA, in a pair) arms its first pipeline stage but issues no copy into it, so
+ * the consumer's bounded wait expires and the call reports
  * CAKE_GG_ERR_TIMEOUT through the status word. */
 #define CAKE_GG_DEBUG_DROP_FIRST_LOAD 1
 
@@ -183,6 +184,14 @@ int cake_gg_check_status(const void *workspace, void *stream);
 
 /* Static, never-NULL description of a status code. */
 const char *cake_gg_strerror(int code);
+
+/* Measurement aid (co-run robustness): launch `ctas` CTAs on `stream`, each
+ * holding one SM (it takes the maximum shared memory) for `ns` nanoseconds,
+ * then exiting.  Bounded by time alone; touches no memory.  The grouped-GEMM
+ * calls on another stream then run on the remaining SMs; the weight
+ * gradient's tile counter lets the CTAs that do run take the whole walk.
+ * CAKE_GG_ERR_INVALID_ARG for ctas outside 1..1024 or ns above 10 s. */
+int cake_gg_corun_spinner(int32_t ctas, uint64_t ns, void *stream);
 
 /* Host-side replica of the kernel's tile walk, for testing the scheduler on
  * any machine.  Given host offsets[E+1], writes up to `capacity` tiles, each

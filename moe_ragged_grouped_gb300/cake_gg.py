@@ -37,7 +37,7 @@ PASSES = {"fwd": CAKE_GG_FWD, "dgrad": CAKE_GG_DGRAD, "wgrad": CAKE_GG_WGRAD}
 DTYPES = {"bf16": CAKE_GG_BF16, "fp32": CAKE_GG_FP32}
 
 EXPORTED = ["cake_gg_plan", "cake_gg_fwd", "cake_gg_dgrad", "cake_gg_wgrad",
-            "cake_gg_check_status", "cake_gg_strerror", "cake_gg_tile_walk"]
+            "cake_gg_check_status", "cake_gg_strerror", "cake_gg_tile_walk", "cake_gg_corun_spinner"]
 
 
 class CakeGGPlan(ctypes.Structure):
@@ -101,6 +101,8 @@ def load_library(path: str = LIB_PATH):
         f.argtypes = [plan_p, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, sz, vp]
         f.restype = ctypes.c_int
     lib.cake_gg_check_status.argtypes = [vp, vp]
+    lib.cake_gg_corun_spinner.argtypes = [i32, ctypes.c_uint64, vp]
+    lib.cake_gg_corun_spinner.restype = ctypes.c_int
     lib.cake_gg_check_status.restype = ctypes.c_int
     lib.cake_gg_strerror.argtypes = [ctypes.c_int]
     lib.cake_gg_strerror.restype = ctypes.c_char_p
@@ -204,6 +206,11 @@ def cake_gg_wgrad_noalloc(plan, G, X, dW, offsets, out_dtype, deterministic, str
 def cake_gg_check_status(workspace, stream=None) -> int:
     """cake_gg_check_status(): synchronises the stream and returns the device status word."""
     return load_library().cake_gg_check_status(_ptr(workspace), _stream(stream, workspace))
+
+
+def cake_gg_corun_spinner(ctas, ns, stream) -> int:
+    """cake_gg_corun_spinner(): hold `ctas` SMs for `ns` nanoseconds on `stream` (a cudaStream_t value)."""
+    return load_library().cake_gg_corun_spinner(int(ctas), int(ns), ctypes.c_void_p(int(stream)))
 
 
 def cake_gg_tile_walk(plan, offsets) -> np.ndarray:

@@ -435,10 +435,11 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.csplit = mode == kModeWgrad ? plan->cluster_splits : 0;
     p.debug_flags = plan->debug_flags;
     p.prefetch = mode == kModeWgrad && !plan->swap_ab ? env_int("CAKE_GG_PREFETCH", 0) : 0;
-    // weight-gradient units differ in length (skewed experts): take them from a
-    // global counter in heaviest-first order (the cluster split keeps its
-    // static one-unit-per-cluster walk)
-    p.dyn = mode == kModeWgrad && plan->cluster_splits == 0 && env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
+    // units from a global counter (heaviest first for the weight gradient):
+    // skewed experts balance, and when other work holds some SMs the CTAs that
+    // run take the whole walk instead of waiting for their late peers' shares
+    // (the cluster split keeps its static one-unit-per-cluster walk)
+    p.dyn = plan->cluster_splits == 0 && env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
     p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
     p.tail = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_units : 0;
     p.tail_s = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_splits : 0;
@@ -473,6 +474,17 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
 }
 
 }  // namespace
+
+// Co-run aid: each CTA holds one SM (its shared memory keeps any other CTA
+// off it) for `ns` nanoseconds of global time, sleeping, then exits.  Bounded
+// by time alone; touches no memory.
+__global__ void __launch_bounds__(32, 1) corun_spinner_kernel(uint64_t ns)
+{
+    extern __shared__ uint8_t hold[];
+    (void)hold;
+    const uint64_t t0 = cakegg::global_timer_ns();
+    while (cakegg::global_timer_ns() - t0 < ns) __nanosleep(2000);
+}
 
 extern "C" {
 
@@ -710,6 +722,23 @@ int cake_gg_check_status(const void *workspace, void *stream)
     if (cudaMemsetAsync(const_cast<void *>(workspace), 0, sizeof st, s) != cudaSuccess) return CAKE_GG_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return CAKE_GG_ERR_CUDA;
     return st;
+}
+
+int cake_gg_corun_spinner(int32_t ctas, uint64_t ns, void *stream)
+{
+    if (ctas < 1 || ctas > 1024 || ns > 10000000000ull) return CAKE_GG_ERR_INVALID_ARG;
+    DevInfo dev;
+    int rc = device_info(&dev);
+    if (rc != CAKE_GG_OK) return rc;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(corun_spinner_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemOptInLimit)) != cudaSuccess)
+            return CAKE_GG_ERR_CUDA;
+        attr = true;
+    }
+    corun_spinner_kernel<<<ctas, 32, kSmemOptInLimit, static_cast<cudaStream_t>(stream)>>>(ns);
+    return cudaGetLastError() == cudaSuccess ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
 }
 
 int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t capacity,

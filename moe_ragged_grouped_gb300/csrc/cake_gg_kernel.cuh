@@ -242,7 +242,7 @@ __device__ __forceinline__ bool warp_next_unit(UnitSeq &u, int64_t unit0, int64_
     __syncwarp();
     if (lane == 0) {
         if (leader) mbar_arrive(smem_u32(&c->uq_empty[slot]));
-        else mbar_arrive_cluster(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
+        else mbar_arrive_remote(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
     }
     ++u.pos;
     return u.t >= 0;
@@ -607,21 +607,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     t = int64_t(nxt) < total ? int64_t(nxt) : -1;
                     c->uq[slot] = t;
-                    if (PAIR == 2) st_shared_cluster_b64(map_to_cta(smem_u32(&c->uq[slot]), 1), t);
                     mbar_arrive(smem_u32(&c->uq_full[slot]));
-                    if (PAIR == 2) mbar_arrive_cluster(map_to_cta(smem_u32(&c->uq_full[slot]), 1));
+                    // the odd CTA's slot: data and signal in one asynchronous store
+                    // (that CTA armed its barrier for these 8 bytes)
+                    if (PAIR == 2)
+                        st_async_b64(map_to_cta(smem_u32(&c->uq[slot]), 1), t,
+                                     map_to_cta(smem_u32(&c->uq_full[slot]), 1));
                     ++us.pos;
                     if (t < 0) break;
                     nxt = atomicAdd(p.sched, 1);  // in flight while this unit's copies go out
                 } else {
-                    // the odd CTA's producer reads the queue like every other role
+                    // the odd CTA's producer reads the queue like every other role; it
+                    // also arms each slot's barrier for the next 8-byte delivery (the
+                    // even CTA writes a slot again only after every reader released it)
                     const int slot = int(us.pos % kUQ);
+                    if (us.pos == 0)
+                        for (int i = 0; i < kUQ; ++i) mbar_arrive_expect_tx(smem_u32(&c->uq_full[i]), 8u);
                     if (!thread_wait_cluster(smem_u32(&c->uq_full[slot]), uint32_t((us.pos / kUQ) & 1), c, p)) {
                         ok = false;
                         break;
                     }
                     t = *reinterpret_cast<volatile int64_t *>(&c->uq[slot]);
-                    mbar_arrive_cluster(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
+                    if (t >= 0) mbar_arrive_expect_tx(smem_u32(&c->uq_full[slot]), 8u);
+                    mbar_arrive_remote(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
                     ++us.pos;
                     if (t < 0) break;
                 }
@@ -635,7 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
                     const uint32_t sb = sa + a_bytes;
                     mbar_arrive_expect_tx(fb, tx);
-                    const bool drop = (p.debug_flags & 1) && blockIdx.x == 0 && issued == 0;
+                    // test hook: the walk's first unit (whichever CTA takes it) loses its
+                    // first copy on the even / single CTA
+                    const bool drop = (p.debug_flags & 1) && t == 0 && kb == ti.kb0 && rank == 0;
                     if (!drop) {
                         // B atoms this CTA loads: all of them, or its half of a pair's
                         const int nb = p.bn / 64;

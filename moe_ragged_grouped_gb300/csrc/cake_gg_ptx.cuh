@@ -171,6 +171,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Asynchronous 8-byte store into a peer CTA's shared memory whose arrival
+// counts 8 bytes down on the peer's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_b64(uint32_t remote_addr, int64_t v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "l"(v), "r"(remote_bar)
+                 : "memory");
+}
+
 // 8-byte store into a peer CTA's shared memory (address from mapa).
 __device__ __forceinline__ void st_shared_cluster_b64(uint32_t cluster_addr, int64_t v)
 {

@@ -127,7 +127,10 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
         assert (cover[:off[-1]] == 1).all() and (cover[off[-1]:] == 0).all()
     else:
         mdim, ndim = (K, N) if plan.swap_ab else (N, K)
-        cover = np.zeros((len(sizes), mdim, ndim), np.int32)
+        # weight-gradient tiles are aligned bm x bn blocks of each expert's output: coverage
+        # exactly once <=> every (expert, m-tile, n-tile) block appears as one split group
+        n_mt, n_nt = -(-mdim // bm), -(-ndim // bn)
+        cover = np.zeros((len(sizes), n_mt, n_nt), np.int32)
         splits = {}
         for e, mt, nt, s, S, kb0, kb1, ticket in tiles:
             splits.setdefault((e, mt, nt), []).append((s, S, kb0, kb1, ticket))
@@ -143,7 +146,8 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
                 # trailing pieces of a short expert may be empty
                 assert a[3] == b[2] and (b[2] < b[3] or plan.cluster_splits > 0 or plan.tail_splits > 0)
             assert len({x[4] for x in lst}) == 1
-            cover[e, mt * bm:min((mt + 1) * bm, mdim), nt * bn:min((nt + 1) * bn, ndim)] += 1
+            assert 0 <= mt < n_mt and 0 <= nt < n_nt
+            cover[e, mt, nt] += 1
         assert (cover == 1).all()
         # heaviest-first over experts (k-blocks per split, ties by expert index)
         costs = []

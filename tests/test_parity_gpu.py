@@ -322,3 +322,26 @@ def test_wide_tiles_bitwise_equal_to_256_wide(monkeypatch):
     monkeypatch.setenv("CAKE_GG_WIDE", "0")
     narrow = run("wgrad", X, W, G, off, "fp32", 1)
     assert torch.equal(wide.view(torch.int32), narrow.view(torch.int32))
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+def test_results_unchanged_next_to_a_spinner(pass_):
+    """A bounded spinner on another stream holds 32 SMs for 5 ms: CTAs that start late find the
+    unit counter drained or take what is left; the output bits do not change."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs([3000, 0, 5000, 1200], 512, 768, seed=26)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    ref = run(pass_, X, W, G, off, "fp32", 1)
+    side = torch.cuda.Stream()
+    for _ in range(2):
+        assert gg.cake_gg_corun_spinner(32, 5_000_000, side.cuda_stream) == gg.CAKE_GG_OK
+        out = run(pass_, X, W, G, off, "fp32", 1)
+        torch.cuda.synchronize()
+        M = int(off[-1])
+        a, b = (ref, out) if pass_ == "wgrad" else (ref[:M], out[:M])
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_spinner_rejects_bad_arguments():
+    assert gg.cake_gg_corun_spinner(0, 1000, 0) == gg.CAKE_GG_ERR_INVALID_ARG
+    assert gg.cake_gg_corun_spinner(8, 20_000_000_000, 0) == gg.CAKE_GG_ERR_INVALID_ARG
