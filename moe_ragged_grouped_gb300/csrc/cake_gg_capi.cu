@@ -276,7 +276,7 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         (plan->pair != 1 && plan->pair != 2) ||
         (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
         plan->tile_n < 64 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
-        (plan->tile_n > 256 && (plan->tile_n != 512 || pass != CAKE_GG_WGRAD || plan->pair != 2 || plan->swap_ab ||
+        (plan->tile_n > 256 && (plan->tile_n != 512 || plan->pair != 2 || plan->swap_ab ||
                                 plan->tile_k != 64 || plan->cluster_splits > 0)) ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
         (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
@@ -364,8 +364,10 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
             const uint64_t dx[2] = {uint64_t(K), M};
             const uint64_t dw[3] = {uint64_t(K), uint64_t(N), uint64_t(E)};
             if ((rc = encode_map(&ma, opA, 2, dx, 64, kTileM)) != CAKE_GG_OK) return rc;
-            if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(plan->pair == 2 ? bn / 2 : bn))) != CAKE_GG_OK)
-                return rc;
+            // this CTA's W rows per box: all bn, its half of a pair's, or its half of
+            // each 256-column MMA tile of a 512-wide one
+            const int wrows = (bn > 256 ? 256 : bn) / plan->pair;
+            if ((rc = encode_map(&mb, opB, 3, dw, 64, uint32_t(wrows))) != CAKE_GG_OK) return rc;
         }
     } else if (mode == kModeDgrad) {
         if (kps > 1) {
@@ -406,7 +408,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
         if (!stack_b && (rc = encode_map(&mb, pb, 2, db, 64, uint32_t(bk))) != CAKE_GG_OK) return rc;
     }
 
-    if (bn > 256 && !stack_b) return CAKE_GG_ERR_UNSUPPORTED;  // wide tiles load B through stacked maps
+    // wide tiles load an MN-major B through stacked maps (K-major W: plain boxes)
+    if (bn > 256 && !stack_b && mode != kModeFwd) return CAKE_GG_ERR_UNSUPPORTED;
 
     KParams p{};
     p.offsets = offsets;
@@ -559,8 +562,15 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // MMAs sharing each A stage; TMEM holds one accumulator): a quarter fewer
     // operand bytes per flop, and a wave covers twice an expert's tile area
     bool wide = false;
+    const int64_t out_w = pass == CAKE_GG_FWD ? N : K;   // forward / data gradient output width
     if (pass == CAKE_GG_WGRAD && plan->pair == 2 && !plan->swap_ab && bn == 256 && K >= 1024 &&
         M_max / E >= 8192 && env_int("CAKE_GG_WIDE", 1) != 0) {
+        bn = 512;
+        plan->tile_n = bn;
+        wide = true;
+    }
+    if (pass != CAKE_GG_WGRAD && plan->pair == 2 && bn == 256 && out_w % 512 == 0 &&
+        (pass == CAKE_GG_FWD ? K : N) >= 1024 && env_int("CAKE_GG_WIDE_FD", 0) != 0) {
         bn = 512;
         plan->tile_n = bn;
         wide = true;

@@ -684,13 +684,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // K-major A (X or G): all k-chunks of the stage in one box when chunked
                             if (p.chunk_a) tma_load_3d(sa, &mapA, fb, 0, ti.row0, kb * kps);
                             else tma_load_2d(sa, &mapA, fb, k0, ti.row0);
-                            if (MODE == kModeFwd) {
+                            if (MODE == kModeFwd && p.bn > 256) {
+                                // a 512-wide tile: this CTA's half of each 256-row W block
+                                // (K-major: 256 / PAIR rows of 128 bytes per block)
+                                const int32_t wrow = ti.nt * p.bn + rank * (256 / PAIR);
+                                tma_load_3d(sb, &mapB, fb, k0, wrow, ti.e);
+                                tma_load_3d(sb + uint32_t(256 / PAIR) * 128u, &mapB, fb, k0, wrow + 256, ti.e);
+                            } else if (MODE == kModeFwd) {
                                 // this CTA's rows of the W tile: all bn, or its half of a pair's
                                 const int32_t wrow = ti.nt * p.bn + rank * (p.bn / PAIR);
                                 if (p.chunk_b)
                                     tma_load_4d(sb, &mapB, fb, 0, wrow, kb * kps, ti.e);
                                 else
                                     tma_load_3d(sb, &mapB, fb, k0, wrow, ti.e);
+                            } else if (p.stack_b && p.bn > 256) {
+                                // a 512-wide tile: this CTA's half of each 256-column MMA tile
+                                const int hb = 256 / 64 / PAIR;
+                                tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb + rank * hb, ti.e);
+                                tma_load_4d(sb + uint32_t(hb) * atom_b, &mapB, fb, 0, k0, ti.nt * nb + 4 + rank * hb,
+                                            ti.e);
                             } else if (p.stack_b) {
                                 // W as {64, N, K/64, E}: this CTA's atoms of one bk-row block in one box
                                 tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb + jb0, ti.e);
@@ -774,7 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p.bn > 256) {
                             // this CTA's halves of the two 256-column B tiles sit 2 * (128 / PAIR / 64) atoms apart
                             const uint32_t half = uint32_t(256 / 64 / PAIR) * atom_b;
-                            const uint64_t bd1 = smem_desc_sw128(sb + half, atom_b, 1024);
+                            const uint64_t bd1 =
+                                B_MN ? smem_desc_sw128(sb + half, atom_b, 1024) : smem_desc_sw128(sb + half, 16, 1024);
                             issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                             issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem + 256u, ad0, bd1, idesc, first, chunk_b);
                         } else if (kps == 1)

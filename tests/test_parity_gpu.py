@@ -324,6 +324,31 @@ def test_wide_tiles_bitwise_equal_to_256_wide(monkeypatch):
     assert torch.equal(wide.view(torch.int32), narrow.view(torch.int32))
 
 
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+@pytest.mark.parametrize("det,out_dtype", [(1, "bf16"), (0, "fp32")])
+def test_wide_forward_and_data_gradient_tiles(pass_, det, out_dtype, monkeypatch):
+    """256 x 512 pair tiles for the forward (K-major W: two 128-row boxes per CTA) and the data
+    gradient (MN-major W: two stacked boxes per CTA): ragged experts, an empty one, a partial
+    last row tile, NaN rows past the last offset."""
+    monkeypatch.setenv("CAKE_GG_WIDE_FD", "1")
+    plan = gg.cake_gg_plan(pass_, 4, 2037, 1024, 1536, out_dtype, det)
+    assert plan.tile_n == 512 and plan.pair == 2 and plan.tile_k == 64
+    check_case(pass_, [700, 0, 1300, 33], 1024, 1536, out_dtype, det, seed=26, extra_rows=4)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+def test_wide_forward_and_data_gradient_bitwise_equal_to_256_wide(pass_, monkeypatch):
+    """Each output element sees the same sequence of K = 16 MMA steps in both tile widths."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs([1500, 0, 2100], 1024, 1536, seed=27)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    monkeypatch.setenv("CAKE_GG_WIDE_FD", "1")
+    wide = run(pass_, X, W, G, off, "fp32", 1)
+    monkeypatch.setenv("CAKE_GG_WIDE_FD", "0")
+    narrow = run(pass_, X, W, G, off, "fp32", 1)
+    assert torch.equal(wide.view(torch.int32), narrow.view(torch.int32))
+
+
 @pytest.mark.parametrize("pass_", PASSES)
 def test_results_unchanged_next_to_a_spinner(pass_):
     """A bounded spinner on another stream holds 32 SMs for 5 ms: CTAs that start late find the
