@@ -57,7 +57,7 @@ int env_int(const char *name, int dflt)
 // (expressed in k-block equivalents) -- returned as k-blocks per split
 // (0 = no split).  A pure function of the problem: never of the CTA count
 // a launch uses, so deterministic results do not depend on max_sms.
-int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn, int bk)
+int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn, int bk, int64_t tail_s)
 {
     if (out_tiles <= 0 || kblocks_per_expert < 2 * kMinSplitChunk) return 0;
     const double kps = bk / 64.0;
@@ -66,6 +66,13 @@ int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn
     const double c_split = partial_kb + 4.0 / kps;
     auto cost = [&](int64_t S) {
         const int64_t units = out_tiles * S;
+        if (S == 1 && tail_s > 1) {
+            // unsplit with a split tail: full waves, then the last partial wave's
+            // units as tail_s pieces (about 1 / tail_s of a wave) and one finish
+            const int64_t full = units / kWaveCtas;
+            const double per = double(kblocks_per_expert);
+            return double(full) * per + (units % kWaveCtas ? per / double(tail_s) + c_split : 0.0);
+        }
         const int64_t waves = (units + kWaveCtas - 1) / kWaveCtas;
         const double per = double(kblocks_per_expert) / double(S) + (S > 1 ? c_split : 0.0);
         return double(waves) * per;
@@ -81,6 +88,37 @@ int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn
     }
     if (best_s == 1) return 0;
     return int32_t((kblocks_per_expert + best_s - 1) / best_s);
+}
+
+// Split tail of an unsplit weight gradient: the last partial wave of
+// equal-length units (U mod P units for P = 152 CTAs / pair, a fixed wave so
+// the plan never depends on max_sms) runs as S pieces each, filling about one
+// more wave of 1/S length instead of a whole wave with few units.  Returns the
+// tail's (units, pieces), or (0, 0) when it does not pay.
+void choose_tail(int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn, int32_t bk, int32_t pair,
+                 int32_t *tail_units, int32_t *tail_splits)
+{
+    *tail_units = 0;
+    *tail_splits = 0;
+    const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, 0, 0, pair, bk);
+    const int64_t units = int64_t(E) * m_units_w(g) * g.n_tiles;
+    const int64_t P = kWaveCtas / pair;
+    const int64_t T = units % P;
+    const int64_t kb_per_unit = (M_max / E) / bk;
+    // long units only: on short ones the pieces' partial-sum finish costs
+    // about what the shorter last wave saves
+    if (units > P && T > 0 && 2 * T <= P && kb_per_unit >= 64) {
+        int64_t S = P / T;
+        if (S > kMaxTailSplits) S = kMaxTailSplits;
+        while (S > 1 && kb_per_unit < 4 * S) --S;   // pieces of at least ~4 stages
+        // partial slots of at most 16 MiB (T units x pair x S pieces x one FP32 tile)
+        const int64_t tile_bytes = int64_t(kTileM) * bn * 4;
+        while (S > 1 && T * pair * S * tile_bytes > (int64_t(16) << 20)) --S;
+        if (S >= 2) {
+            *tail_units = int32_t(T);
+            *tail_splits = int32_t(S);
+        }
+    }
 }
 
 int tmem_cols_for(int bn)
@@ -563,8 +601,13 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // operand bytes per flop, and a wave covers twice an expert's tile area
     bool wide = false;
     const int64_t out_w = pass == CAKE_GG_FWD ? N : K;   // forward / data gradient output width
+    // (only when those tiles fill at least half a wave of pairs: fewer, larger
+    // units leave SMs idle or force a split whose finish the single
+    // accumulator cannot overlap)
+    const int env_wide = env_int("CAKE_GG_WIDE", 1);   // 0 off, 1 by the rule, 2 wherever they fit
+    const int64_t wide_units = int64_t(E) * ((N + 2 * kTileM - 1) / (2 * kTileM)) * ((int64_t(K) + 511) / 512);
     if (pass == CAKE_GG_WGRAD && plan->pair == 2 && !plan->swap_ab && bn == 256 && K >= 1024 &&
-        M_max / E >= 8192 && env_int("CAKE_GG_WIDE", 1) != 0) {
+        M_max / E >= 8192 && (wide_units >= kWaveCtas / 2 || env_wide == 2) && env_wide != 0) {
         bn = 512;
         plan->tile_n = bn;
         wide = true;
@@ -602,7 +645,11 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
         const int64_t tpe = int64_t(g.m_tiles_w) * g.n_tiles;
         if (tpe * E > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
-        plan->split_chunk = choose_split_chunk(tpe * E, (M_max / E + bk - 1) / bk, bn, bk);
+        // the unsplit alternative may finish its last partial wave as a split tail
+        int32_t tu = 0, ts = 0;
+        if (!plan->swap_ab && env_int("CAKE_GG_TAIL", 1) != 0)
+            choose_tail(E, N, K, M_max, bn, bk, plan->pair, &tu, &ts);
+        plan->split_chunk = choose_split_chunk(tpe * E, (M_max / E + bk - 1) / bk, bn, bk, ts);
         const char *es = std::getenv("CAKE_GG_SPLIT_CHUNK");
         if (es && *es) {
             const int v = std::atoi(es);
@@ -628,32 +675,10 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
             plan->split_chunk = 0;
         }
     }
-    // split tail: the last partial wave of equal-length weight-gradient units
-    // (U mod P units for P = 152 CTAs / pair, a fixed wave so the plan never
-    // depends on max_sms) runs as S pieces each, filling about one more wave
-    // of 1/S length instead of a whole wave with few units
+    // split tail of an unsplit weight gradient (see choose_tail)
     if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->split_chunk == 0 && plan->cluster_splits == 0 &&
-        env_int("CAKE_GG_TAIL", 1) != 0) {
-        const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, 0, 0, plan->pair, bk);
-        const int64_t units = int64_t(E) * m_units_w(g) * g.n_tiles;
-        const int64_t P = kWaveCtas / plan->pair;
-        const int64_t T = units % P;
-        const int64_t kb_per_unit = (M_max / E) / bk;
-        // long units only: on short ones the pieces' partial-sum finish costs
-        // about what the shorter last wave saves
-        if (units > P && T > 0 && 2 * T <= P && kb_per_unit >= 64) {
-            int64_t S = P / T;
-            if (S > kMaxTailSplits) S = kMaxTailSplits;
-            while (S > 1 && kb_per_unit < 4 * S) --S;   // pieces of at least ~4 stages
-            // partial slots of at most 16 MiB (T units x pair x S pieces x one FP32 tile)
-            const int64_t tile_bytes = int64_t(kTileM) * bn * 4;
-            while (S > 1 && T * plan->pair * S * tile_bytes > (int64_t(16) << 20)) --S;
-            if (S >= 2) {
-                plan->tail_units = int32_t(T);
-                plan->tail_splits = int32_t(S);
-            }
-        }
-    }
+        env_int("CAKE_GG_TAIL", 1) != 0)
+        choose_tail(E, N, K, M_max, bn, bk, plan->pair, &plan->tail_units, &plan->tail_splits);
     const int csp = plan->cluster_splits;
     int stages = kMaxStages;
     const int pr = plan->pair;

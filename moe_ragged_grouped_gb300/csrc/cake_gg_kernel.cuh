@@ -314,6 +314,109 @@ __device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
     else static_cast<uint16_t *>(out)[idx] = f32_to_bf16_rn(v);
 }
 
+// Finish of one row of a split output tile by the tile's last arriving split:
+// the FP32 partials p_0 .. p_{nsum-1} (each laid out [col/4][row] float4,
+// slot_stride floats apart) are summed in split order (s = p_0; s += p_1; ...)
+// and row `lrow` of the tile is written (transposed for swapped operands).
+// Each batch loads CB float4 columns of SB slots: SB * CB = 16 independent
+// 16-byte loads in flight per thread, whatever nsum is.  A lone accumulator
+// (non-deterministic splits) is zeroed as it is read, ready for the next call.
+template <int CB, int SB, bool OUT_F32, bool TRANSPOSED>
+__device__ __forceinline__ void finish_split_row(float *base0, int nsum, int64_t slot_stride, bool zero_after,
+                                                 int bn, int lrow, bool row_ok, int32_t cols_valid, void *out,
+                                                 int64_t out_base, int64_t ld)
+{
+    for (int c4 = 0; c4 < bn / 4; c4 += CB) {
+        float4 acc[CB];
+        for (int s0 = 0; s0 < nsum; s0 += SB) {
+            float4 b[SB][CB];
+#pragma unroll
+            for (int u = 0; u < SB; ++u)
+#pragma unroll
+                for (int j = 0; j < CB; ++j)
+                    if (s0 + u < nsum)
+                        b[u][j] = __ldcg(reinterpret_cast<const float4 *>(
+                            base0 + (s0 + u) * slot_stride + (int64_t(c4 + j) * kTileM + lrow) * 4));
+            if (zero_after) {
+#pragma unroll
+                for (int j = 0; j < CB; ++j)
+                    *reinterpret_cast<float4 *>(base0 + (int64_t(c4 + j) * kTileM + lrow) * 4) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < SB; ++u) {
+                if (s0 + u < nsum) {
+#pragma unroll
+                    for (int j = 0; j < CB; ++j) {
+                        if (s0 + u == 0) {
+                            acc[j] = b[u][j];
+                        } else {
+                            acc[j].x += b[u][j].x;
+                            acc[j].y += b[u][j].y;
+                            acc[j].z += b[u][j].z;
+                            acc[j].w += b[u][j].w;
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < CB; ++j) {
+            const int col = (c4 + j) * 4;
+            if (row_ok && col < cols_valid) {
+                const float vv[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+                if (TRANSPOSED) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        store_scalar<OUT_F32>(out, out_base + int64_t(col + q4) * ld + lrow, vv[q4]);
+                } else if (OUT_F32) {
+                    *reinterpret_cast<float4 *>(static_cast<float *>(out) + out_base + int64_t(lrow) * ld + col) =
+                        acc[j];
+                } else {
+                    uint2 pk;
+                    pk.x = pack_bf16x2(vv[0], vv[1]);
+                    pk.y = pack_bf16x2(vv[2], vv[3]);
+                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + out_base + int64_t(lrow) * ld + col) =
+                        pk;
+                }
+            }
+        }
+    }
+}
+
+// One warp's 32-row x 128-byte slab of an output tile (this lane's row in w)
+// through the warp's staging buffer and a TMA tensor store at (x, y[, z]).
+// With two buffers per warp they alternate across every slab the warp ever
+// stores (buf persists across tiles), so "all store groups but the newest
+// have read their buffers" always covers the buffer written next.
+template <int MODE>
+__device__ __forceinline__ void stage_and_store(uint8_t *staging, int &buf, int staging_bufs, int q, int lane,
+                                                const uint32_t (&w)[32], const CUtensorMap *map, int32_t x,
+                                                int32_t y, int32_t z)
+{
+    uint8_t *stg = staging + (size_t(buf) * 4 + q) * 4096;
+    if (lane == 0) {
+        // the store that last used this buffer has read it
+        if (staging_bufs == 2) bulk_wait_read_but_one();
+        else bulk_wait_read_all();
+    }
+    __syncwarp();
+    uint8_t *rowp = stg + lane * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4 *>(rowp + ((ch ^ (lane & 7)) << 4)) =
+            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (MODE == kModeWgrad) tma_store_3d(map, smem_u32(stg), x, y, z);
+        else tma_store_2d(map, smem_u32(stg), x, y);
+        bulk_commit_group();
+    }
+    __syncwarp();
+    if (staging_bufs == 2) buf ^= 1;
+}
+
 // All MMAs of one stage: 4 * KPS k-steps of 16.  Descriptors are built once
 // per stage and advanced by adding (byte offset >> 4) to the 14-bit start
 // address field (shared-memory addresses stay below 2^18, so no carry).
@@ -615,7 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      map_to_cta(smem_u32(&c->uq_full[slot]), 1));
                     ++us.pos;
                     if (t < 0) break;
-                    nxt = atomicAdd(p.sched, 1);  // in flight while this unit's copies go out
                 } else {
                     // the odd CTA's producer reads the queue like every other role; it
                     // also arms each slot's barrier for the next 8-byte delivery (the
@@ -634,7 +736,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (t < 0) break;
                 }
                 const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
+                // the next unit is fetched while this one's last stages go out: early
+                // enough to hide the atomic, late enough that every CTA of the grid
+                // has taken its first unit (fetching at once would let the first
+                // pairs to start hold two units while late ones find none)
+                const int32_t fetch_kb = ti.kb1 - (p.stages + 1) > ti.kb0 ? ti.kb1 - (p.stages + 1) : ti.kb0;
+                bool fetched = !(p.dyn && leader);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                    if (!fetched && kb == fetch_kb) {
+                        nxt = atomicAdd(p.sched, 1);  // in flight while the copies go out
+                        fetched = true;
+                    }
                     if (!thread_wait(smem_u32(&c->empty[stage]), phase ^ 1u, c, p, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -718,6 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
+                // a unit without k-blocks (an empty expert's zero tile) fetches here
+                if (!fetched && ok) nxt = atomicAdd(p.sched, 1);
             }
             if (!ok) {
                 // drain: the most recent issue into each stage must land before exit
@@ -829,6 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int etid = tid - 64;         // 0..127
         int it = 0;
         int cs_it = 0;                     // cluster-split tiles reduced so far
+        int stg_buf = 0;                   // staging buffer this warp writes next
         bool qok = true;
         for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, qok); ++it) {
             const int64_t t = us.t;
@@ -983,14 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   (MODE == kModeWgrad ? q * 32 < rows_valid : q * 32 + 32 <= rows_valid);
             if (tma_path) {
                 constexpr int CW = OUT_F32 ? 32 : 64;  // columns per 128-byte row
-                int buf = 0;
                 // only chunks that exist: every staging write must be followed by its
                 // committed store, or the alternating-buffer wait (all groups but the
                 // newest have read their buffers) would let a write overtake a store
                 for (int c0 = 0; c0 < p.bn && c0 < cols_valid; c0 += CW) {
-                    // this warp's staging buffers alternate when there are two
-                    uint8_t *stg = staging + (size_t(buf) * 4 + q) * 4096;
-                    const uint32_t stg_u32 = smem_u32(stg);
                     uint32_t w[32];
                     if (empty_tile) {
 #pragma unroll
@@ -1009,29 +1120,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
                         }
                     }
-                    if (lane == 0) {
-                        // the store that last used this buffer has read it
-                        if (p.staging_bufs == 2) bulk_wait_read_but_one();
-                        else bulk_wait_read_all();
-                    }
-                    __syncwarp();
-                    uint8_t *rowp = stg + lane * 128;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        *reinterpret_cast<uint4 *>(rowp + ((ch ^ (lane & 7)) << 4)) =
-                            make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const int32_t x = ti.nt * p.bn + c0;
-                        if (MODE == kModeWgrad)
-                            tma_store_3d(&mapOut, stg_u32, x, ti.mt * kTileM + q * 32, ti.e);
-                        else
-                            tma_store_2d(&mapOut, stg_u32, x, ti.row0 + q * 32);
-                        bulk_commit_group();
-                    }
-                    __syncwarp();
-                    if (p.staging_bufs == 2) buf ^= 1;
+                    const int32_t x = ti.nt * p.bn + c0;
+                    if (MODE == kModeWgrad)
+                        stage_and_store<MODE>(staging, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
+                                              ti.mt * kTileM + q * 32, ti.e);
+                    else
+                        stage_and_store<MODE>(staging, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
+                                              ti.row0 + q * 32, 0);
                 }
             }
             for (int c0 = 0; c0 < p.bn && !tma_path; c0 += 32) {
@@ -1095,63 +1190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                : slot_ptr;
                     const int nsum = slots ? ti.S : 1;
                     const int64_t slot_stride = int64_t(kTileM) * p.bn;
-                    // 4 float4 columns x up to 4 slots per batch: 16 independent loads in flight
-                    for (int c4 = 0; c4 < p.bn / 4; c4 += 4) {
-                        float4 acc[4];
-                        for (int s0 = 0; s0 < nsum; s0 += 4) {
-                            float4 b[4][4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    if (s0 + u < nsum)
-                                        b[u][j] = __ldcg(reinterpret_cast<const float4 *>(
-                                            base0 + (s0 + u) * slot_stride + (int64_t(c4 + j) * kTileM + lrow) * 4));
-                            if (!slots) {
-                                // the atomic accumulator is read only here: leave it zeroed for the next call
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    *reinterpret_cast<float4 *>(base0 + (int64_t(c4 + j) * kTileM + lrow) * 4) =
-                                        make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                if (s0 + u < nsum) {
-#pragma unroll
-                                    for (int j = 0; j < 4; ++j) {
-                                        if (s0 + u == 0) acc[j] = b[u][j];
-                                        else {
-                                            acc[j].x += b[u][j].x;
-                                            acc[j].y += b[u][j].y;
-                                            acc[j].z += b[u][j].z;
-                                            acc[j].w += b[u][j].w;
-                                        }
-                                    }
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int col = (c4 + j) * 4;
-                            if (row_ok && col < cols_valid) {
-                                const float vv[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
-                                if (MODE == kModeWgrad && SWAP) {
-#pragma unroll
-                                    for (int q4 = 0; q4 < 4; ++q4)
-                                        store_scalar<OUT_F32>(p.out, out_base + int64_t(col + q4) * ld + lrow, vv[q4]);
-                                } else if (OUT_F32) {
-                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + out_base +
-                                                                int64_t(lrow) * ld + col) = acc[j];
-                                } else {
-                                    uint2 pk;
-                                    pk.x = pack_bf16x2(vv[0], vv[1]);
-                                    pk.y = pack_bf16x2(vv[2], vv[3]);
-                                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + out_base +
-                                                               int64_t(lrow) * ld + col) = pk;
-                                }
-                            }
-                        }
-                    }
+                    constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
+                    if (nsum == 1)
+                        finish_split_row<16, 1, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
+                                                              cols_valid, p.out, out_base, ld);
+                    else if (nsum == 2)
+                        finish_split_row<8, 2, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
+                                                             cols_valid, p.out, out_base, ld);
+                    else
+                        finish_split_row<4, 4, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
+                                                             cols_valid, p.out, out_base, ld);
                 }
             }
         }

@@ -300,12 +300,14 @@ def test_scheduler_words_return_to_zero():
 
 
 @pytest.mark.parametrize("det,out_dtype", [(1, "fp32"), (0, "bf16"), (1, "bf16")])
-def test_wide_weight_gradient_tiles(det, out_dtype):
+def test_wide_weight_gradient_tiles(det, out_dtype, monkeypatch):
     """256 x 512 pair tiles (two N = 256 MMAs per k-step into one 512-column accumulator):
     an empty expert, a last column tile of 64 (K = 1088), a last pair whose odd CTA lies past
-    N = 384, NaN rows past the last offset."""
+    N = 384, NaN rows past the last offset.  (The plan takes these tiles for shapes this small
+    only when forced: 18 units fill less than half a wave.)"""
     import torch
     from moe_ragged_grouped_gb300 import cake_gg as gg_
+    monkeypatch.setenv("CAKE_GG_WIDE", "2")
     plan = gg_.cake_gg_plan("wgrad", 3, 25004, 384, 1088, out_dtype, det)
     assert plan.tile_n == 512 and plan.pair == 2
     check_case("wgrad", [12000, 0, 13000], 384, 1088, out_dtype, det, seed=24, extra_rows=4)
@@ -316,8 +318,10 @@ def test_wide_tiles_bitwise_equal_to_256_wide(monkeypatch):
     the same sequence of K = 16 MMA steps in both tile widths."""
     import torch
     monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "0")
+    monkeypatch.setenv("CAKE_GG_WIDE", "2")
     Xb, Wb, Gb, off = make_inputs([12000, 0, 13000], 384, 1088, seed=25)
     X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    assert gg.cake_gg_plan("wgrad", 3, 25004, 384, 1088, "fp32", 1).tile_n == 512
     wide = run("wgrad", X, W, G, off, "fp32", 1)
     monkeypatch.setenv("CAKE_GG_WIDE", "0")
     narrow = run("wgrad", X, W, G, off, "fp32", 1)
