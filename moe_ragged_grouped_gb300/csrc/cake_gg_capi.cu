@@ -593,7 +593,12 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->tile_n = bn;
     // two CTAs compute a 256-row tile as one MMA (each holds half of the B
     // tile) when it is wide; swapped thin weight gradients stay single
-    plan->pair = (bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab)) ? 2 : 1;
+    // (a forward / data gradient whose whole reduction is one 64-deep k-block
+    // is bound by its epilogue's stores: single CTAs do as well and keep the
+    // ring shallow)
+    const int64_t red_fd = pass == CAKE_GG_FWD ? K : N;
+    plan->pair = (bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab) &&
+                  !(pass != CAKE_GG_WGRAD && red_fd <= 64)) ? 2 : 1;
     const int env_pair = env_int("CAKE_GG_PAIR", -1);
     if (env_pair == 0) plan->pair = 1;
     // long weight-gradient units: a pair takes a 256 x 512 tile (two N = 256

@@ -318,9 +318,9 @@ __device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
 // the FP32 partials p_0 .. p_{nsum-1} (each laid out [col/4][row] float4,
 // slot_stride floats apart) are summed in split order (s = p_0; s += p_1; ...)
 // and row `lrow` of the tile is written (transposed for swapped operands).
-// Each batch loads CB float4 columns of SB slots: SB * CB = 16 independent
-// 16-byte loads in flight per thread, whatever nsum is.  A lone accumulator
-// (non-deterministic splits) is zeroed as it is read, ready for the next call.
+// Each batch loads CB float4 columns of SB slots: SB * CB independent
+// 16-byte loads in flight per thread.  A lone accumulator (non-deterministic
+// splits) is zeroed as it is read, ready for the next call.
 template <int CB, int SB, bool OUT_F32, bool TRANSPOSED>
 __device__ __forceinline__ void finish_split_row(float *base0, int nsum, int64_t slot_stride, bool zero_after,
                                                  int bn, int lrow, bool row_ok, int32_t cols_valid, void *out,
@@ -378,6 +378,64 @@ __device__ __forceinline__ void finish_split_row(float *base0, int nsum, int64_t
                     pk.y = pack_bf16x2(vv[2], vv[3]);
                     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + out_base + int64_t(lrow) * ld + col) =
                         pk;
+                }
+            }
+        }
+    }
+}
+
+// Row `lrow` of this CTA's slice [q0, q1) of float4 columns of a
+// cluster-split tile: the csplit FP32 partials (one per CTA of the cluster,
+// each at red_buf in its own shared memory, laid out [col/4][row] float4) are
+// read through distributed shared memory, summed in split order (s = 0, 1,
+// ..., csplit - 1) and stored (transposed for swapped operands).  A batch
+// holds 4 float4 columns x 4 splits in registers (compile-time indices); more
+// splits are added group after group, still in split order.
+template <bool OUT_F32, bool TRANSPOSED>
+__device__ __forceinline__ void cluster_reduce_slice(uint32_t my_buf, int csplit, int q0, int q1, int lrow,
+                                                     bool store_ok, int32_t cols_valid, void *out,
+                                                     int64_t out_base, int64_t ld)
+{
+    constexpr int QB = 4;   // float4 columns per batch
+    constexpr int SG = 4;   // splits per group
+    for (int qc = q0; qc < q1; qc += QB) {
+        float4 acc[QB];
+        for (int s0 = 0; s0 < csplit; s0 += SG) {
+            float4 b4[QB][SG];
+#pragma unroll
+            for (int jj = 0; jj < QB; ++jj)
+#pragma unroll
+                for (int u = 0; u < SG; ++u)
+                    if (s0 + u < csplit && qc + jj < q1)
+                        b4[jj][u] = ld_shared_cluster_f4(map_to_cta(my_buf, uint32_t(s0 + u)) +
+                                                         uint32_t(((qc + jj) * kTileM + lrow) * 16));
+#pragma unroll
+            for (int jj = 0; jj < QB; ++jj) {
+#pragma unroll
+                for (int u = 0; u < SG; ++u) {
+                    if (s0 + u < csplit && qc + jj < q1) {
+                        if (s0 + u == 0) {
+                            acc[jj] = b4[jj][u];
+                        } else {
+                            acc[jj].x += b4[jj][u].x;
+                            acc[jj].y += b4[jj][u].y;
+                            acc[jj].z += b4[jj][u].z;
+                            acc[jj].w += b4[jj][u].w;
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < QB; ++jj) {
+            const int col = (qc + jj) * 4;
+            if (qc + jj < q1 && store_ok && col < cols_valid) {
+                const float vv[4] = {acc[jj].x, acc[jj].y, acc[jj].z, acc[jj].w};
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int64_t idx = TRANSPOSED ? out_base + int64_t(col + q4) * ld + lrow
+                                                   : out_base + int64_t(lrow) * ld + col + q4;
+                    store_scalar<OUT_F32>(out, idx, vv[q4]);
                 }
             }
         }
@@ -483,7 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int E = p.E;
-    const int csplit = MODE == kModeWgrad ? p.csplit : 0;
+    // (cluster splits exist only for swapped weight gradients: the other
+    // instantiations compile none of that path)
+    const int csplit = MODE == kModeWgrad && SWAP ? p.csplit : 0;
     Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit,
                        MODE == kModeWgrad ? p.tail : 0, MODE == kModeWgrad ? p.tail_s : 0);
     // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + r
@@ -1023,8 +1083,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // orders the other threads' stores before this thread's
                 // cluster-scope release arrivals)
                 named_bar_sync(1, 128);
-                if (etid == 0)
-                    for (int j = 0; j < csplit; ++j) mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), j));
+                if (etid == 0) {
+                    fence_acq_rel_cluster();
+                    for (int j = 0; j < csplit; ++j)
+                        mbar_arrive_cluster_relaxed(map_to_cta(smem_u32(&c->red_ready), j));
+                }
                 bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
                 if (!named_bar_and(1, 128, okr)) break;
                 // my slice of float4 columns, summed over the splits in split order
@@ -1033,43 +1096,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int q0 = rank * per;
                 const int q1 = q0 + per < nq ? q0 + per : nq;
                 const uint32_t my_buf = smem_u32(red_buf);
-                // two float4 columns x up to kMaxCsplit splits in flight per batch
-                // (compile-time indices keep them in registers); then the splits are
-                // summed in order s = 0, 1, ..., csplit - 1
-                for (int qc = q0; qc < q1; qc += 2) {
-                    float4 b4[2][kMaxCsplit];
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                        for (int s_ = 0; s_ < kMaxCsplit; ++s_)
-                            if (s_ < csplit && qc + jj < q1)
-                                b4[jj][s_] = ld_shared_cluster_f4(map_to_cta(my_buf, uint32_t(s_)) +
-                                                                  uint32_t(((qc + jj) * kTileM + lrow) * 16));
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        if (qc + jj >= q1) continue;
-                        float4 acc = b4[jj][0];
-#pragma unroll
-                        for (int s_ = 1; s_ < kMaxCsplit; ++s_) {
-                            if (s_ < csplit) {
-                                acc.x += b4[jj][s_].x;
-                                acc.y += b4[jj][s_].y;
-                                acc.z += b4[jj][s_].z;
-                                acc.w += b4[jj][s_].w;
-                            }
-                        }
-                        const int col = (qc + jj) * 4;
-                        if (row_ok && col < cols_valid && ti.valid) {
-                            const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                const int64_t idx = SWAP ? out_base + int64_t(col + q4) * ld + lrow
-                                                         : out_base + int64_t(lrow) * ld + col + q4;
-                                store_scalar<OUT_F32>(p.out, idx, vv[q4]);
-                            }
-                        }
-                    }
-                }
+                constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
+                cluster_reduce_slice<OUT_F32, kTr>(my_buf, csplit, q0, q1, lrow, row_ok && ti.valid, cols_valid,
+                                                   p.out, out_base, ld);
                 // done reading the peers' partials (a cluster's last unit needs no
                 // signal: the teardown cluster barrier keeps every peer alive)
                 if (t + unit_step < total) {
@@ -1191,15 +1220,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int nsum = slots ? ti.S : 1;
                     const int64_t slot_stride = int64_t(kTileM) * p.bn;
                     constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
+                    // (16 loads in flight; 8 in swapped kernels, which also hold
+                    // the cluster reduction and otherwise pass the register limit)
+                    constexpr int kCB = kTr ? 8 : 16;
                     if (nsum == 1)
-                        finish_split_row<16, 1, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
-                                                              cols_valid, p.out, out_base, ld);
+                        finish_split_row<kCB, 1, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
+                                                               cols_valid, p.out, out_base, ld);
                     else if (nsum == 2)
-                        finish_split_row<8, 2, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
-                                                             cols_valid, p.out, out_base, ld);
+                        finish_split_row<kCB / 2, 2, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow,
+                                                                   row_ok, cols_valid, p.out, out_base, ld);
                     else
-                        finish_split_row<4, 4, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
-                                                             cols_valid, p.out, out_base, ld);
+                        finish_split_row<kCB / 4, 4, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow,
+                                                                   row_ok, cols_valid, p.out, out_base, ld);
                 }
             }
         }

@@ -171,6 +171,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Relaxed arrive on an mbarrier given by its cluster address.  After one
+// fence_acq_rel_cluster, a run of these publishes the thread's (and, through
+// a preceding CTA barrier, its CTA's) prior writes to every peer that later
+// acquires the arrivals, with one fence instead of one release per arrive.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // Asynchronous 8-byte store into a peer CTA's shared memory whose arrival
 // counts 8 bytes down on the peer's mbarrier (both addresses from mapa).
 __device__ __forceinline__ void st_async_b64(uint32_t remote_addr, int64_t v, uint32_t remote_bar)

@@ -253,6 +253,18 @@ def test_double_staging_partial_last_tile(pass_, out_dtype, max_sms, monkeypatch
     check_case(pass_, [0, 777, 2048, 301], N, K, out_dtype, 1, seed=19, extra_rows=4, max_sms=max_sms)
 
 
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+@pytest.mark.parametrize("width", [320, 448])
+@pytest.mark.parametrize("max_sms", [2, 0])
+def test_double_staging_odd_slab_count(pass_, width, max_sms, monkeypatch):
+    """BF16 output 320 = 256 + 64 or 448 = 256 + 192 wide: the last column tile stores an odd
+    number of 64-column slabs (1 or 3), so a warp's next tile starts on the buffer its previous
+    tile's last store may still be reading unless the buffers alternate across tiles."""
+    monkeypatch.setenv("CAKE_GG_STAGING_BUFS", "2")
+    N, K = (width, 256) if pass_ == "fwd" else (256, width)
+    check_case(pass_, [0, 777, 2048, 301, 1500], N, K, "bf16", 1, seed=28, extra_rows=4, max_sms=max_sms)
+
+
 @pytest.mark.parametrize("pass_", PASSES)
 @pytest.mark.parametrize("tile_k", ["64", "128"])
 def test_pairs_at_both_stage_depths_and_few_ctas(pass_, tile_k, monkeypatch):
