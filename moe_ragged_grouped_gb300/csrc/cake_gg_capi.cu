@@ -324,7 +324,7 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         (plan->tail_splits > 1 && (pass != CAKE_GG_WGRAD || plan->swap_ab || plan->split_chunk > 0 ||
                                    plan->cluster_splits > 0)) ||
         smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits,
-                       plan->pair) > kSmemLimit)
+                       plan->pair, plan->E) > kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->N % 8 != 0 || plan->K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
     // operands with M_max rows may be null when there are no rows at all
@@ -506,7 +506,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     grid -= grid % CL;
     if (grid < CL) grid = CL;
 
-    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs, p.csplit, P);
+    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs, p.csplit, P, E);
     cudaError_t err;
     if (mode == kModeFwd) err = launch_fwd(out_f32, P, ma, mb, mo, p, grid, smem, stream);
     else if (mode == kModeDgrad) err = launch_dgrad(out_f32, P, ma, mb, mo, p, grid, smem, stream);
@@ -644,7 +644,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     plan->tile_k = bk;
 
     // deeper stages only while at least two of them fit
-    while (bk > 64 && smem_bytes_for(bn, 2, bk / 64, 1, 0, plan->pair) > kSmemLimit) bk /= 2;
+    while (bk > 64 && smem_bytes_for(bn, 2, bk / 64, 1, 0, plan->pair, E) > kSmemLimit) bk /= 2;
     plan->tile_k = bk;
     if (pass == CAKE_GG_WGRAD) {
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
@@ -687,25 +687,29 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     const int csp = plan->cluster_splits;
     int stages = kMaxStages;
     const int pr = plan->pair;
-    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64, 1, csp, pr) > kSmemLimit) --stages;
+    while (stages > 2 && smem_bytes_for(bn, stages, bk / 64, 1, csp, pr, E) > kSmemLimit) --stages;
     // a short reduction per tile (thin data gradient / forward) makes the
     // epilogue the critical path: trade ring depth for double-buffered staging
     const int32_t red_len = pass == CAKE_GG_FWD ? K : pass == CAKE_GG_DGRAD ? N : 1 << 30;
     int staging_bufs = 1;
     if ((red_len + bk - 1) / bk <= 4) {
         int st2 = stages;
-        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) > kSmemLimit) --st2;
-        if (smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) <= kSmemLimit) {
+        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp, pr, E) > kSmemLimit) --st2;
+        if (smem_bytes_for(bn, st2, bk / 64, 2, csp, pr, E) <= kSmemLimit) {
             staging_bufs = 2;
             stages = st2;
         }
     }
+    // a 512-wide tile has one accumulator: the MMA waits for its epilogue, so
+    // let the epilogue's slab writes overlap its stores when room allows
+    if (wide && plan->pass == CAKE_GG_WGRAD && smem_bytes_for(bn, stages, bk / 64, 2, csp, pr, E) <= kSmemLimit)
+        staging_bufs = 2;
     const int env_sb = env_int("CAKE_GG_STAGING_BUFS", 0);
     if (env_sb == 1) staging_bufs = 1;
     if (env_sb == 2 && staging_bufs == 1) {
         int st2 = stages;
-        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) > kSmemLimit) --st2;
-        if (smem_bytes_for(bn, st2, bk / 64, 2, csp, pr) <= kSmemLimit) {
+        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2, csp, pr, E) > kSmemLimit) --st2;
+        if (smem_bytes_for(bn, st2, bk / 64, 2, csp, pr, E) <= kSmemLimit) {
             staging_bufs = 2;
             stages = st2;
         }

@@ -95,11 +95,15 @@ struct __align__(16) Ctrl {
     int32_t abort_flag;
     int32_t bad;
     int32_t last_flag;
-    int32_t off[kMaxE + 1];
-    int32_t order[kMaxE];
-    int32_t pref[kMaxE + 1];
-    int32_t spref[kMaxE + 1];
 };
+
+// Walk tables after the control block, sized by the launch's E: off[E+1]
+// offsets, order[E] processing position -> expert, pref[E+1] unit prefix in
+// processing order, spref[E+1] split prefix by expert id (16-byte aligned).
+__host__ __device__ constexpr size_t tables_bytes_for(int E)
+{
+    return (size_t(4 * E + 3) * 4u + 15u) / 16u * 16u;
+}
 
 // A stage holds kps = bk / 64 k-chunks of A (128 rows) and B (bn rows).
 // One ring stage: A (128 rows) and this CTA's rows of B (all bn of them, or
@@ -115,11 +119,11 @@ __host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit)
     return csplit > 0 ? size_t(kTileM) * size_t(bn) * 4u : 0u;
 }
 
-__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps = 1, int staging_bufs = 1,
-                                                    int csplit = 0, int pair = 1)
+__host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps, int staging_bufs, int csplit,
+                                                    int pair, int E)
 {
     return 1024 + size_t(stages) * stage_bytes_for(bn, kps, pair) + size_t(staging_bufs) * kStagingBytes +
-           csplit_bytes_for(bn, csplit) + sizeof(Ctrl);
+           csplit_bytes_for(bn, csplit) + sizeof(Ctrl) + tables_bytes_for(E);
 }
 
 // Bounded wait on one mbarrier phase, by every lane of the calling warp;
@@ -536,6 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
     float *red_buf = reinterpret_cast<float *>(staging + size_t(p.staging_bufs) * kStagingBytes);
     Ctrl *c = reinterpret_cast<Ctrl *>(reinterpret_cast<uint8_t *>(red_buf) + csplit_bytes_for(p.bn, p.csplit));
+    int32_t *const t_off = reinterpret_cast<int32_t *>(c + 1);
+    int32_t *const t_order = t_off + (p.E + 1);
+    int32_t *const t_pref = t_order + p.E;
+    int32_t *const t_spref = t_pref + (p.E + 1);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -618,8 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t cnt = e < E ? expert_tiles(g, rows) : 0;
             const int32_t cost = e < E ? expert_cost(g, rows) : 0;
             const int32_t spl = e < E ? expert_splits(g, rows) : 0;
-            if (e < E) c->off[e] = a;
-            if (e == E - 1) c->off[E] = b;
+            if (e < E) t_off[e] = a;
+            if (e == E - 1) t_off[E] = b;
             int32_t rank = e;
             if (walk_is_sorted(g)) {
                 rank = 0;
@@ -628,9 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rank += (cj > cost) || (cj == cost && j < e);
                 }
             }
-            if (e < E) c->order[rank] = e;
+            if (e < E) t_order[rank] = e;
             __syncwarp();
-            const int32_t op = lane < E ? c->order[lane] : 0;
+            const int32_t op = lane < E ? t_order[lane] : 0;
             int32_t cnt_p = __shfl_sync(full_mask, cnt, op);
             if (lane >= E) cnt_p = 0;
             int32_t inc_t = cnt_p, inc_s = spl;
@@ -644,22 +652,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (lane < E) {
-                c->pref[lane] = inc_t - cnt_p;
-                c->spref[lane] = inc_s - spl;
+                t_pref[lane] = inc_t - cnt_p;
+                t_spref[lane] = inc_s - spl;
             }
             if (lane == 31) {
-                c->pref[E] = inc_t;
-                c->spref[E] = inc_s;
+                t_pref[E] = inc_t;
+                t_spref[E] = inc_s;
             }
         }
     } else {
         // block-wide build for many experts (temporaries in the ring)
         int32_t *t_cnt = reinterpret_cast<int32_t *>(ring);
         int32_t *t_cost = t_cnt + kMaxE;
-        for (int i = tid; i <= E; i += kThreads) c->off[i] = p.offsets[i];
+        for (int i = tid; i <= E; i += kThreads) t_off[i] = p.offsets[i];
         __syncthreads();
         for (int e = tid; e < E; e += kThreads) {
-            const int32_t a = c->off[e], b = c->off[e + 1];
+            const int32_t a = t_off[e], b = t_off[e + 1];
             if ((e == 0 && a != 0) || b < a || (e == E - 1 && int64_t(b) > p.M_max)) c->bad = 1;
             const int32_t rows = b - a;
             t_cnt[e] = expert_tiles(g, rows < 0 ? 0 : rows);
@@ -674,10 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t cj = t_cost[j];
                     rank += (cj > ce) || (cj == ce && j < e);
                 }
-                c->order[rank] = e;
+                t_order[rank] = e;
             }
         } else {
-            for (int e = tid; e < E; e += kThreads) c->order[e] = e;
+            for (int e = tid; e < E; e += kThreads) t_order[e] = e;
         }
         __syncthreads();
         if (warp == 0) {
@@ -686,8 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b0 = lane * per;
             int32_t sum_t = 0, sum_s = 0;
             for (int i = b0; i < b0 + per && i < E; ++i) {
-                sum_t += t_cnt[c->order[i]];
-                sum_s += expert_splits(g, c->off[i + 1] - c->off[i]);
+                sum_t += t_cnt[t_order[i]];
+                sum_s += expert_splits(g, t_off[i + 1] - t_off[i]);
             }
             int32_t inc_t = sum_t, inc_s = sum_s;
 #pragma unroll
@@ -701,14 +709,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int32_t run_t = inc_t - sum_t, run_s = inc_s - sum_s;
             for (int i = b0; i < b0 + per && i < E; ++i) {
-                c->pref[i] = run_t;
-                c->spref[i] = run_s;
-                run_t += t_cnt[c->order[i]];
-                run_s += expert_splits(g, c->off[i + 1] - c->off[i]);
+                t_pref[i] = run_t;
+                t_spref[i] = run_s;
+                run_t += t_cnt[t_order[i]];
+                run_s += expert_splits(g, t_off[i + 1] - t_off[i]);
             }
             if (lane == 31) {
-                c->pref[E] = inc_t;
-                c->spref[E] = inc_s;
+                t_pref[E] = inc_t;
+                t_spref[E] = inc_s;
             }
         }
     }
@@ -735,8 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after_sync();
 
-    if (MODE == kModeWgrad && g.tail > 0 && !tail_active(g, c->off, c->order)) g.tail = g.tail_s = 0;
-    const int64_t total = walk_length(g, c->pref[E]);
+    if (MODE == kModeWgrad && g.tail > 0 && !tail_active(g, t_off, t_order)) g.tail = g.tail_s = 0;
+    const int64_t total = walk_length(g, t_pref[E]);
     const uint32_t tmem_base = c->tmem_base;
     const uint32_t acc_stride = uint32_t(p.tmem_cols) / 2;
     // a 512-wide tile fills TMEM: one accumulator, released before the next unit
@@ -795,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++us.pos;
                     if (t < 0) break;
                 }
-                const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
+                const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
                 // the next unit is fetched while this one's last stages go out: early
                 // enough to hide the atomic, late enough that every CTA of the grid
                 // has taken its first unit (fetching at once would let the first
@@ -917,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool any_mma = false;
         for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, ok); ++it) {
             const int64_t t = us.t;
-            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
+            const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
             const int acc = nacc == 2 ? (it & 1) : 0;
             const uint32_t acc_phase = nacc == 2 ? (uint32_t(it >> 1) & 1u) : (uint32_t(it) & 1u);
             if (leader) {
@@ -1007,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool qok = true;
         for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, qok); ++it) {
             const int64_t t = us.t;
-            const Tile ti = decode_tile(g, t, c->off, c->order, c->pref, c->spref, rank);
+            const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
             const int acc = nacc == 2 ? (it & 1) : 0;
             const uint32_t acc_phase = nacc == 2 ? (uint32_t(it >> 1) & 1u) : (uint32_t(it) & 1u);
             // (in a pair the even CTA's MMA commit arrives on both CTAs' tfull)
