@@ -32,6 +32,7 @@ _U16P = ctypes.POINTER(ctypes.c_uint16)
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _I64P = ctypes.POINTER(ctypes.c_int64)
 _F64P = ctypes.POINTER(ctypes.c_double)
+_F32P = ctypes.POINTER(ctypes.c_float)
 
 
 def compile_oracle(out_path: str = _LIB_PATH, mutant: int = 0) -> str:
@@ -61,6 +62,15 @@ def _bind(lib):
     lib.oracle_wgrad_at.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
+    rt = [_F32P, _F32P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+    for name in ("oracle_router_bf16x3", "oracle_router_exact"):
+        f = getattr(lib, name)
+        f.argtypes = rt + [_F64P]
+        f.restype = ctypes.c_int
+    lib.oracle_router_bf16x3_at.argtypes = rt + [_I64P, _I64P, ctypes.c_int64, _F64P]
+    lib.oracle_router_bf16x3_at.restype = ctypes.c_int
+    lib.oracle_round_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_round_bf16.restype = ctypes.c_float
     return lib
 
 
@@ -164,6 +174,68 @@ def wgrad_at(G, X, off, E, es, ns, ks, lib=None):
     _check(lib.oracle_wgrad_at(pg, px, po, E, G.shape[0], N, K, pe, pn, pk, es.shape[0],
                                out.ctypes.data_as(_F64P)), "wgrad_at")
     return out
+
+
+# ---- FP32 router GEMM (BF16x3 emulation; flashinfer PR #8438, "Summary") ----
+
+def _f32(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.float32:
+        raise TypeError("router operands are float32")
+    return a, a.ctypes.data_as(_F32P)
+
+
+def router_bf16x3(X, W, lib=None):
+    """Y [T, R] in FP64: sum over k of x_hi w_hi + x_hi w_lo + x_lo w_hi (X [T, K], W [R, K] float32)."""
+    lib = lib or load()
+    X, px = _f32(X); W, pw = _f32(W)
+    (T, K), R = X.shape, W.shape[0]
+    Y = np.zeros((T, R), dtype=np.float64)
+    _check(lib.oracle_router_bf16x3(px, pw, T, R, K, Y.ctypes.data_as(_F64P)), "router_bf16x3")
+    return Y
+
+
+def router_exact(X, W, lib=None):
+    """Y [T, R] in FP64 by the definition sum over k of x w."""
+    lib = lib or load()
+    X, px = _f32(X); W, pw = _f32(W)
+    (T, K), R = X.shape, W.shape[0]
+    Y = np.zeros((T, R), dtype=np.float64)
+    _check(lib.oracle_router_exact(px, pw, T, R, K, Y.ctypes.data_as(_F64P)), "router_exact")
+    return Y
+
+
+def router_bf16x3_at(X, W, ts, rs, lib=None):
+    """Y[ts[i], rs[i]] by the BF16x3 emulation, in FP64."""
+    lib = lib or load()
+    X, px = _f32(X); W, pw = _f32(W)
+    (T, K), R = X.shape, W.shape[0]
+    ts, pt = _idx(ts); rs, pr = _idx(rs)
+    out = np.zeros(ts.shape[0], dtype=np.float64)
+    _check(lib.oracle_router_bf16x3_at(px, pw, T, R, K, pt, pr, ts.shape[0], out.ctypes.data_as(_F64P)),
+           "router_bf16x3_at")
+    return out
+
+
+def round_bf16(v, lib=None) -> float:
+    """The oracle's round-to-nearest-even BF16 of one float32 value (widened back to float)."""
+    return float((lib or load()).oracle_round_bf16(float(v)))
+
+
+def router_tolerance(abs_dot, L):
+    """Per-element bound for a GPU BF16x3 router logit against the emulation (router_bf16x3).
+
+    The GPU sums the same L = 3K exact BF16 products in FP32 (MMA accumulation,
+    order hardware-defined): |gpu - emu| <= 2^-22 * L * sum_k |x_k w_k| (about
+    L * u32 with u32 = 2^-24, times a factor 4 of margin for the split terms and
+    the accumulator's alignment).  ``abs_dot`` is sum_k |x_k| |w_k|.
+    """
+    return 2.0 ** -22 * float(L) * np.asarray(abs_dot, dtype=np.float64)
+
+
+def router_emulation_bound(abs_dot):
+    """|emulation - definition| <= 3 * 2^-16 * sum_k |x_k| |w_k| (the dropped x_lo w_lo and split residues)."""
+    return 3.0 * 2.0 ** -16 * np.asarray(abs_dot, dtype=np.float64)
 
 
 def num_threads(lib=None) -> int:

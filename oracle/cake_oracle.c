@@ -32,6 +32,9 @@
  * Every entry point validates the offsets (off[0] == 0, non-decreasing,
  * off[E] <= M) and returns 0 on success, -1 on invalid arguments.
  *
+ * The FP32 router GEMM of the same family (BF16x3 emulation) is at the end of
+ * this file.
+ *
  * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake; it is
  * used only by the test that shows the oracle's pins catch such mistakes.
  */
@@ -214,6 +217,112 @@ int oracle_wgrad_at(const uint16_t *G, const uint16_t *X, const int32_t *off, in
         out[i] = wgrad_elem(G, X, off, (int32_t)es[i], (int32_t)ns[i], (int32_t)ks[i], N, K);
     return 0;
 }
+
+/* ---- FP32 router GEMM (BF16x3 emulation) -------------------------------
+ *
+ * The dense projection family's FP32 router GEMM (flashinfer PR #8438,
+ * "Summary": "an FP32 router GEMM (256 experts, BF16x3 emulation)"):
+ * logits Y [T, R] = X [T, K] W^T with FP32 X and router weights W [R, K].
+ * The pages name the emulation and nothing more; the reading taken here is
+ * the usual one: every FP32 value v is split as hi = bf16(v) (round to
+ * nearest, ties to even) and lo = bf16(v - hi), and the product keeps the
+ * three leading terms of (x_hi + x_lo)(w_hi + w_lo):
+ *
+ *   Y[t, r] ~= sum_k  x_hi w_hi + x_hi w_lo + x_lo w_hi          (x = X[t,k], w = W[r,k])
+ *
+ * oracle_router_bf16x3 computes exactly that sum in FP64 (each term exact,
+ * summed in k order, the three terms of one k in the order written);
+ * oracle_router_exact computes the definition sum_k x w in FP64. */
+
+/* Round an FP32 value to the nearest BF16 (ties to even), returned widened
+ * to FP32; NaN stays NaN.  Written from the definition: keep the top 16 bits
+ * of the binary32 pattern after adding half a BF16 unit in the last place,
+ * minus one when the kept part is even (so exact halves go to even). */
+static float round_bf16(float v)
+{
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u) return v;  /* NaN */
+    const uint32_t keep_lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + keep_lsb;
+    u &= 0xFFFF0000u;
+    float r;
+    memcpy(&r, &u, sizeof r);
+    return r;
+}
+
+static void split_bf16x2(float v, double *hi, double *lo)
+{
+    const float h = round_bf16(v);
+#if ORACLE_MUTANT == 6 /* planted mistake: the low part is never formed */
+    *hi = (double)h;
+    *lo = 0.0;
+    return;
+#endif
+    const float l = round_bf16(v - h);   /* v - h is exact in FP32 */
+    *hi = (double)h;
+    *lo = (double)l;
+}
+
+static double router_bf16x3_elem(const float *X, const float *W, int64_t t, int32_t r, int32_t K)
+{
+    const float *x = X + t * (int64_t)K;
+    const float *w = W + (int64_t)r * K;
+    double s = 0.0;
+    for (int32_t k = 0; k < K; ++k) {
+        double xh, xl, wh, wl;
+        split_bf16x2(x[k], &xh, &xl);
+        split_bf16x2(w[k], &wh, &wl);
+        s += xh * wh;
+        s += xh * wl;
+        s += xl * wh;
+    }
+    return s;
+}
+
+static double router_exact_elem(const float *X, const float *W, int64_t t, int32_t r, int32_t K)
+{
+    const float *x = X + t * (int64_t)K;
+    const float *w = W + (int64_t)r * K;
+    double s = 0.0;
+    for (int32_t k = 0; k < K; ++k) s += (double)x[k] * (double)w[k];
+    return s;
+}
+
+/* Y [T, R] (FP64) by the BF16x3 emulation; 0 on success, -1 on bad sizes. */
+int oracle_router_bf16x3(const float *X, const float *W, int64_t T, int32_t R, int32_t K, double *Y)
+{
+    if (T < 0 || R < 1 || K < 1) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t r = 0; r < R; ++r) Y[t * R + r] = router_bf16x3_elem(X, W, t, r, K);
+    return 0;
+}
+
+/* Y [T, R] (FP64) by the definition sum_k x w. */
+int oracle_router_exact(const float *X, const float *W, int64_t T, int32_t R, int32_t K, double *Y)
+{
+    if (T < 0 || R < 1 || K < 1) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t r = 0; r < R; ++r) Y[t * R + r] = router_exact_elem(X, W, t, r, K);
+    return 0;
+}
+
+/* out[i] = Y[ts[i], rs[i]] by the BF16x3 emulation (any size). */
+int oracle_router_bf16x3_at(const float *X, const float *W, int64_t T, int32_t R, int32_t K,
+                            const int64_t *ts, const int64_t *rs, int64_t count, double *out)
+{
+    if (T < 0 || R < 1 || K < 1) return -1;
+    for (int64_t i = 0; i < count; ++i)
+        if (ts[i] < 0 || ts[i] >= T || rs[i] < 0 || rs[i] >= R) return -1;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < count; ++i) out[i] = router_bf16x3_elem(X, W, ts[i], (int32_t)rs[i], K);
+    return 0;
+}
+
+/* BF16 rounding of one FP32 value, exposed for the pins. */
+float oracle_round_bf16(float v) { return round_bf16(v); }
 
 /* Number of OpenMP threads the entry points above use. */
 int oracle_num_threads(void)
