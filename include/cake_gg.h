@@ -177,6 +177,50 @@ int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void
 int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
                           const int32_t *offsets, int out_dtype, int deterministic, void *stream);
 
+/* ---- FP32 router GEMM (BF16x3 emulation) ---------------------------------
+ *
+ * The dense projection family's FP32 router GEMM (flashinfer PR #8438,
+ * "Summary": "an FP32 router GEMM (256 experts, BF16x3 emulation)"): logits
+ * Y [T, R] = X [T, K] W^T, with X [T, K], router weights W [R, K] and Y all
+ * FP32, row-major.  The emulation (the pages name it and nothing more; the
+ * usual reading is taken): every value v is split as hi = bf16(v) and
+ * lo = bf16(v - hi), round to nearest even, and
+ *   Y[t, r] ~= sum_k x_hi w_hi + x_hi w_lo + x_lo w_hi
+ * with every product exact and the sum accumulated in FP32 by the tensor
+ * cores.  It drops x_lo w_lo and the split residues:
+ * |Y - X W^T| <= 3 * 2^-16 * sum_k |x_k w_k| plus FP32 accumulation error.
+ *
+ * The plan is a caller-owned POD; `gemm` is the forward plan of the one-expert
+ * BF16 GEMM with reduction length 3K that the call runs. */
+typedef struct cake_gg_router_plan {
+    int32_t abi_version;     /* CAKE_GG_ABI_VERSION                          */
+    int32_t R;               /* router outputs (experts), a multiple of 8    */
+    int64_t T;               /* tokens, 0 .. 2^31 - 1                        */
+    int32_t K;               /* model width, a multiple of 8                 */
+    int32_t reserved;
+    uint64_t workspace_bytes;/* the call's whole workspace (see below)       */
+    cake_gg_plan_t gemm;     /* the forward plan it runs                     */
+} cake_gg_router_plan_t;
+
+/* Fill *rp.  Pure host arithmetic.  CAKE_GG_ERR_ALIGNMENT unless R and K are
+ * multiples of 8; CAKE_GG_ERR_INVALID_ARG for T < 0, R or K < 1, max_sms < 0;
+ * CAKE_GG_ERR_OVERFLOW when a size does not fit.  rp->workspace_bytes is the
+ * workspace the call needs: the forward plan's workspace, the offsets of the
+ * one-expert problem and BF16 copies X' [T, 3K], W' [R, 3K] (about 6 (T + R) K
+ * bytes). */
+int cake_gg_router_plan(cake_gg_router_plan_t *rp, int64_t T, int32_t R, int32_t K, int32_t max_sms);
+
+/* Y = X W^T by BF16x3 emulation.  X, W, Y, workspace: device pointers,
+ * 16-byte aligned; the workspace is rp->workspace_bytes, caller-owned, filled
+ * with zeros once after allocation (as for cake_gg_fwd), unused by anyone else
+ * until the stream has run the call.  Enqueues two kernels on `stream` (the
+ * split into X' and W', then the forward GEMM); allocates nothing, never
+ * synchronises.  Host-detected errors return non-zero and enqueue nothing;
+ * the forward pass's device-detected errors land in the workspace's status
+ * word (cake_gg_check_status). */
+int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const float *W, float *Y,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, return the status word of `workspace` (CAKE_GG_OK,
  * or the first _BAD_OFFSETS / _TIMEOUT recorded by a call since the last
  * check) and reset it to CAKE_GG_OK; CAKE_GG_ERR_CUDA if a CUDA call failed. */

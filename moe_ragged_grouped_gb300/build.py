@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(HERE, "libcake_gg.so")
 
-SOURCES = ["cake_gg_capi.cu", "cake_gg_fwd.cu", "cake_gg_dgrad.cu", "cake_gg_wgrad.cu"]
+SOURCES = ["cake_gg_capi.cu", "cake_gg_fwd.cu", "cake_gg_dgrad.cu", "cake_gg_wgrad.cu", "cake_gg_router.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -37,7 +37,8 @@ PASSES = {"fwd": CAKE_GG_FWD, "dgrad": CAKE_GG_DGRAD, "wgrad": CAKE_GG_WGRAD}
 DTYPES = {"bf16": CAKE_GG_BF16, "fp32": CAKE_GG_FP32}
 
 EXPORTED = ["cake_gg_plan", "cake_gg_fwd", "cake_gg_dgrad", "cake_gg_wgrad",
-            "cake_gg_check_status", "cake_gg_strerror", "cake_gg_tile_walk", "cake_gg_corun_spinner"]
+            "cake_gg_check_status", "cake_gg_strerror", "cake_gg_tile_walk", "cake_gg_corun_spinner",
+            "cake_gg_router_plan", "cake_gg_router_fp32"]
 
 
 class CakeGGPlan(ctypes.Structure):
@@ -71,6 +72,19 @@ class CakeGGPlan(ctypes.Structure):
 
     def as_dict(self):
         return {f[0]: getattr(self, f[0]) for f in self._fields_ if f[0] != "reserved"}
+
+
+class CakeGGRouterPlan(ctypes.Structure):
+    """Mirror of cake_gg_router_plan_t (same field order, same C layout)."""
+    _fields_ = [
+        ("abi_version", ctypes.c_int32),
+        ("R", ctypes.c_int32),
+        ("T", ctypes.c_int64),
+        ("K", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_uint64),
+        ("gemm", CakeGGPlan),
+    ]
 
 
 class CakeGGError(RuntimeError):
@@ -111,6 +125,11 @@ def load_library(path: str = LIB_PATH):
     lib.cake_gg_tile_walk.restype = ctypes.c_int
     lib.cake_gg_wgrad_noalloc.argtypes = [plan_p, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp]
     lib.cake_gg_wgrad_noalloc.restype = ctypes.c_int
+    rplan_p = ctypes.POINTER(CakeGGRouterPlan)
+    lib.cake_gg_router_plan.argtypes = [rplan_p, i64, i32, i32, i32]
+    lib.cake_gg_router_plan.restype = ctypes.c_int
+    lib.cake_gg_router_fp32.argtypes = [rplan_p, vp, vp, vp, vp, sz, vp]
+    lib.cake_gg_router_fp32.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -231,6 +250,22 @@ def cake_gg_tile_walk(plan, offsets) -> np.ndarray:
     return out
 
 
+def cake_gg_router_plan(T, R, K, max_sms=0) -> CakeGGRouterPlan:
+    """cake_gg_router_plan(): plan of the FP32 router GEMM (BF16x3 emulation); raises on error."""
+    rp = CakeGGRouterPlan()
+    rc = load_library().cake_gg_router_plan(ctypes.byref(rp), int(T), int(R), int(K), int(max_sms))
+    if rc != CAKE_GG_OK:
+        raise CakeGGError(rc, "cake_gg_router_plan")
+    return rp
+
+
+def cake_gg_router_fp32(rp, X, W, Y, workspace, workspace_bytes=None, stream=None) -> int:
+    """cake_gg_router_fp32(): Y = X W^T by BF16x3 emulation on float32 torch tensors; returns the status."""
+    s = _stream(stream, X, W, Y)
+    nb = int(workspace.numel() * workspace.element_size()) if workspace_bytes is None else int(workspace_bytes)
+    return load_library().cake_gg_router_fp32(ctypes.byref(rp), _ptr(X), _ptr(W), _ptr(Y), _ptr(workspace), nb, s)
+
+
 # ---------------------------------------------------------------- tensor-level helpers
 
 
@@ -282,4 +317,28 @@ def grouped_gemm(pass_, a, b, offsets, out_dtype="bf16", deterministic=True, max
         st = cake_gg_check_status(workspace, stream)
         if st != CAKE_GG_OK:
             raise CakeGGError(st, f"cake_gg pass {pass_} (device status)")
+    return out
+
+
+def router_gemm(X, W, max_sms=0, out=None, plan=None, workspace=None, stream=None, check=True):
+    """FP32 router logits Y [T, R] = X [T, K] W [R, K]^T by BF16x3 emulation (float32 torch tensors).
+
+    Allocates the output and the workspace through torch when not given.
+    """
+    import torch
+    T, K = int(X.shape[0]), int(X.shape[1])
+    R = int(W.shape[0])
+    if plan is None:
+        plan = cake_gg_router_plan(T, R, K, max_sms)
+    if out is None:
+        out = torch.empty((T, R), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = torch.zeros(max(int(plan.workspace_bytes), 256), dtype=torch.uint8, device=X.device)
+    rc = cake_gg_router_fp32(plan, X, W, out, workspace, stream=stream)
+    if rc != CAKE_GG_OK:
+        raise CakeGGError(rc, "cake_gg_router_fp32")
+    if check:
+        st = cake_gg_check_status(workspace, stream)
+        if st != CAKE_GG_OK:
+            raise CakeGGError(st, "cake_gg_router_fp32 (device status)")
     return out

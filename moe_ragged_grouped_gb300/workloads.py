@@ -386,3 +386,29 @@ def pages_workload(shape: str) -> tuple:
         raise ValueError(shape)
     od = "fp32" if "fp32" in parts[4:] else "bf16"
     return Workload(shape.replace(" ", "_"), E, N, K, sizes), od
+
+
+# ---------------------------------------------------------------------------
+# FP32 router GEMM inputs (dense projection family, flashinfer PR #8438,
+# "Summary": an FP32 router GEMM over 256 experts)
+# ---------------------------------------------------------------------------
+
+ROUTER_T, ROUTER_K, ROUTER_R = 16384, 4096, 256
+
+
+def router_inputs(T: int, K: int, R: int, seed: int = 0):
+    """(X [T, K], W [R, K]) float32 numpy arrays: X ~ N(0, 1), W ~ N(0, 1/K), generation order X, W."""
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((T, K), dtype=np.float32)
+    W = (rng.standard_normal((R, K), dtype=np.float32) * np.float32(1.0 / math.sqrt(K))).astype(np.float32)
+    return X, W
+
+
+def router_inputs_torch(T: int, K: int, R: int, seed: int = 0, device="cuda"):
+    """(X, W) float32 torch tensors drawn on ``device`` by a seeded generator (large sizes)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    X = torch.randn((T, K), generator=gen, device=device, dtype=torch.float32)
+    W = torch.randn((R, K), generator=gen, device=device, dtype=torch.float32) * (1.0 / math.sqrt(K))
+    return X, W

@@ -225,10 +225,10 @@ def round_bf16(v, lib=None) -> float:
 def router_tolerance(abs_dot, L):
     """Per-element bound for a GPU BF16x3 router logit against the emulation (router_bf16x3).
 
-    The GPU sums the same L = 3K exact BF16 products in FP32 (MMA accumulation,
-    order hardware-defined): |gpu - emu| <= 2^-22 * L * sum_k |x_k w_k| (about
-    L * u32 with u32 = 2^-24, times a factor 4 of margin for the split terms and
-    the accumulator's alignment).  ``abs_dot`` is sum_k |x_k| |w_k|.
+    The GPU sums the same L = 3K exact BF16 products in FP32 (tensor-core
+    accumulation, order hardware-defined): |gpu - emu| <= 2^-22 * L * sum_k
+    |x_k w_k|, the sequential FP32 bound L * 2^-24 * sum|terms| with a factor 4
+    of margin for the accumulator's alignment.  ``abs_dot`` is sum_k |x_k| |w_k|.
     """
     return 2.0 ** -22 * float(L) * np.asarray(abs_dot, dtype=np.float64)
 
