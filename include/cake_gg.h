@@ -190,8 +190,9 @@ int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void 
  * cores.  It drops x_lo w_lo and the split residues:
  * |Y - X W^T| <= 3 * 2^-16 * sum_k |x_k w_k| plus FP32 accumulation error.
  *
- * The plan is a caller-owned POD; `gemm` is the forward plan of the one-expert
- * BF16 GEMM with reduction length 3K that the call runs. */
+ * The plan is a caller-owned POD; `gemm` is the plan of the kernel the call
+ * runs: the grouped GEMM's forward pass in a router mode (E = 1) whose
+ * converter warps split FP32 X tiles into BF16 high and low tiles on chip. */
 typedef struct cake_gg_router_plan {
     int32_t abi_version;     /* CAKE_GG_ABI_VERSION                          */
     int32_t R;               /* router outputs (experts), a multiple of 8    */
@@ -205,19 +206,18 @@ typedef struct cake_gg_router_plan {
 /* Fill *rp.  Pure host arithmetic.  CAKE_GG_ERR_ALIGNMENT unless R and K are
  * multiples of 8; CAKE_GG_ERR_INVALID_ARG for T < 0, R or K < 1, max_sms < 0;
  * CAKE_GG_ERR_OVERFLOW when a size does not fit.  rp->workspace_bytes is the
- * workspace the call needs: the forward plan's workspace, the offsets of the
- * one-expert problem and BF16 copies X' [T, 3K], W' [R, 3K] (about 6 (T + R) K
- * bytes). */
+ * workspace the call needs: the kernel's header, the offsets of the
+ * one-expert problem and W' [R, 2K] = [w_hi | w_lo] in BF16 (4 R K bytes). */
 int cake_gg_router_plan(cake_gg_router_plan_t *rp, int64_t T, int32_t R, int32_t K, int32_t max_sms);
 
 /* Y = X W^T by BF16x3 emulation.  X, W, Y, workspace: device pointers,
  * 16-byte aligned; the workspace is rp->workspace_bytes, caller-owned, filled
  * with zeros once after allocation (as for cake_gg_fwd), unused by anyone else
- * until the stream has run the call.  Enqueues two kernels on `stream` (the
- * split into X' and W', then the forward GEMM); allocates nothing, never
- * synchronises.  Host-detected errors return non-zero and enqueue nothing;
- * the forward pass's device-detected errors land in the workspace's status
- * word (cake_gg_check_status). */
+ * until the stream has run the call.  Enqueues two kernels on `stream` (W's
+ * split into W', then the router kernel); allocates nothing, never
+ * synchronises.  Host-detected errors return non-zero and enqueue nothing; the
+ * router kernel's device-detected errors land in the workspace's status word
+ * (cake_gg_check_status). */
 int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const float *W, float *Y,
                         void *workspace, size_t workspace_bytes, void *stream);
 

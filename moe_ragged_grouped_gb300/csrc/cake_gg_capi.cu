@@ -516,6 +516,98 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
 
 }  // namespace
 
+// ---- FP32 router GEMM (BF16x3): plan and launch of the fused forward kernel ----
+// (called by cake_gg_router.cu; the kernel splits FP32 X tiles into BF16 high
+// and low parts on chip and reads W's parts, W' = [w_hi | w_lo] [R, 2K], from
+// the caller's workspace)
+
+namespace cakegg {
+
+int router_plan(cake_gg_plan_t *plan, int64_t T, int32_t R, int32_t K, int32_t max_sms)
+{
+    std::memset(plan, 0, sizeof(*plan));
+    plan->abi_version = CAKE_GG_ABI_VERSION;
+    plan->pass = CAKE_GG_FWD;
+    plan->E = 1;
+    plan->N = R;
+    plan->K = K;
+    plan->M_max = T;
+    plan->out_dtype = CAKE_GG_FP32;
+    plan->deterministic = 1;
+    plan->max_sms = max_sms;
+    plan->tile_m = kTileM;
+    plan->timeout_ns = kDefaultTimeoutNs;
+    const int32_t bn = R >= 256 ? 256 : ((R + 63) / 64) * 64;
+    plan->tile_n = bn;
+    plan->pair = bn % 128 == 0 ? 2 : 1;
+    plan->tile_k = 64;
+    int stages = kMaxStages;
+    while (stages > 2 && smem_bytes_for(bn, stages, 1, 1, 0, plan->pair, 1, true) > kSmemLimit) --stages;
+    if (smem_bytes_for(bn, stages, 1, 1, 0, plan->pair, 1, true) > kSmemLimit) return CAKE_GG_ERR_UNSUPPORTED;
+    plan->stages = stages;
+    plan->staging_bufs = 1;
+    plan->workspace_bytes = kHeaderBytes;
+    return CAKE_GG_OK;
+}
+
+int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, float *Y, const int32_t *offsets,
+               void *ws, cudaStream_t stream)
+{
+    DevInfo dev;
+    int rc = device_info(&dev);
+    if (rc != CAKE_GG_OK) return rc;
+    if ((rc = get_encoder()) != CAKE_GG_OK) return rc;
+    const int N = plan->N, K = plan->K, bn = plan->tile_n, P = plan->pair;
+    const uint64_t M = uint64_t(plan->M_max);
+    if (M == 0) return CAKE_GG_OK;
+    CUtensorMap ma, mb, mo;
+    const uint64_t dx[2] = {uint64_t(K), M};
+    const uint64_t dw[3] = {2 * uint64_t(K), uint64_t(N), 1};
+    const uint64_t dy[2] = {uint64_t(N), M};
+    if ((rc = encode_map(&ma, X, 2, dx, 32, kTileM, true)) != CAKE_GG_OK) return rc;   // FP32, 32 x 128 boxes
+    if ((rc = encode_map(&mb, Wsplit, 3, dw, 64, uint32_t(bn / P))) != CAKE_GG_OK) return rc;
+    if ((rc = encode_map(&mo, Y, 2, dy, 32, 32, true)) != CAKE_GG_OK) return rc;
+
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    KParams p{};
+    p.offsets = offsets;
+    p.out = Y;
+    p.status = reinterpret_cast<int32_t *>(wsb);
+    p.tickets = nullptr;
+    p.partials = nullptr;
+    p.M_max = plan->M_max;
+    p.E = 1;
+    p.N = N;
+    p.K = K;
+    p.bn = bn;
+    p.bk = 64;
+    p.stages = plan->stages;
+    p.det = 1;
+    p.tmem_cols = tmem_cols_for(bn);
+    p.tma_store = 1;
+    p.epoch = next_epoch();
+    p.pdl = env_int("CAKE_GG_PDL", 1) != 0 ? 1 : 0;
+    p.staging_bufs = plan->staging_bufs;
+    p.debug_flags = plan->debug_flags;
+    p.dyn = env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
+    p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
+    p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
+    p.prefetch = env_int("CAKE_GG_PREFETCH", 0);
+    if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
+
+    const Geom g = make_geom(kModeFwd, 1, N, K, plan->M_max, bn, 0, 0, P, 64);
+    const uint64_t unit_bound = (M / (uint64_t(kTileM) * P) + 2) * uint64_t(g.n_tiles);
+    int grid = dev.sms;
+    if (plan->max_sms > 0 && plan->max_sms < grid) grid = plan->max_sms;
+    if (unit_bound * P < uint64_t(grid)) grid = int(unit_bound * P);
+    grid -= grid % P;
+    if (grid < P) grid = P;
+    const size_t smem = smem_bytes_for(bn, plan->stages, 1, 1, 0, P, 1, true);
+    return launch_router(P, ma, mb, mo, p, grid, smem, stream) == cudaSuccess ? CAKE_GG_OK : CAKE_GG_ERR_CUDA;
+}
+
+}  // namespace cakegg
+
 // Co-run aid: each CTA holds one SM (its shared memory keeps any other CTA
 // off it) for `ns` nanoseconds of global time, sleeping, then exits.  Bounded
 // by time alone; touches no memory.

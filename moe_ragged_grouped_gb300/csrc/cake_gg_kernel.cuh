@@ -36,6 +36,10 @@
 namespace cakegg {
 
 constexpr int kThreads = 192;
+constexpr int kThreadsRouter = 320;   // + 4 converter warps
+constexpr uint32_t kRouterABytes = kTileM * 64 * 4;   // 32 KB: a 128 x 64 FP32 A tile, later its BF16 hi | lo
+
+__host__ __device__ constexpr int threads_for(int kmode) { return kmode == kModeRouter ? kThreadsRouter : kThreads; }
 constexpr int kMaxStages = 8;
 constexpr int kMaxCsplit = 8;   // largest cluster split (portable cluster size)
 constexpr int kStatusBadOffsets = 7;
@@ -85,6 +89,7 @@ struct __align__(16) Ctrl {
     uint64_t empty[kMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t conv[kMaxStages];  // router: the stage's A tile is split into BF16 hi | lo (both CTAs of a pair)
     uint64_t drain;
     uint64_t red_ready;     // cluster split: all csplit partials of the current tile are in place
     uint64_t red_consumed;  // cluster split: every peer has read this CTA's partial
@@ -108,9 +113,12 @@ __host__ __device__ constexpr size_t tables_bytes_for(int E)
 // A stage holds kps = bk / 64 k-chunks of A (128 rows) and B (bn rows).
 // One ring stage: A (128 rows) and this CTA's rows of B (all bn of them, or
 // half of them in a 2-SM pair), kps 64-deep k-chunks each.
-__host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1, int pair = 1)
+__host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1, int pair = 1, bool router = false)
 {
-    return uint32_t(kps) * (kABytes + uint32_t(bn / pair) * 128u);
+    // router: a 64-deep stage of FP32 A (split in place into BF16 hi | lo) and
+    // this CTA's BF16 W rows twice (high, then low parts)
+    return router ? kRouterABytes + 2u * uint32_t(bn / pair) * 128u
+                  : uint32_t(kps) * (kABytes + uint32_t(bn / pair) * 128u);
 }
 
 // Cluster split: one FP32 partial tile (128 rows x bn) per CTA, read by its peers.
@@ -120,9 +128,9 @@ __host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit)
 }
 
 __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps, int staging_bufs, int csplit,
-                                                    int pair, int E)
+                                                    int pair, int E, bool router = false)
 {
-    return 1024 + size_t(stages) * stage_bytes_for(bn, kps, pair) + size_t(staging_bufs) * kStagingBytes +
+    return 1024 + size_t(stages) * stage_bytes_for(bn, kps, pair, router) + size_t(staging_bufs) * kStagingBytes +
            csplit_bytes_for(bn, csplit) + sizeof(Ctrl) + tables_bytes_for(E);
 }
 
@@ -519,11 +527,14 @@ static __device__ __noinline__ void zero_stale_rows(uint8_t *ring, uint32_t ring
 
 // ---------------------------------------------------------------- kernel
 
-template <int MODE, bool SWAP, bool OUT_F32, int PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KMODE, bool SWAP, bool OUT_F32, int PAIR>
+__global__ void __launch_bounds__(threads_for(KMODE), 1)
     cake_gg_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapOut, const KParams p)
 {
+    // the router is the forward pass (walk, epilogue) with FP32 A tiles split by converter warps
+    constexpr bool RT = KMODE == kModeRouter;
+    constexpr int MODE = RT ? kModeFwd : KMODE;
     constexpr bool A_MN = (MODE == kModeWgrad);
     constexpr bool B_MN = (MODE != kModeFwd);
 
@@ -532,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *ring = smem_raw + (ring_u32 - raw_u32);
     const int kps = p.bk / kTileK;                 // k-chunks per stage
-    const uint32_t stage_bytes = stage_bytes_for(p.bn, kps, PAIR);
-    const uint32_t a_bytes = uint32_t(kps) * kABytes;
+    const uint32_t stage_bytes = stage_bytes_for(p.bn, kps, PAIR, RT);
+    const uint32_t a_bytes = RT ? kRouterABytes : uint32_t(kps) * kABytes;
     const uint32_t atom_a = uint32_t(kps) * kBoxBytes;   // MN-major: 64 x bk atom
     const uint32_t atom_b = atom_a;
     const uint32_t chunk_b = uint32_t(p.bn / PAIR) * 128u;  // K-major B: one 64-deep chunk of this CTA's rows
@@ -584,8 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 64) {
         for (int s = 0; s < p.stages; ++s) {
             // the even CTA of a pair also counts its peer's "stage loaded" relay
-            mbar_init(smem_u32(&c->full[s]), PAIR == 2 && rank == 0 ? 2u : 1u);
+            // (router: the relay is the peer converters' "stage split" on conv)
+            mbar_init(smem_u32(&c->full[s]), PAIR == 2 && rank == 0 && !RT ? 2u : 1u);
             mbar_init(smem_u32(&c->empty[s]), 1);
+            if (RT) mbar_init(smem_u32(&c->conv[s]), PAIR == 2 && rank == 0 ? 2u : 1u);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c->tfull[a]), 1);
@@ -594,9 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&c->drain), 1);
         for (int i = 0; i < kUQ; ++i) {
             mbar_init(smem_u32(&c->uq_full[i]), 1);
-            // readers of a slot: MMA (or relay) warp, 4 epilogue warps, and the
-            // odd CTA's producer in a pair
-            mbar_init(smem_u32(&c->uq_empty[i]), PAIR == 2 ? 11u : 5u);
+            // readers of a slot: MMA (or relay) warp, 4 epilogue warps, the
+            // odd CTA's producer in a pair, and the router's 4 converter warps
+            mbar_init(smem_u32(&c->uq_empty[i]), (PAIR == 2 ? 11u : 5u) + (RT ? 4u * PAIR : 0u));
         }
         if (csplit > 0) {
             mbar_init(smem_u32(&c->red_ready), uint32_t(csplit));
@@ -664,9 +677,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block-wide build for many experts (temporaries in the ring)
         int32_t *t_cnt = reinterpret_cast<int32_t *>(ring);
         int32_t *t_cost = t_cnt + kMaxE;
-        for (int i = tid; i <= E; i += kThreads) t_off[i] = p.offsets[i];
+        for (int i = tid; i <= E; i += int(blockDim.x)) t_off[i] = p.offsets[i];
         __syncthreads();
-        for (int e = tid; e < E; e += kThreads) {
+        for (int e = tid; e < E; e += int(blockDim.x)) {
             const int32_t a = t_off[e], b = t_off[e + 1];
             if ((e == 0 && a != 0) || b < a || (e == E - 1 && int64_t(b) > p.M_max)) c->bad = 1;
             const int32_t rows = b - a;
@@ -675,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (walk_is_sorted(g)) {
-            for (int e = tid; e < E; e += kThreads) {
+            for (int e = tid; e < E; e += int(blockDim.x)) {
                 const int32_t ce = t_cost[e];
                 int32_t rank = 0;
                 for (int j = 0; j < E; ++j) {
@@ -685,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 t_order[rank] = e;
             }
         } else {
-            for (int e = tid; e < E; e += kThreads) t_order[e] = e;
+            for (int e = tid; e < E; e += int(blockDim.x)) t_order[e] = e;
         }
         __syncthreads();
         if (warp == 0) {
@@ -860,6 +873,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = jb0; j < jb1; ++j)
                                     tma_load_2d(sb + (j - jb0) * atom_b, &mapB, fb, ti.nt * p.bn + 64 * j, r);
                             }
+                        } else if (RT) {
+                            // router: the FP32 X tile as two 32-column boxes (128-byte rows,
+                            // 128-byte swizzle; converted in place to BF16 hi | lo), then this
+                            // CTA's rows of W's BF16 high and low parts (W' = [w_hi | w_lo])
+                            tma_load_2d(sa, &mapA, fb, k0, ti.row0);
+                            tma_load_2d(sa + kRouterABytes / 2, &mapA, fb, k0 + 32, ti.row0);
+                            // the ring is shallow (64 KB stages) and each stage waits for its
+                            // split as well: pull X `prefetch` stages ahead into L2
+                            if (p.prefetch > 0 && kb + p.prefetch < ti.kb1) {
+                                tma_prefetch_l2_2d(&mapA, k0 + p.prefetch * 64, ti.row0);
+                                tma_prefetch_l2_2d(&mapA, k0 + p.prefetch * 64 + 32, ti.row0);
+                            }
+                            const int32_t wrow = ti.nt * p.bn + rank * (p.bn / PAIR);
+                            tma_load_3d(sb, &mapB, fb, k0, wrow, 0);
+                            tma_load_3d(sb + uint32_t(p.bn / PAIR) * 128u, &mapB, fb, p.K + k0, wrow, 0);
                         } else {
                             // K-major A (X or G): all k-chunks of the stage in one box when chunked
                             if (p.chunk_a) tma_load_3d(sa, &mapA, fb, 0, ti.row0, kb * kps);
@@ -948,8 +976,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
-                // (the even CTA's full barrier also counts the peer's relay)
-                if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
+                // (the even CTA's full barrier also counts the peer's relay; the
+                // router's MMA waits instead for both CTAs' converters on conv,
+                // whose waits cover the copies, and the odd CTA's warp has nothing
+                // to relay)
+                if (RT) {
+                    if (leader && !(PAIR == 2 ? cluster_wait(smem_u32(&c->conv[stage]), phase, c, p)
+                                              : warp_wait(smem_u32(&c->conv[stage]), phase, c, p))) {
+                        ok = false;
+                        break;
+                    }
+                } else if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
                     ok = false;
                     break;
                 }
@@ -965,7 +1002,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t ad0 = A_MN ? smem_desc_sw128(sa, atom_a, 1024) : smem_desc_sw128(sa, 16, 1024);
                         const uint64_t bd0 = B_MN ? smem_desc_sw128(sb, atom_b, 1024) : smem_desc_sw128(sb, 16, 1024);
                         const bool first = kb == ti.kb0;
-                        if (p.bn > 256) {
+                        if (RT) {
+                            // x_hi w_hi + x_hi w_lo + x_lo w_hi into one accumulator
+                            const uint64_t al = smem_desc_sw128(sa + kRouterABytes / 2, 16, 1024);
+                            const uint64_t bl = smem_desc_sw128(sb + uint32_t(p.bn / PAIR) * 128u, 16, 1024);
+                            issue_stage_mmas<1, false, false, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
+                            issue_stage_mmas<1, false, false, PAIR>(d_tmem, ad0, bl, idesc, false, chunk_b);
+                            issue_stage_mmas<1, false, false, PAIR>(d_tmem, al, bd0, idesc, false, chunk_b);
+                        } else if (p.bn > 256) {
                             // this CTA's halves of the two 256-column B tiles sit 2 * (128 / PAIR / 64) atoms apart
                             const uint32_t half = uint32_t(256 / 64 / PAIR) * atom_b;
                             const uint64_t bd1 =
@@ -981,7 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else umma_commit<1>(smem_u32(&c->empty[stage]));
                     }
                     any_mma = true;
-                } else if (lane == 0) {
+                } else if (lane == 0 && !RT) {
                     mbar_arrive_remote(map_to_cta(smem_u32(&c->full[stage]), 0));
                 }
                 __syncwarp();
@@ -1004,7 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-    } else {
+    } else if (!RT || warp < 6) {
         // ======================= epilogue (warps 2..5) =======================
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int lrow = q * 32 + lane;    // tile row held by this thread
@@ -1243,9 +1287,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+    } else {
+        // ================== converters (router: warps 6..9) ==================
+        // Thread `crow` owns A row crow of every stage: its 64 FP32 values (one
+        // 128-byte row in each of the two 32-column boxes, 128-byte swizzle)
+        // become a 128-byte row of BF16 high parts written over the first box
+        // and one of low parts over the second -- the K-major, 128-byte
+        // swizzled layout of a 64-deep BF16 A tile.  A thread reads only its
+        // own row before writing it, so the split needs no barrier inside.
+        const int crow = (warp - 6) * 32 + lane;
+        const int sw = crow & 7;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, ok);) {
+            const Tile ti = decode_tile(g, us.t, t_off, t_order, t_pref, t_spref, rank);
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
+                if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *row_a = ring + size_t(stage) * stage_bytes + size_t(crow) * 128u;
+                uint8_t *row_b = row_a + kRouterABytes / 2;
+                float v[64];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(row_a + ((ch ^ sw) << 4));
+                    const float4 x1 = *reinterpret_cast<const float4 *>(row_b + ((ch ^ sw) << 4));
+                    v[4 * ch] = x0.x; v[4 * ch + 1] = x0.y; v[4 * ch + 2] = x0.z; v[4 * ch + 3] = x0.w;
+                    v[32 + 4 * ch] = x1.x; v[33 + 4 * ch] = x1.y; v[34 + 4 * ch] = x1.z; v[35 + 4 * ch] = x1.w;
+                }
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    // one rounding gives both high parts; widened back exactly from their bits
+                    hi[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                    const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xFFFF0000u);
+                    lo[j] = pack_bf16x2(v[2 * j] - h0, v[2 * j + 1] - h1);      // v - hi is exact in FP32
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    *reinterpret_cast<uint4 *>(row_a + ((ch ^ sw) << 4)) =
+                        make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
+                    *reinterpret_cast<uint4 *>(row_b + ((ch ^ sw) << 4)) =
+                        make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+                }
+                // generic-proxy writes -> visible to the tensor cores' reads
+                fence_proxy_async_smem();
+                named_bar_sync(2, 128);
+                if (warp == 6 && lane == 0) {
+                    if (leader) mbar_arrive(smem_u32(&c->conv[stage]));
+                    else mbar_arrive_cluster(map_to_cta(smem_u32(&c->conv[stage]), 0));
+                }
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
     }
 
-    if (warp >= 2) {
+    if (warp >= 2 && (!RT || warp < 6)) {
         if (lane == 0) bulk_wait_all();  // epilogue stores complete before the CTA retires
         __syncwarp();
     }

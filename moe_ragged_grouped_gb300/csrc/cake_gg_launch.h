@@ -15,6 +15,9 @@ cudaError_t launch_dgrad(bool out_f32, int pair, const CUtensorMap &a, const CUt
                          const KParams &p, int grid, size_t smem, cudaStream_t stream);
 cudaError_t launch_wgrad(bool out_f32, bool swap, int pair, const CUtensorMap &a, const CUtensorMap &b,
                          const CUtensorMap &o, const KParams &p, int grid, size_t smem, cudaStream_t stream);
+// the FP32 router GEMM (BF16x3): the forward pass with on-chip splitting, FP32 output
+cudaError_t launch_router(int pair, const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                          const KParams &p, int grid, size_t smem, cudaStream_t stream);
 
 template <int MODE, bool SWAP, bool OUT_F32, int PAIR>
 cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o, const KParams &p,
@@ -55,7 +58,7 @@ cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         ++na;
     }
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(MODE), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;

@@ -6,12 +6,12 @@
 // Every FP32 value v is split as hi = bf16(v) and lo = bf16(v - hi) (round to
 // nearest, ties to even), and the three leading products of
 // (x_hi + x_lo)(w_hi + w_lo) are kept.  Two launches on the caller's stream:
-//   1. a split kernel writes X' [T, 3K] = [x_hi | x_hi | x_lo] and
-//      W' [R, 3K] = [w_hi | w_lo | w_hi] (BF16) into the caller's workspace,
-//      and the offsets {0, T} of a one-expert problem;
-//   2. the grouped GEMM's forward pass (E = 1, reduction length 3K, FP32
-//      output): Y = X' W'^T = X_hi W_hi^T + X_hi W_lo^T + X_lo W_hi^T, every
-//      product exact in the tensor core and summed in one FP32 accumulator.
+//   1. a small kernel splits W into W' [R, 2K] = [w_hi | w_lo] (BF16) in the
+//      caller's workspace and writes the offsets {0, T} of a one-expert problem;
+//   2. the grouped GEMM's forward kernel in its router mode: it loads FP32 X
+//      tiles, converter warps split them on chip into BF16 high and low tiles,
+//      and the tensor cores sum x_hi w_hi + x_hi w_lo + x_lo w_hi, every product
+//      exact, in one FP32 accumulator.
 #include <cstdint>
 #include <cstring>
 
@@ -19,6 +19,13 @@
 #include <cuda_runtime.h>
 
 #include "../../include/cake_gg.h"
+
+namespace cakegg {
+// (cake_gg_capi.cu) plan and launch of the router mode of the grouped GEMM kernel
+int router_plan(cake_gg_plan_t *plan, int64_t T, int32_t R, int32_t K, int32_t max_sms);
+int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, float *Y, const int32_t *offsets,
+               void *ws, cudaStream_t stream);
+}  // namespace cakegg
 
 namespace {
 
@@ -34,18 +41,17 @@ bool mul_ok(uint64_t a, uint64_t b, uint64_t *out)
     return true;
 }
 
-// Workspace layout: GEMM workspace | offsets {0, T} | X' | W' (each 256-aligned).
+// Workspace layout: GEMM workspace | offsets {0, T} | W' [R, 2K] (each 256-aligned).
 struct RouterLayout {
-    uint64_t offsets_off, xs_off, ws_off, total;
+    uint64_t offsets_off, ws_off, total;
 };
 
 RouterLayout router_layout(const cake_gg_router_plan_t &rp)
 {
     RouterLayout L;
     L.offsets_off = align_up(rp.gemm.workspace_bytes, kAlign);
-    L.xs_off = L.offsets_off + kAlign;
-    L.ws_off = align_up(L.xs_off + uint64_t(rp.T) * 3u * uint64_t(rp.K) * 2u, kAlign);
-    L.total = align_up(L.ws_off + uint64_t(rp.R) * 3u * uint64_t(rp.K) * 2u, kAlign);
+    L.ws_off = L.offsets_off + kAlign;
+    L.total = align_up(L.ws_off + uint64_t(rp.R) * 2u * uint64_t(rp.K) * 2u, kAlign);
     return L;
 }
 
@@ -54,15 +60,14 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
     return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
 }
 
-// One thread: 8 consecutive values of one row (two float4 loads), their BF16
-// high and low parts written as 16-byte vectors at the row's three segments.
-// Rows [0, T) are X ([hi | hi | lo]); rows [T, T + R) are W ([hi | lo | hi]).
+// One thread: 8 consecutive values of one row of W (two float4 loads), their
+// BF16 high and low parts written as 16-byte vectors at k and K + k of W'.
 __global__ void __launch_bounds__(kSplitThreads)
-    router_split_kernel(const float *__restrict__ X, const float *__restrict__ W, uint16_t *__restrict__ Xs,
-                        uint16_t *__restrict__ Ws, int64_t T, int32_t R, int32_t K, int32_t *__restrict__ offsets)
+    router_split_w_kernel(const float *__restrict__ W, uint16_t *__restrict__ Ws, int32_t R, int32_t K, int64_t T,
+                          int32_t *__restrict__ offsets)
 {
     const int64_t groups_per_row = K / 8;
-    const int64_t total = (T + R) * groups_per_row;
+    const int64_t total = int64_t(R) * groups_per_row;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         offsets[0] = 0;
         offsets[1] = int32_t(T);
@@ -71,8 +76,7 @@ __global__ void __launch_bounds__(kSplitThreads)
          gi += int64_t(gridDim.x) * blockDim.x) {
         const int64_t row = gi / groups_per_row;
         const int64_t k = (gi - row * groups_per_row) * 8;
-        const bool is_x = row < T;
-        const float *src = is_x ? X + row * K + k : W + (row - T) * K + k;
+        const float *src = W + row * K + k;
         const float4 v0 = __ldg(reinterpret_cast<const float4 *>(src));
         const float4 v1 = __ldg(reinterpret_cast<const float4 *>(src) + 1);
         const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -86,12 +90,9 @@ __global__ void __launch_bounds__(kSplitThreads)
             hi[j] = pack2(h0, h1);
             lo[j] = pack2(l0, l1);
         }
-        const uint4 vh = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        const uint4 vl = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        uint16_t *dst = is_x ? Xs + row * 3 * int64_t(K) + k : Ws + (row - T) * 3 * int64_t(K) + k;
-        *reinterpret_cast<uint4 *>(dst) = vh;
-        *reinterpret_cast<uint4 *>(dst + K) = is_x ? vh : vl;
-        *reinterpret_cast<uint4 *>(dst + 2 * int64_t(K)) = is_x ? vl : vh;
+        uint16_t *dst = Ws + row * 2 * int64_t(K) + k;
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(dst + K) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
@@ -105,10 +106,10 @@ int cake_gg_router_plan(cake_gg_router_plan_t *rp, int64_t T, int32_t R, int32_t
     std::memset(rp, 0, sizeof(*rp));
     if (T < 0 || T > INT32_MAX || R < 1 || K < 1 || max_sms < 0) return CAKE_GG_ERR_INVALID_ARG;
     if (R % 8 != 0 || K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
-    if (int64_t(K) * 3 > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
+    if (int64_t(K) * 2 > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
     uint64_t t0;
-    if (!mul_ok(uint64_t(T) + uint64_t(R), uint64_t(K) * 6u, &t0)) return CAKE_GG_ERR_OVERFLOW;
-    const int rc = cake_gg_plan(&rp->gemm, CAKE_GG_FWD, 1, T, R, 3 * K, CAKE_GG_FP32, 1, max_sms);
+    if (!mul_ok(uint64_t(T) + uint64_t(R), uint64_t(K) * 4u, &t0)) return CAKE_GG_ERR_OVERFLOW;
+    const int rc = cakegg::router_plan(&rp->gemm, T, R, K, max_sms);
     if (rc != CAKE_GG_OK) return rc;
     rp->abi_version = CAKE_GG_ABI_VERSION;
     rp->T = T;
@@ -126,13 +127,12 @@ int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const f
     if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(Y) |
          reinterpret_cast<uintptr_t>(workspace)) % 16 != 0)
         return CAKE_GG_ERR_ALIGNMENT;
-    if (rp->gemm.K != 3 * rp->K || rp->gemm.N != rp->R || rp->gemm.M_max != rp->T || rp->gemm.E != 1)
+    if (rp->gemm.K != rp->K || rp->gemm.N != rp->R || rp->gemm.M_max != rp->T || rp->gemm.E != 1)
         return CAKE_GG_ERR_INVALID_ARG;
     const RouterLayout L = router_layout(*rp);
     if (workspace_bytes < L.total || rp->workspace_bytes != L.total) return CAKE_GG_ERR_WORKSPACE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets_off);
-    uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs_off);
     uint16_t *wsplit = reinterpret_cast<uint16_t *>(ws + L.ws_off);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -140,16 +140,14 @@ int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const f
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return CAKE_GG_ERR_CUDA;
-    const int64_t groups = (rp->T + rp->R) * int64_t(rp->K / 8);
+    const int64_t groups = int64_t(rp->R) * int64_t(rp->K / 8);
     int64_t blocks = (groups + kSplitThreads - 1) / kSplitThreads;
     const int64_t cap = int64_t(sms) * 8;   // a few resident blocks per SM, grid-stride beyond
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    router_split_kernel<<<unsigned(blocks), kSplitThreads, 0, s>>>(X, W, xs, wsplit, rp->T, rp->R, rp->K, offsets);
+    router_split_w_kernel<<<unsigned(blocks), kSplitThreads, 0, s>>>(W, wsplit, rp->R, rp->K, rp->T, offsets);
     if (cudaGetLastError() != cudaSuccess) return CAKE_GG_ERR_CUDA;
-    if (rp->T == 0) return CAKE_GG_OK;
-    return cake_gg_fwd(&rp->gemm, xs, wsplit, Y, offsets, CAKE_GG_FP32, 1, workspace, rp->gemm.workspace_bytes,
-                       stream);
+    return cakegg::router_run(&rp->gemm, X, wsplit, Y, offsets, workspace, s);
 }
 
 }  // extern "C"

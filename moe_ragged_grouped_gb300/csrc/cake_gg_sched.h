@@ -39,6 +39,9 @@ namespace cakegg {
 constexpr int kModeFwd = 0;
 constexpr int kModeDgrad = 1;
 constexpr int kModeWgrad = 2;
+// The FP32 router GEMM (BF16x3): the forward pass's walk and epilogue, FP32
+// operand tiles split into BF16 high and low parts inside the kernel.
+constexpr int kModeRouter = 3;
 
 constexpr int kTileM = 128;     // MMA rows (TMEM lanes)
 constexpr int kTileK = 64;      // reduction elements of one k-chunk (one 128-byte swizzle row)

@@ -130,6 +130,12 @@ def test_moe_gate_up(pass_):
     run_and_check(wl.moe_gate_up(), pass_, "bf16", 1, np.random.default_rng(3))
 
 
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+def test_moe_gate_up_fp32_output(pass_):
+    """FP32 output of the forward and data gradient at full size (the FP32 accumulator stored as is)."""
+    run_and_check(wl.moe_gate_up(), pass_, "fp32", 1, np.random.default_rng(4))
+
+
 @pytest.mark.parametrize("out_dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("det,env", [(1, None), (0, None), (1, {"CAKE_GG_SPLIT_CHUNK": "16"}),
                                      (0, {"CAKE_GG_SPLIT_CHUNK": "16"})])
