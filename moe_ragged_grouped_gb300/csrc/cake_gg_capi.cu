@@ -454,6 +454,9 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.out = out;
     p.status = reinterpret_cast<int32_t *>(wsb);
     p.tickets = reinterpret_cast<uint64_t *>(wsb + w.tickets_off);
+    // an early split of a tile polls this long for the tile's other partials
+    // before leaving the finish to whoever arrives last
+    p.spin_ns = uint64_t(env_int("CAKE_GG_SPIN_NS", 6000) > 0 ? env_int("CAKE_GG_SPIN_NS", 6000) : 0);
     p.partials = reinterpret_cast<float *>(wsb + w.partials_off);
     p.M_max = plan->M_max;
     p.E = E;

@@ -53,7 +53,8 @@ struct KParams {
     const int32_t *offsets;
     void *out;
     int32_t *status;
-    uint64_t *tickets;      // per split output tile: (epoch << 32) | arrivals
+    uint64_t *tickets;      // per split output tile: (epoch << 32) | arrivals, then slices claimed
+    uint64_t spin_ns;       // how long an early split waits for its tile's other partials (0 = never)
     float *partials;
     int64_t M_max;
     int32_t E, N, K;
@@ -100,6 +101,7 @@ struct __align__(16) Ctrl {
     int32_t abort_flag;
     int32_t bad;
     int32_t last_flag;
+    int32_t claim;          // split finish: the slice the epilogue claimed last
 };
 
 // Walk tables after the control block, sized by the launch's E: off[E+1]
@@ -266,6 +268,15 @@ __device__ __forceinline__ bool warp_next_unit(UnitSeq &u, int64_t unit0, int64_
 // S concurrent updates race, so the CAS loop ends within S tries (bounded at
 // 64; on exhaustion the caller is told it is not last and the status word
 // records a timeout).
+// A claim on a split tile's ticket word once it holds all S arrivals of this
+// call: the old count minus S is the next 64-column slice to reduce (>= the
+// slice count: none left).  A plain fetch-and-add, so it can be in flight
+// while the previous slice is reduced.
+__device__ __forceinline__ unsigned long long ticket_claim(uint64_t *t)
+{
+    return atomicAdd(reinterpret_cast<unsigned long long *>(t), 1ull);
+}
+
 __device__ __forceinline__ uint32_t ticket_arrive(uint64_t *t, uint32_t epoch, int32_t *status)
 {
     uint64_t cur = *reinterpret_cast<volatile uint64_t *>(t);
@@ -326,19 +337,20 @@ __device__ __forceinline__ void store_scalar(void *out, int64_t idx, float v)
     else static_cast<uint16_t *>(out)[idx] = f32_to_bf16_rn(v);
 }
 
-// Finish of one row of a split output tile by the tile's last arriving split:
-// the FP32 partials p_0 .. p_{nsum-1} (each laid out [col/4][row] float4,
-// slot_stride floats apart) are summed in split order (s = p_0; s += p_1; ...)
-// and row `lrow` of the tile is written (transposed for swapped operands).
+// Finish of one row of one slice (float4 columns [c4_begin, c4_end)) of a
+// split output tile: the FP32 partials p_0 .. p_{nsum-1} (each laid out
+// [col/4][row] float4, slot_stride floats apart) are summed in split order
+// (s = p_0; s += p_1; ...) and row `lrow` of the slice is written (transposed
+// for swapped operands).
 // Each batch loads CB float4 columns of SB slots: SB * CB independent
 // 16-byte loads in flight per thread.  A lone accumulator (non-deterministic
 // splits) is zeroed as it is read, ready for the next call.
 template <int CB, int SB, bool OUT_F32, bool TRANSPOSED>
 __device__ __forceinline__ void finish_split_row(float *base0, int nsum, int64_t slot_stride, bool zero_after,
-                                                 int bn, int lrow, bool row_ok, int32_t cols_valid, void *out,
-                                                 int64_t out_base, int64_t ld)
+                                                 int c4_begin, int c4_end, int lrow, bool row_ok,
+                                                 int32_t cols_valid, void *out, int64_t out_base, int64_t ld)
 {
-    for (int c4 = 0; c4 < bn / 4; c4 += CB) {
+    for (int c4 = c4_begin; c4 < c4_end; c4 += CB) {
         float4 acc[CB];
         for (int s0 = 0; s0 < nsum; s0 += SB) {
             float4 b[SB][CB];
@@ -1253,37 +1265,68 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             }
 
             if (split) {
-                // ticket: the last split of this output tile to arrive finishes it
+                // ticket: count this split's arrival.  Every split that then sees all
+                // S partials of the tile written (the last to arrive at once, earlier
+                // ones after a short bounded poll) claims 64-column slices of the tile
+                // and reduces them; the last one keeps claiming until none is left, so
+                // the tile is always finished and no split ever waits on work that has
+                // not started.  A slice's sum is in split order, whoever computes it.
+                // Claims are fetch-and-adds on the same ticket word once it holds all
+                // S arrivals of this call (count - S = the slice); the next claim is
+                // issued before the current slice is reduced, hiding its latency.
                 __syncwarp();
                 named_bar_sync(1, 128);
                 if (etid == 0) {
                     __threadfence();
                     const uint32_t before = ticket_arrive(p.tickets + ti.ticket, p.epoch, p.status);
-                    c->last_flag = (before == uint32_t(ti.S - 1));
+                    bool all_in = before == uint32_t(ti.S - 1);
+                    if (!all_in && before != 0xffffffffu && p.spin_ns > 0) {
+                        const uint64_t t0 = global_timer_ns();
+                        while (!all_in && global_timer_ns() - t0 < p.spin_ns) {
+                            const uint64_t w = ld_acquire_gpu_u64(p.tickets + ti.ticket);
+                            all_in = uint32_t(w >> 32) == p.epoch && uint32_t(w & 0xffffffffu) >= uint32_t(ti.S);
+                        }
+                    }
+                    c->last_flag = all_in;
                 }
                 __syncwarp();
                 named_bar_sync(1, 128);
-                const bool last = c->last_flag != 0;
+                const bool all_in = c->last_flag != 0;
                 named_bar_sync(1, 128);  // everyone read last_flag before the next tile rewrites it
-                if (last) {
+                if (all_in) {
                     __threadfence();
                     float *base0 = slots ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
                                                : slot_ptr;
                     const int nsum = slots ? ti.S : 1;
                     const int64_t slot_stride = int64_t(kTileM) * p.bn;
+                    const int nsl = (p.bn + 63) / 64;   // 64-column slices (16 float4 columns)
                     constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
                     // (16 loads in flight; 8 in swapped kernels, which also hold
                     // the cluster reduction and otherwise pass the register limit)
                     constexpr int kCB = kTr ? 8 : 16;
-                    if (nsum == 1)
-                        finish_split_row<kCB, 1, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow, row_ok,
-                                                               cols_valid, p.out, out_base, ld);
-                    else if (nsum == 2)
-                        finish_split_row<kCB / 2, 2, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow,
+                    uint64_t *tk = p.tickets + ti.ticket;
+                    if (etid == 0) c->claim = int32_t(uint32_t(ticket_claim(tk)) - uint32_t(ti.S));
+                    named_bar_sync(1, 128);
+                    int sl = c->claim;
+                    named_bar_sync(1, 128);  // everyone read the claim before it is replaced
+                    while (sl >= 0 && sl < nsl) {
+                        unsigned long long nxt = 0;
+                        if (etid == 0) nxt = ticket_claim(tk);  // in flight while this slice is reduced
+                        const int c4b = sl * 16, c4e = sl * 16 + 16 < p.bn / 4 ? sl * 16 + 16 : p.bn / 4;
+                        if (nsum == 1)
+                            finish_split_row<kCB, 1, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, c4b, c4e, lrow,
                                                                    row_ok, cols_valid, p.out, out_base, ld);
-                    else
-                        finish_split_row<kCB / 4, 4, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, p.bn, lrow,
-                                                                   row_ok, cols_valid, p.out, out_base, ld);
+                        else if (nsum == 2)
+                            finish_split_row<kCB / 2, 2, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, c4b, c4e,
+                                                                       lrow, row_ok, cols_valid, p.out, out_base, ld);
+                        else
+                            finish_split_row<kCB / 4, 4, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, c4b, c4e,
+                                                                       lrow, row_ok, cols_valid, p.out, out_base, ld);
+                        if (etid == 0) c->claim = int32_t(uint32_t(nxt) - uint32_t(ti.S));
+                        named_bar_sync(1, 128);
+                        sl = c->claim;
+                        named_bar_sync(1, 128);
+                    }
                 }
             }
         }

@@ -481,6 +481,13 @@ __device__ __forceinline__ void red_add_v4_f32(float *addr, float a, float b, fl
                  : "memory");
 }
 
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *addr)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint64_t atomic_cas_acq_rel_gpu_u64(uint64_t *addr, uint64_t cmp, uint64_t val)
 {
     uint64_t old;
