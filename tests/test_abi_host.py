@@ -228,3 +228,54 @@ def test_tile_walk_split_tail():
     plan, tiles = _check_walk_coverage("wgrad", [59491, 25895, 15919, 11271], N=6144, K=2048)
     assert plan.tail_splits > 1
     assert not [t for t in tiles if t[4] > 1]
+
+
+# ---- FP32 router GEMM (BF16x3) planning, host side -----------------------------------------
+
+
+def test_router_plan_validates_and_sizes_its_workspace():
+    """cake_gg_router_plan: R and K multiples of 8, T >= 0; the workspace is the kernel header,
+    the one-expert offsets and W' [R, 2K] in BF16; the plan it runs is the one-expert forward
+    pass over the original K (the router kernel splits X itself)."""
+    for args, code in [((16, 250, 64), gg.CAKE_GG_ERR_ALIGNMENT), ((16, 256, 60), gg.CAKE_GG_ERR_ALIGNMENT),
+                       ((-1, 256, 64), gg.CAKE_GG_ERR_INVALID_ARG), ((16, 0, 64), gg.CAKE_GG_ERR_INVALID_ARG),
+                       ((16, 256, 64, -1), gg.CAKE_GG_ERR_INVALID_ARG)]:
+        with pytest.raises(gg.CakeGGError) as ei:
+            gg.cake_gg_router_plan(*args)
+        assert ei.value.code == code, args
+    rp = gg.cake_gg_router_plan(16384, 256, 4096)
+    assert (rp.T, rp.R, rp.K) == (16384, 256, 4096)
+    g = rp.gemm
+    assert (g.E, g.N, g.K, g.M_max, g.pass_) == (1, 256, 4096, 16384, gg.CAKE_GG_FWD)
+    assert g.out_dtype == gg.CAKE_GG_FP32 and g.deterministic == 1
+    assert (g.tile_n, g.tile_k, g.pair) == (256, 64, 2) and g.stages >= 2
+    hdr = (int(g.workspace_bytes) + 255) // 256 * 256
+    assert rp.workspace_bytes == hdr + 256 + (256 * 2 * 4096 * 2 + 255) // 256 * 256
+    # small router widths run single CTAs on 64-wide tiles
+    small = gg.cake_gg_router_plan(300, 16, 64)
+    assert (small.gemm.tile_n, small.gemm.pair) == (64, 1)
+    # no dependence on max_sms beyond the field itself
+    capped = gg.cake_gg_router_plan(16384, 256, 4096, 10)
+    assert capped.workspace_bytes == rp.workspace_bytes and capped.gemm.stages == g.stages
+
+
+def test_router_plan_struct_layout():
+    """The ctypes mirror of cake_gg_router_plan_t: 8-byte aligned fields, the nested forward plan last."""
+    assert gg.CakeGGRouterPlan.gemm.offset % 8 == 0
+    assert gg.CakeGGRouterPlan.workspace_bytes.offset == 24
+    assert ctypes.sizeof(gg.CakeGGRouterPlan) == 32 + ctypes.sizeof(gg.CakeGGPlan)
+
+
+def test_router_call_rejects_bad_arguments_before_any_cuda_call():
+    """cake_gg_router_fp32's host checks (null, misaligned, workspace) run before any CUDA call."""
+    lib = gg.load_library()
+    rp = gg.cake_gg_router_plan(256, 64, 128)
+    good, nb = 1 << 20, int(rp.workspace_bytes)
+    call = lambda x, w, y, ws, n: lib.cake_gg_router_fp32(ctypes.byref(rp), x, w, y, ws, n, None)
+    assert call(0, good, good, good, nb) == gg.CAKE_GG_ERR_INVALID_ARG          # null X
+    assert call(good, good, good, 0, nb) == gg.CAKE_GG_ERR_INVALID_ARG          # null workspace
+    assert call(good + 4, good, good, good, nb) == gg.CAKE_GG_ERR_ALIGNMENT     # misaligned X
+    assert call(good, good, good, good, nb - 1) == gg.CAKE_GG_ERR_WORKSPACE     # workspace too small
+    bad = gg.CakeGGRouterPlan.from_buffer_copy(rp)
+    bad.gemm.K = 3 * rp.K                                                       # plan / call mismatch
+    assert lib.cake_gg_router_fp32(ctypes.byref(bad), good, good, good, good, nb, None) == gg.CAKE_GG_ERR_INVALID_ARG
