@@ -55,6 +55,20 @@ def test_bitwise_across_runs_and_sm_caps(pass_, sizes, N, K, env, monkeypatch):
         assert torch.equal(capped.view(torch.int32), ref.view(torch.int32)), f"max_sms={cap} differs"
 
 
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad", "wgrad"])
+def test_many_experts_bitwise_across_sm_caps(pass_):
+    """E = 300 (tables built block-wide, heaviest first): bitwise equal across runs and SM
+    caps."""
+    import torch
+    rng = np.random.default_rng(31)
+    sizes = [int(v) for v in rng.multinomial(12000, rng.dirichlet(np.full(300, 0.5)))]
+    X, W, G, off = inputs(sizes, 128, 256, seed=31)
+    ref = run(pass_, X, W, G, off, "fp32", 1)
+    for cap in (0, 100, 148, 7):
+        again = run(pass_, X, W, G, off, "fp32", 1, max_sms=cap)
+        assert torch.equal(again.view(torch.int32), ref.view(torch.int32)), f"max_sms={cap} differs"
+
+
 def test_forward_rows_independent_of_other_experts():
     """A forward output row depends only on its own row and its expert's weights."""
     import torch

@@ -68,6 +68,34 @@ def check_case(pass_, sizes, N, K, out_dtype, det, seed=0, extra_rows=0, max_sms
 PASSES = ["fwd", "dgrad", "wgrad"]
 
 
+def many_expert_sizes(E, M, seed, alpha):
+    """Ragged sizes of E experts summing to M (Dirichlet shares, so some are empty)."""
+    rng = np.random.default_rng(seed)
+    sizes = [int(v) for v in rng.multinomial(M, rng.dirichlet(np.full(E, alpha)))]
+    sizes[0] = sizes[E // 2] = sizes[-1] = 0
+    return sizes
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("det", [1, 0])
+def test_many_experts_block_built_tables(pass_, det):
+    """E = 200 > 32: the walk tables (offsets, heaviest-first order, prefixes) are built by the
+    whole CTA rather than one warp; skewed sizes with empty experts, first and last included."""
+    sizes = many_expert_sizes(200, 9000, 29, 0.7)
+    check_case(pass_, sizes, 128, 192, "fp32", det, seed=29, extra_rows=5)
+
+
+@pytest.mark.parametrize("pass_", PASSES)
+def test_maximum_expert_count(pass_):
+    """E = 1024, the most the on-chip tables hold: mostly tiny experts, two long ones, empty
+    ones anywhere."""
+    rng = np.random.default_rng(30)
+    sizes = [int(v) for v in rng.integers(0, 12, 1024)]
+    sizes[0] = sizes[-1] = sizes[511] = 0
+    sizes[100], sizes[900] = 700, 1300
+    check_case(pass_, sizes, 64, 128, "bf16", 1, seed=30, extra_rows=3)
+
+
 @pytest.mark.parametrize("pass_", PASSES)
 @pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("det", [1, 0])
