@@ -97,6 +97,15 @@ def test_maximum_expert_count(pass_):
 
 
 @pytest.mark.parametrize("pass_", PASSES)
+@pytest.mark.parametrize("N,K", [(8, 8), (8, 136), (136, 8), (24, 40)])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_smallest_widths(pass_, N, K, out_dtype):
+    """N and K down to 8, the smallest the interface takes: every tile and copy box reaches
+    past the tensor's edge (zero fill on loads, clipped or masked stores)."""
+    check_case(pass_, [0, 130, 1, 257], N, K, out_dtype, 1, seed=32, extra_rows=3)
+
+
+@pytest.mark.parametrize("pass_", PASSES)
 @pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("det", [1, 0])
 def test_tiny_config(pass_, out_dtype, det):
