@@ -18,7 +18,9 @@
  *
  * Deterministic mode (PR #8258: "bitwise reproducible from run to run"): every
  * output element is computed by a fixed sequence of FP32 operations that
- * depends only on (pass, E, M_max, N, K, out_dtype) and the offsets -- never on
+ * depends only on the plan -- which cake_gg_plan() derives from (pass, E,
+ * M_max, N, K, out_dtype) alone unless a plan override below is set -- and
+ * the offsets: never on
  * max_sms, on which CTA runs a tile, or on arrival order (the weight
  * gradient takes its tiles from a counter at run time; the results are the
  * same bits whichever CTA computes a tile).  Split reductions add FP32
@@ -42,6 +44,22 @@
  * it.  Split-tile tickets are tagged with a per-call number and never need
  * clearing; the weight gradient's tile counter (workspace header) is zeroed
  * by the last CTA of each call.
+ *
+ * Environment overrides (tuning and test hooks, unset in normal use):
+ *   read by cake_gg_plan(), recorded in the plan it fills (a deterministic
+ *   plan's summation order follows them):
+ *     CAKE_GG_TILE_N (64..256), CAKE_GG_TILE_K (64, 128, 256), CAKE_GG_PAIR=0
+ *     (single CTAs only), CAKE_GG_WIDE (0: no 256 x 512 weight-gradient tiles,
+ *     2: wherever they fit), CAKE_GG_WIDE_FD=1 (512-wide forward / data-
+ *     gradient tiles), CAKE_GG_SPLIT_CHUNK (k-blocks per split, 0 = no split),
+ *     CAKE_GG_CSPLIT (0, or 2..8 cluster splits), CAKE_GG_TAIL=0 (no split
+ *     tail), CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2);
+ *   read by each compute call, changing no result:
+ *     CAKE_GG_PDL=0 (no programmatic dependent launch), CAKE_GG_DYN=0 (static
+ *     unit order), CAKE_GG_SPIN_NS (an early split's poll for its tile's
+ *     other partials, default 6000), CAKE_GG_PREFETCH (L2 prefetch distance
+ *     in stages), CAKE_GG_STACK=0 and CAKE_GG_TMA_STORE=0 (plainer copy and
+ *     store paths).
  *
  * Errors: host-detected problems return a non-zero cake_gg_status_t and
  * enqueue nothing.  Problems only the GPU can see (bad offsets, a bounded wait
