@@ -279,3 +279,59 @@ def test_router_call_rejects_bad_arguments_before_any_cuda_call():
     bad = gg.CakeGGRouterPlan.from_buffer_copy(rp)
     bad.gemm.K = 3 * rp.K                                                       # plan / call mismatch
     assert lib.cake_gg_router_fp32(ctypes.byref(bad), good, good, good, good, nb, None) == gg.CAKE_GG_ERR_INVALID_ARG
+
+
+C_PROGRAM = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "cake_gg.h"
+
+int main(void)
+{
+    cake_gg_plan_t plan;
+    cake_gg_router_plan_t rp;
+    int rc = cake_gg_plan(&plan, CAKE_GG_WGRAD, 8, 131072, 3072, 4096, CAKE_GG_BF16, 1, 0);
+    if (rc != CAKE_GG_OK) {
+        printf("error %d %s\n", rc, cake_gg_strerror(rc));
+        return 1;
+    }
+    rc = cake_gg_router_plan(&rp, 16384, 256, 4096, 0);
+    if (rc != CAKE_GG_OK) return 2;
+    printf("%u %u %u %u %u %u %u\n", (unsigned)sizeof(cake_gg_plan_t), (unsigned)offsetof(cake_gg_plan_t, M_max),
+           (unsigned)offsetof(cake_gg_plan_t, timeout_ns), (unsigned)offsetof(cake_gg_plan_t, workspace_bytes),
+           (unsigned)offsetof(cake_gg_plan_t, staging_bufs), (unsigned)sizeof(cake_gg_router_plan_t),
+           (unsigned)offsetof(cake_gg_router_plan_t, gemm));
+    printf("%d %d %d %d %d %d %llu %llu\n", plan.tile_n, plan.tile_k, plan.stages, plan.pair, plan.split_chunk,
+           plan.tail_splits, (unsigned long long)plan.workspace_bytes, (unsigned long long)rp.workspace_bytes);
+    return 0;
+}
+"""
+
+
+def test_header_compiles_as_c99_and_layouts_match(tmp_path):
+    """A strict C99 program includes the header, links the library and plans on the host: the
+    ABI is plain C, its struct layouts are the ctypes mirrors', and C callers get the same plan."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(gg.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(ROOT, "include"), str(src), "-o", str(exe), "-L", libdir, "-lcake_gg",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stdout + run.stderr
+    layout, fields = [line.split() for line in run.stdout.strip().splitlines()]
+    P, R = gg.CakeGGPlan, gg.CakeGGRouterPlan
+    assert [int(v) for v in layout] == [ctypes.sizeof(P), P.M_max.offset, P.timeout_ns.offset,
+                                        P.workspace_bytes.offset, P.staging_bufs.offset, ctypes.sizeof(R),
+                                        R.gemm.offset]
+    plan = gg.cake_gg_plan("wgrad", 8, 131072, 3072, 4096, "bf16", 1)
+    rp = gg.cake_gg_router_plan(16384, 256, 4096)
+    assert [int(v) for v in fields] == [plan.tile_n, plan.tile_k, plan.stages, plan.pair, plan.split_chunk,
+                                        plan.tail_splits, plan.workspace_bytes, rp.workspace_bytes]
