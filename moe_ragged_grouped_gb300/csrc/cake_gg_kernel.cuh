@@ -92,7 +92,7 @@ struct __align__(16) Ctrl {
     uint64_t tempty[2];
     uint64_t conv[kMaxStages];  // router: the stage's A tile is split into BF16 hi | lo (both CTAs of a pair)
     uint64_t drain;
-    uint64_t red_ready;     // cluster split: all csplit partials of the current tile are in place
+    uint64_t red_ready;     // cluster split: every split's part of this CTA's slice has arrived
     uint64_t red_consumed;  // cluster split: every peer has read this CTA's partial
     uint64_t uq_full[kUQ];  // unit queue slot written (by the even CTA's producer)
     uint64_t uq_empty[kUQ]; // (even CTA) every role of the cluster has read the slot
@@ -123,10 +123,12 @@ __host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1, int 
                   : uint32_t(kps) * (kABytes + uint32_t(bn / pair) * 128u);
 }
 
-// Cluster split: one FP32 partial tile (128 rows x bn) per CTA, read by its peers.
+// Cluster split: the receive buffer of this CTA's slice of a tile's float4
+// columns, one copy per split (S x ceil(cols4 / S) <= cols4 + S - 1 columns of
+// 128 rows x 16 bytes).
 __host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit)
 {
-    return csplit > 0 ? size_t(kTileM) * size_t(bn) * 4u : 0u;
+    return csplit > 0 ? size_t(kTileM) * 16u * size_t(bn / 4 + csplit) : 0u;
 }
 
 __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps, int staging_bufs, int csplit,
@@ -408,64 +410,6 @@ __device__ __forceinline__ void finish_split_row(float *base0, int nsum, int64_t
     }
 }
 
-// Row `lrow` of this CTA's slice [q0, q1) of float4 columns of a
-// cluster-split tile: the csplit FP32 partials (one per CTA of the cluster,
-// each at red_buf in its own shared memory, laid out [col/4][row] float4) are
-// read through distributed shared memory, summed in split order (s = 0, 1,
-// ..., csplit - 1) and stored (transposed for swapped operands).  A batch
-// holds 4 float4 columns x 4 splits in registers (compile-time indices); more
-// splits are added group after group, still in split order.
-template <bool OUT_F32, bool TRANSPOSED>
-__device__ __forceinline__ void cluster_reduce_slice(uint32_t my_buf, int csplit, int q0, int q1, int lrow,
-                                                     bool store_ok, int32_t cols_valid, void *out,
-                                                     int64_t out_base, int64_t ld)
-{
-    constexpr int QB = 4;   // float4 columns per batch
-    constexpr int SG = 4;   // splits per group
-    for (int qc = q0; qc < q1; qc += QB) {
-        float4 acc[QB];
-        for (int s0 = 0; s0 < csplit; s0 += SG) {
-            float4 b4[QB][SG];
-#pragma unroll
-            for (int jj = 0; jj < QB; ++jj)
-#pragma unroll
-                for (int u = 0; u < SG; ++u)
-                    if (s0 + u < csplit && qc + jj < q1)
-                        b4[jj][u] = ld_shared_cluster_f4(map_to_cta(my_buf, uint32_t(s0 + u)) +
-                                                         uint32_t(((qc + jj) * kTileM + lrow) * 16));
-#pragma unroll
-            for (int jj = 0; jj < QB; ++jj) {
-#pragma unroll
-                for (int u = 0; u < SG; ++u) {
-                    if (s0 + u < csplit && qc + jj < q1) {
-                        if (s0 + u == 0) {
-                            acc[jj] = b4[jj][u];
-                        } else {
-                            acc[jj].x += b4[jj][u].x;
-                            acc[jj].y += b4[jj][u].y;
-                            acc[jj].z += b4[jj][u].z;
-                            acc[jj].w += b4[jj][u].w;
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int jj = 0; jj < QB; ++jj) {
-            const int col = (qc + jj) * 4;
-            if (qc + jj < q1 && store_ok && col < cols_valid) {
-                const float vv[4] = {acc[jj].x, acc[jj].y, acc[jj].z, acc[jj].w};
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int64_t idx = TRANSPOSED ? out_base + int64_t(col + q4) * ld + lrow
-                                                   : out_base + int64_t(lrow) * ld + col + q4;
-                    store_scalar<OUT_F32>(out, idx, vv[q4]);
-                }
-            }
-        }
-    }
-}
-
 // One warp's 32-row x 128-byte slab of an output tile (this lane's row in w)
 // through the warp's staging buffer and a TMA tensor store at (x, y[, z]).
 // With two buffers per warp they alternate across every slab the warp ever
@@ -624,7 +568,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             mbar_init(smem_u32(&c->uq_empty[i]), (PAIR == 2 ? 11u : 5u) + (RT ? 4u * PAIR : 0u));
         }
         if (csplit > 0) {
-            mbar_init(smem_u32(&c->red_ready), uint32_t(csplit));
+            mbar_init(smem_u32(&c->red_ready), 1u);   // this CTA's arrival; the peers' bytes as tx
             mbar_init(smem_u32(&c->red_consumed), uint32_t(csplit));
         }
         fence_barrier_init();
@@ -1115,14 +1059,30 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             const bool row_ok = lrow < rows_valid;
 
             if (csplit > 0) {
-                // ---- cluster split: partial in shared memory, reduced through DSMEM ----
-                // my previous partial must have been read by every peer
+                // ---- cluster split: partial slices pushed to their owners, summed there ----
+                // CTA r of the cluster owns float4 columns [r per, (r + 1) per) of the
+                // tile.  Every CTA pushes its partial's part of each slice into the
+                // owner's receive buffer rec[s][q][row] (s = the pushing CTA's split)
+                // with st.async, counted in bytes on the owner's red_ready; the owner
+                // sums rec[0 .. S-1] in split order and stores its slice.  Before
+                // pushing a tile's slices a CTA waits until every owner has summed
+                // the previous tile's (red_consumed).
                 if (cs_it > 0) {
                     bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t((cs_it - 1) & 1), c, p);
                     if (!named_bar_and(1, 128, okc)) break;
                 }
                 // only the float4 columns that reach the output travel
                 const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
+                const int cs = csplit > 0 ? csplit : 1;   // (csplit > 0 here; keeps the division well-defined)
+                const int per = (nq + cs - 1) / cs;
+                const int q0 = rank * per;
+                const int q1 = q0 + per < nq ? q0 + per : nq;
+                uint8_t *rec = reinterpret_cast<uint8_t *>(red_buf);
+                const uint32_t rec_u32 = smem_u32(rec);
+                // this CTA's arrival on its own red_ready, expecting the other splits' bytes
+                if (etid == 0)
+                    mbar_arrive_expect_tx(smem_u32(&c->red_ready),
+                                          uint32_t(csplit - 1) * uint32_t(q1 > q0 ? q1 - q0 : 0) * kTileM * 16u);
                 for (int c0 = 0; c0 < 4 * nq; c0 += 32) {
                     float v[32];
                     if (empty_tile) {
@@ -1136,35 +1096,52 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                     }
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4)
-                        *reinterpret_cast<float4 *>(red_buf + (((c0 >> 2) + j4) * kTileM + lrow) * 4) =
-                            make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const int qi = (c0 >> 2) + j4;   // float4 column of the tile
+                        if (qi < nq) {
+                            const int owner = qi / per;
+                            const uint32_t off = uint32_t(((rank * per + qi - owner * per) * kTileM + lrow) * 16);
+                            const float4 x = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
+                            if (owner == rank)
+                                *reinterpret_cast<float4 *>(rec + off) = x;
+                            else
+                                st_async_v4(map_to_cta(rec_u32 + off, uint32_t(owner)), x,
+                                            map_to_cta(smem_u32(&c->red_ready), uint32_t(owner)));
+                        }
+                    }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&c->tempty[acc]));
-                // publish: every peer may read my partial (the epilogue barrier
-                // orders the other threads' stores before this thread's
-                // cluster-scope release arrivals)
-                named_bar_sync(1, 128);
-                if (etid == 0) {
-                    fence_acq_rel_cluster();
-                    for (int j = 0; j < csplit; ++j)
-                        mbar_arrive_cluster_relaxed(map_to_cta(smem_u32(&c->red_ready), j));
-                }
+                named_bar_sync(1, 128);   // this CTA's own part of its slice is in place
                 bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
                 if (!named_bar_and(1, 128, okr)) break;
-                // my slice of float4 columns, summed over the splits in split order
-                const int cs = csplit > 0 ? csplit : 1;  // (csplit > 0 here; keeps the division well-defined)
-                const int per = (nq + cs - 1) / cs;
-                const int q0 = rank * per;
-                const int q1 = q0 + per < nq ? q0 + per : nq;
-                const uint32_t my_buf = smem_u32(red_buf);
+                // my slice, summed over the splits in split order (s = 0, 1, ..., S - 1)
                 constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
-                cluster_reduce_slice<OUT_F32, kTr>(my_buf, csplit, q0, q1, lrow, row_ok && ti.valid, cols_valid,
-                                                   p.out, out_base, ld);
-                // done reading the peers' partials (a cluster's last unit needs no
-                // signal: the teardown cluster barrier keeps every peer alive)
+                for (int q = q0; q < q1; ++q) {
+                    const uint8_t *src = rec + (size_t(q - q0) * kTileM + lrow) * 16;
+                    float4 a = *reinterpret_cast<const float4 *>(src);
+                    for (int sp = 1; sp < csplit; ++sp) {
+                        const float4 b = *reinterpret_cast<const float4 *>(src + size_t(sp) * per * kTileM * 16);
+                        a.x += b.x;
+                        a.y += b.y;
+                        a.z += b.z;
+                        a.w += b.w;
+                    }
+                    const int col = q * 4;
+                    if (row_ok && ti.valid && col < cols_valid) {
+                        const float vv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int64_t idx = kTr ? out_base + int64_t(col + q4) * ld + lrow
+                                                    : out_base + int64_t(lrow) * ld + col + q4;
+                            store_scalar<OUT_F32>(p.out, idx, vv[q4]);
+                        }
+                    }
+                }
+                // done with my receive buffer (a cluster's last unit needs no signal:
+                // every push has landed once its owner's wait ended, and the teardown
+                // cluster barrier keeps every peer alive)
                 if (t + unit_step < total) {
                     named_bar_sync(1, 128);
                     if (etid == 0)

@@ -171,21 +171,23 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Relaxed arrive on an mbarrier given by its cluster address.  After one
-// fence_acq_rel_cluster, a run of these publishes the thread's (and, through
-// a preceding CTA barrier, its CTA's) prior writes to every peer that later
-// acquires the arrivals, with one fence instead of one release per arrive.
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 // Asynchronous 8-byte store into a peer CTA's shared memory whose arrival
 // counts 8 bytes down on the peer's mbarrier (both addresses from mapa).
 __device__ __forceinline__ void st_async_b64(uint32_t remote_addr, int64_t v, uint32_t remote_bar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(remote_addr),
                  "l"(v), "r"(remote_bar)
+                 : "memory");
+}
+
+// 16-byte asynchronous store into a peer CTA's shared memory, counted in bytes
+// on the peer's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                 "r"(__float_as_uint(v.w)), "r"(remote_bar)
                  : "memory");
 }
 
@@ -217,18 +219,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
         : "memory");
     return done != 0;
 }
-
-__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
