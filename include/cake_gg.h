@@ -16,7 +16,8 @@
  *   offsets[E] <= M_max.  Rows >= offsets[E] of Y and dX are never written;
  *   the weight gradient ignores them.  An empty expert gets an exact zero dW.
  *
- * Deterministic mode (PR #8258: "bitwise reproducible from run to run"): every
+ * Deterministic mode (PR #8258, opening summary: the deterministic kernel
+ * gives the same bits on every run): every
  * output element is computed by a fixed sequence of FP32 operations that
  * depends only on the plan -- which cake_gg_plan() derives from (pass, E,
  * M_max, N, K, out_dtype) alone unless a plan override below is set -- and
@@ -25,9 +26,10 @@
  * gradient takes its tiles from a counter at run time; the results are the
  * same bits whichever CTA computes a tile).  Split reductions add FP32
  * partials in split order and round once.  Non-deterministic mode
- * (PR #8258: tail partial tiles added "into a shared FP32 sum with atomic
- * reductions", last CTA per tile found by a "per-tile ticket") may change the
- * order of the weight gradient's split sums from run to run.  The forward and
+ * (PR #8258, opening summary, 2nd paragraph: split tail partials are added
+ * into one FP32 tile by atomic reductions, and a ticket per tile tells the
+ * last CTA to finish it) may change the order of the weight gradient's split
+ * sums from run to run.  The forward and
  * data-gradient passes never split and are deterministic in both modes.
  *
  * Ownership: the caller owns every buffer (inputs, outputs, offsets,
@@ -42,8 +44,10 @@
  * (and again after a device-detected error).  Every call that ends without a
  * device-detected error leaves it ready for the next call, so no call clears
  * it.  Split-tile tickets are tagged with a per-call number and never need
- * clearing; the weight gradient's tile counter (workspace header) is zeroed
- * by the last CTA of each call.
+ * clearing; that number lives in the workspace header and each call's last
+ * CTA advances it on the device, so a call replayed from a captured CUDA
+ * graph gets a fresh number as well.  The unit counter (workspace header) is
+ * zeroed by the last CTA of each call.
  *
  * Environment overrides (tuning and test hooks, unset in normal use):
  *   read by cake_gg_plan(), recorded in the plan it fills (a deterministic
@@ -153,15 +157,22 @@ int cake_gg_fwd(const cake_gg_plan_t *plan, const void *X, const void *W, void *
                 const int32_t *offsets, int out_dtype, int deterministic,
                 void *workspace, size_t workspace_bytes, void *stream);
 
-/* Data gradient dX = G W_e per expert.  G [M_max, N], W [E, N, K],
- * dX [M_max, K].  Writes rows [0, offsets[E]) of dX only. */
+/* Data gradient dX = G W_e per expert (PR #8258 opening summary: the input
+ * gradient of the grouped expert layer; PR #8363 "Definitions" for the dense
+ * family's [T, d_out] gradient and [T, d_in] result).  G [M_max, N],
+ * W [E, N, K], dX [M_max, K]: device pointers, 16-byte aligned.  out_dtype and
+ * deterministic must equal the plan's.  Writes rows [0, offsets[E]) of dX
+ * only. */
 int cake_gg_dgrad(const cake_gg_plan_t *plan, const void *G, const void *W, void *dX,
                   const int32_t *offsets, int out_dtype, int deterministic,
                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* Weight gradient dW_e = G_e^T X_e per expert, the sum over the expert's rows
- * (the ragged reduction).  G [M_max, N], X [M_max, K], dW [E, N, K]; every
- * element of dW is written (zeros for an empty expert). */
+ * (the ragged reduction; PR #8258 opening summary, with BF16 or FP32 dW and
+ * its split tails, and PR #8363 "Definitions" for the dense family's
+ * [d_out, d_in] weight gradient).  G [M_max, N], X [M_max, K], dW [E, N, K]:
+ * device pointers, 16-byte aligned; every element of dW is written (zeros for
+ * an empty expert).  out_dtype and deterministic must equal the plan's. */
 int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
                   const int32_t *offsets, int out_dtype, int deterministic,
                   void *workspace, size_t workspace_bytes, void *stream);
@@ -183,7 +194,9 @@ int cake_gg_wgrad(const cake_gg_plan_t *plan, const void *G, const void *X, void
  *    rejected with CAKE_GG_ERR_SCRATCH_LIMIT before anything is enqueued.
  *  - The first call on each device looks up the scratch array's device
  *    address (with that device current); make that first call before any
- *    stream capture begins.
+ *    stream capture begins.  The address is kept together with the context
+ *    it belongs to: after a device reset (a new primary context) the next
+ *    call looks it up again, so make that call before any capture as well.
  *  - Every call on a device shares the one scratch array, which keeps the
  *    last call's contents; each call clears the parts that must start at
  *    zero.  Calls whose kernels overlap on the GPU (different streams without
@@ -198,9 +211,9 @@ int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void 
 /* ---- FP32 router GEMM (BF16x3 emulation) ---------------------------------
  *
  * The dense projection family's FP32 router GEMM (flashinfer PR #8438,
- * "Summary": "an FP32 router GEMM (256 experts, BF16x3 emulation)"): logits
- * Y [T, R] = X [T, K] W^T, with X [T, K], router weights W [R, K] and Y all
- * FP32, row-major.  The emulation (the pages name it and nothing more; the
+ * "Summary", which names a router GEMM over 256 experts in FP32 emulated
+ * with three BF16 products): logits Y [T, R] = X [T, K] W^T, with X [T, K],
+ * router weights W [R, K] and Y all FP32, row-major.  The emulation (the pages name it and nothing more; the
  * usual reading is taken): every value v is split as hi = bf16(v) and
  * lo = bf16(v - hi), round to nearest even, and
  *   Y[t, r] ~= sum_k x_hi w_hi + x_hi w_lo + x_lo w_hi

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include <cuda.h>
@@ -25,6 +26,7 @@ constexpr int kMaxClusterSplit = 8;         // portable cluster size
 constexpr size_t kSmemLimit = kSmemOptInLimit;
 constexpr uint64_t kHeaderBytes = 256;      // workspace: status word, unit scheduler words, padding
 constexpr uint64_t kSchedOffset = 64;       // next-unit counter; CTAs-retired counter 128 bytes further
+constexpr uint64_t kEpochOffset = 128;      // the last call's ticket tag
 constexpr int kMaxTailSplits = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -141,15 +143,6 @@ struct WsLayout {
     uint64_t total;
     bool ok;
 };
-
-std::atomic<uint32_t> g_epoch{0};
-
-uint32_t next_epoch()
-{
-    uint32_t e = g_epoch.fetch_add(1) + 1;
-    if (e == 0) e = g_epoch.fetch_add(1) + 1;
-    return e;
-}
 
 WsLayout ws_layout(const cake_gg_plan_t &pl)
 {
@@ -469,7 +462,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.det = plan->deterministic ? 1 : 0;
     p.tmem_cols = tmem_cols_for(bn);
     p.tma_store = tma_store ? 1 : 0;
-    p.epoch = next_epoch();
+    p.epoch_word = reinterpret_cast<uint32_t *>(wsb + kEpochOffset);
     p.stack_a = stack_a ? 1 : 0;
     p.stack_b = stack_b ? 1 : 0;
     p.chunk_a = chunk_a ? 1 : 0;
@@ -485,6 +478,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     // (the cluster split keeps its static one-unit-per-cluster walk)
     p.dyn = plan->cluster_splits == 0 && env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
     p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
+    // tickets are in use (split tiles or a split tail): tag them per call
+    p.retire = p.dyn || ((mode == kModeWgrad) && (p.kchunk > 0 || plan->tail_splits > 1)) ? 1 : 0;
     p.tail = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_units : 0;
     p.tail_s = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_splits : 0;
     if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
@@ -588,11 +583,12 @@ int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, f
     p.det = 1;
     p.tmem_cols = tmem_cols_for(bn);
     p.tma_store = 1;
-    p.epoch = next_epoch();
+    p.epoch_word = reinterpret_cast<uint32_t *>(wsb + kEpochOffset);
     p.pdl = env_int("CAKE_GG_PDL", 1) != 0 ? 1 : 0;
     p.staging_bufs = plan->staging_bufs;
     p.debug_flags = plan->debug_flags;
     p.dyn = env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
+    p.retire = p.dyn;
     p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
     p.prefetch = env_int("CAKE_GG_PREFETCH", 0);
@@ -949,8 +945,48 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
 static __device__ __align__(256) uint8_t g_noalloc_scratch[CAKE_GG_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-void *g_noalloc_scratch_addr[64];  // per device; filled by the first call on that device
+
+// The scratch array's device address, per device, with the context it was
+// looked up in: after a device reset (a new primary context) the array lives
+// at a new address, so a call whose current context differs looks it up again.
+struct NoallocAddr {
+    CUcontext ctx;
+    void *addr;
+};
+NoallocAddr g_noalloc_addr[64];
+std::mutex g_noalloc_mu;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+
+int noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CAKE_GG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_ctx_get_current) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return CAKE_GG_ERR_CUDA;
+        g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    }
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return CAKE_GG_ERR_CUDA;
+    NoallocAddr &a = g_noalloc_addr[dev];
+    if (ctx == nullptr || a.addr == nullptr || a.ctx != ctx) {
+        // (the lookup also makes the device's primary context current when no
+        // context was yet)
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return CAKE_GG_ERR_CUDA;
+        if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return CAKE_GG_ERR_CUDA;
+        a.addr = ptr;
+        a.ctx = ctx;
+    }
+    *out = a.addr;
+    return CAKE_GG_OK;
 }
+
+}  // namespace
 
 extern "C" int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, const void *X, void *dW,
                                      const int32_t *offsets, int out_dtype, int deterministic,
@@ -958,20 +994,20 @@ extern "C" int cake_gg_wgrad_noalloc(const cake_gg_plan_t *plan, const void *G, 
 {
     if (!plan) return CAKE_GG_ERR_INVALID_ARG;
     if (plan->workspace_bytes > CAKE_GG_NOALLOC_SCRATCH_BYTES) return CAKE_GG_ERR_SCRATCH_LIMIT;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CAKE_GG_ERR_CUDA;
-    if (!g_noalloc_scratch_addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return CAKE_GG_ERR_CUDA;
-        g_noalloc_scratch_addr[dev] = ptr;
-    }
-    void *scratch = g_noalloc_scratch_addr[dev];
-    int rc = check_call(plan, CAKE_GG_WGRAD, G, X, dW, offsets, out_dtype, deterministic, scratch,
-                        CAKE_GG_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
     if (rc != CAKE_GG_OK) return rc;
-    // callers cannot reach the scratch, so each call clears what must start at zero
+    rc = check_call(plan, CAKE_GG_WGRAD, G, X, dW, offsets, out_dtype, deterministic, scratch,
+                    CAKE_GG_NOALLOC_SCRATCH_BYTES);
+    if (rc != CAKE_GG_OK) return rc;
+    // callers cannot reach the scratch, so each call clears what must start at
+    // zero: all of it but the ticket tag, which must keep advancing from call
+    // to call (the tickets themselves are never cleared)
     const WsLayout w = ws_layout(*plan);
-    if (cudaMemsetAsync(scratch, 0, w.zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    uint8_t *sb = static_cast<uint8_t *>(scratch);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(sb, 0, kEpochOffset, st) != cudaSuccess ||
+        cudaMemsetAsync(sb + kEpochOffset + 4, 0, w.zero_bytes - (kEpochOffset + 4), st) != cudaSuccess)
         return CAKE_GG_ERR_CUDA;
     return run(plan, kModeWgrad, G, X, dW, offsets, scratch, static_cast<cudaStream_t>(stream));
 }

@@ -12,10 +12,11 @@
 //   warps 2..5  epilogue: tcgen05.ld -> registers -> BF16 (round to nearest
 //               even, once) or FP32 -> global, masked at expert and tensor
 //               edges; the weight gradient's split tiles finish through a
-//               per-tile ticket (PR #8258: "the last CTA to arrive on a tile ...
-//               loads the sum ... and writes the output tile"), summing the
-//               FP32 partials in split order in deterministic mode or through
-//               FP32 atomic adds otherwise.
+//               per-tile ticket (PR #8258, opening summary, 2nd paragraph: the
+//               CTA that arrives last on a tile reads the summed partials and
+//               stores the output tile), summing the FP32 partials in split
+//               order in deterministic mode or through FP32 atomic adds
+//               otherwise.
 //
 // Operands are staged with a 128-byte swizzle.  K-major tiles (rows of 64
 // reduction elements) come from one box of {64, rows}; MN-major tiles come
@@ -65,7 +66,8 @@ struct KParams {
     int32_t det;
     int32_t tmem_cols;
     int32_t tma_store;      // epilogue through shared memory + TMA tensor stores
-    uint32_t epoch;         // per-call tag of the tickets (never 0)
+    uint32_t *epoch_word;   // workspace word: the last call's ticket tag (this call uses it + 1, never 0)
+    int32_t retire;         // CTAs count their retirement; the last resets the counters and advances the tag
     int32_t stack_a;        // MN-major A through an atom-stacked map: one box per stage
     int32_t stack_b;        // MN-major B likewise (all of this CTA's B atoms in one box)
     int32_t chunk_a;        // K-major A through a {64, rows, K/64} map: one box per stage
@@ -102,6 +104,7 @@ struct __align__(16) Ctrl {
     int32_t bad;
     int32_t last_flag;
     int32_t claim;          // split finish: the slice the epilogue claimed last
+    uint32_t epoch;         // this call's ticket tag (read from the workspace at set-up)
 };
 
 // Walk tables after the control block, sized by the launch's E: off[E+1]
@@ -579,6 +582,12 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     // start its own part 1
     grid_dependency_wait();
     grid_launch_dependents();
+    if (tid == 32 && p.retire) {
+        // this call's ticket tag: one past the last call's, which the previous
+        // call's last CTA wrote (a call replayed from a CUDA graph advances too)
+        uint32_t e = *reinterpret_cast<volatile uint32_t *>(p.epoch_word) + 1u;
+        c->epoch = e == 0 ? 1u : e;
+    }
     if (E <= 32) {
         // one warp builds every table: lane e holds expert e
         if (warp == 0) {
@@ -702,7 +711,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         }
         return;
     }
-    // peers' barriers must exist before a multicast or a remote arrive reaches
+    // peers' barriers must exist before a commit signal or a remote arrive reaches
     // them: warps that reach into peers (all of a pair; the epilogue of a
     // cluster split) wait here, the others only at teardown
     const bool early_wait = PAIR == 2 || warp >= 2;
@@ -1013,17 +1022,16 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         int cs_it = 0;                     // cluster-split tiles reduced so far
         int stg_buf = 0;                   // staging buffer this warp writes next
         bool qok = true;
+        // cluster split: the bytes of this CTA's slice that its peers push for
+        // the current tile, whether that tile's receive phase is still open (the
+        // peers may push into it) and whether this CTA has armed it
+        uint32_t cs_expect = 0;
+        bool cs_open = false, cs_armed = false;
         for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, qok); ++it) {
             const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
             const int acc = nacc == 2 ? (it & 1) : 0;
             const uint32_t acc_phase = nacc == 2 ? (uint32_t(it >> 1) & 1u) : (uint32_t(it) & 1u);
-            // (in a pair the even CTA's MMA commit arrives on both CTAs' tfull)
-            bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
-            ok = named_bar_and(1, 128, ok);
-            if (!ok) break;
-            tc_fence_after_sync();
-
             const bool empty_tile = ti.kb1 <= ti.kb0;
             const bool split = (MODE == kModeWgrad) && ti.S > 1 && ti.valid;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc) * acc_stride;
@@ -1057,6 +1065,22 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             }
             if (cols_valid > p.bn) cols_valid = p.bn;
             const bool row_ok = lrow < rows_valid;
+            // cluster split: this CTA's float4 columns [q0, q1) of the tile's nq
+            const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
+            const int per = csplit > 0 ? (nq + csplit - 1) / csplit : 0;
+            const int q0 = rank * per;
+            const int q1 = q0 + per < nq ? q0 + per : nq;
+            if (csplit > 0) {
+                cs_expect = uint32_t(csplit - 1) * uint32_t(q1 > q0 ? q1 - q0 : 0) * kTileM * 16u;
+                cs_open = true;
+                cs_armed = false;
+            }
+
+            // (in a pair the even CTA's MMA commit arrives on both CTAs' tfull)
+            bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
+            ok = named_bar_and(1, 128, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
 
             if (csplit > 0) {
                 // ---- cluster split: partial slices pushed to their owners, summed there ----
@@ -1072,17 +1096,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     if (!named_bar_and(1, 128, okc)) break;
                 }
                 // only the float4 columns that reach the output travel
-                const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
-                const int cs = csplit > 0 ? csplit : 1;   // (csplit > 0 here; keeps the division well-defined)
-                const int per = (nq + cs - 1) / cs;
-                const int q0 = rank * per;
-                const int q1 = q0 + per < nq ? q0 + per : nq;
                 uint8_t *rec = reinterpret_cast<uint8_t *>(red_buf);
                 const uint32_t rec_u32 = smem_u32(rec);
                 // this CTA's arrival on its own red_ready, expecting the other splits' bytes
-                if (etid == 0)
-                    mbar_arrive_expect_tx(smem_u32(&c->red_ready),
-                                          uint32_t(csplit - 1) * uint32_t(q1 > q0 ? q1 - q0 : 0) * kTileM * 16u);
+                if (etid == 0) mbar_arrive_expect_tx(smem_u32(&c->red_ready), cs_expect);
+                cs_armed = true;
                 for (int c0 = 0; c0 < 4 * nq; c0 += 32) {
                     float v[32];
                     if (empty_tile) {
@@ -1116,6 +1134,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 named_bar_sync(1, 128);   // this CTA's own part of its slice is in place
                 bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
                 if (!named_bar_and(1, 128, okr)) break;
+                cs_open = false;   // every peer's part of the slice has landed
                 // my slice, summed over the splits in split order (s = 0, 1, ..., S - 1)
                 constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
                 for (int q = q0; q < q1; ++q) {
@@ -1255,13 +1274,13 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 named_bar_sync(1, 128);
                 if (etid == 0) {
                     __threadfence();
-                    const uint32_t before = ticket_arrive(p.tickets + ti.ticket, p.epoch, p.status);
+                    const uint32_t before = ticket_arrive(p.tickets + ti.ticket, c->epoch, p.status);
                     bool all_in = before == uint32_t(ti.S - 1);
                     if (!all_in && before != 0xffffffffu && p.spin_ns > 0) {
                         const uint64_t t0 = global_timer_ns();
                         while (!all_in && global_timer_ns() - t0 < p.spin_ns) {
                             const uint64_t w = ld_acquire_gpu_u64(p.tickets + ti.ticket);
-                            all_in = uint32_t(w >> 32) == p.epoch && uint32_t(w & 0xffffffffu) >= uint32_t(ti.S);
+                            all_in = uint32_t(w >> 32) == c->epoch && uint32_t(w & 0xffffffffu) >= uint32_t(ti.S);
                         }
                     }
                     c->last_flag = all_in;
@@ -1306,6 +1325,16 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     }
                 }
             }
+        }
+        if (csplit > 0 && cs_open && etid == 0) {
+            // left on an abort while a tile's receive phase was open: peers may
+            // have pushed (or be pushing) their parts of this CTA's slice, and
+            // asynchronous stores into it must land before the CTA retires.  Arm
+            // the phase if this CTA had not, then wait for it with a short limit
+            // (a peer that gave up before pushing never completes it; a peer
+            // pushes all of its parts of a tile or none).
+            if (!cs_armed) mbar_arrive_expect_tx(smem_u32(&c->red_ready), cs_expect);
+            drain_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), 2000000ull);
         }
     } else {
         // ================== converters (router: warps 6..9) ==================
@@ -1389,12 +1418,14 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         tc_fence_after_sync();
         tmem_dealloc<2>(tmem_base, uint32_t(p.tmem_cols));
     }
-    if (p.dyn && tid == 0) {
+    if (p.retire && tid == 0) {
         // the last CTA to retire leaves the unit counter at zero for the next
-        // call (every CTA's fetches are done when it counts itself)
+        // call (every CTA's fetches are done when it counts itself) and stores
+        // this call's ticket tag (every CTA read the old one at its set-up)
         __threadfence();
         if (atomicAdd(p.sched + 32, 1) == int32_t(gridDim.x) - 1) {
             atomicExch(p.sched, 0);
+            atomicExch(reinterpret_cast<unsigned int *>(p.epoch_word), c->epoch);
             atomicExch(p.sched + 32, 0);
         }
     }

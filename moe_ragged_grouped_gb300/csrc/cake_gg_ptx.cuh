@@ -106,16 +106,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int32_t c0, int32_t c1, int32_t c2, int32_t c3, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(mask)
-        : "memory");
-}
-
 // Pull a box of a tensor into L2 only (no shared memory, no barrier): issued
 // some stages ahead of the real load so that its data is an L2 hit.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2)
@@ -132,29 +122,6 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                      reinterpret_cast<uint64_t>(map)),
                  "r"(c0), "r"(c1)
                  : "memory");
-}
-
-// Multicast variants: the box lands at the same shared-memory offset in every
-// CTA of `mask` (this cluster), each of whose mbarrier at `bar`'s offset gets
-// the complete-tx.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int32_t c0, int32_t c1, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                               int32_t c0, int32_t c1, int32_t c2, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-        : "memory");
 }
 
 // Address of the same shared-memory offset in CTA `rank` of this cluster.

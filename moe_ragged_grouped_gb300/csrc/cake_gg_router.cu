@@ -1,6 +1,7 @@
 // cake_gg_router.cu -- the FP32 router GEMM of the dense projection family by
-// BF16x3 emulation (flashinfer PR #8438, "Summary": "an FP32 router GEMM (256
-// experts, BF16x3 emulation)"): logits Y [T, R] = X [T, K] W^T with FP32 X and
+// BF16x3 emulation (flashinfer PR #8438, "Summary", which names a router GEMM
+// over 256 experts in FP32 emulated with three BF16 products): logits
+// Y [T, R] = X [T, K] W^T with FP32 X and
 // router weights W [R, K], FP32 output.
 //
 // Every FP32 value v is split as hi = bf16(v) and lo = bf16(v - hi) (round to

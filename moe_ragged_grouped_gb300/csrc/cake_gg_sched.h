@@ -60,7 +60,7 @@ struct Geom {
     int32_t n_tiles;      // output column tiles
     int32_t m_tiles_w;    // weight gradient: output row tiles
     int32_t nkb;          // forward / data gradient: reduction k-blocks
-    int32_t pair;         // CTAs per unit (1, or 2 for a multicast pair)
+    int32_t pair;         // CTAs per unit (1, or 2 for a 2-SM pair sharing one MMA)
     int32_t bk;           // reduction elements per pipeline stage (64 * k-chunks per stage)
     int32_t csplit;       // weight gradient: splits of a tile run by one cluster (0 = off)
     int32_t tail;         // weight gradient: the last `tail` units of the walk are split ...

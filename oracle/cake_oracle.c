@@ -221,8 +221,8 @@ int oracle_wgrad_at(const uint16_t *G, const uint16_t *X, const int32_t *off, in
 /* ---- FP32 router GEMM (BF16x3 emulation) -------------------------------
  *
  * The dense projection family's FP32 router GEMM (flashinfer PR #8438,
- * "Summary": "an FP32 router GEMM (256 experts, BF16x3 emulation)"):
- * logits Y [T, R] = X [T, K] W^T with FP32 X and router weights W [R, K].
+ * "Summary", which names a router GEMM over 256 experts in FP32 emulated
+ * with three BF16 products): logits Y [T, R] = X [T, K] W^T with FP32 X and router weights W [R, K].
  * The pages name the emulation and nothing more; the reading taken here is
  * the usual one: every FP32 value v is split as hi = bf16(v) (round to
  * nearest, ties to even) and lo = bf16(v - hi), and the product keeps the

@@ -2,9 +2,14 @@
 
 Inputs are drawn on the GPU by a seeded generator (the benchmark's recipe) and
 copied to the host for the FP64 oracle, which evaluates sampled outputs one by
-one: uniform random elements plus every expert's first and last rows, tile
-edges, and (weight gradient) every expert including empty ones.  Each sample
-must satisfy the parity bound |gpu - ref| <= 2^-8 |ref| + 2^-18 L max|a| max|b|.
+one.  The sample is stratified by output tile: one random element from every
+128-row x 64-column block of every output (forward / data gradient: blocks of
+each expert's own rows, starting at its first row, so every tile any launch
+shape takes is hit, including every piece of a split tail and every 64-column
+slice a split finish reduces; weight gradient: blocks of every expert's dW,
+empty experts included), plus uniform random elements, every expert's first
+and last rows and the tile edges.  Each sample must satisfy the parity bound
+|gpu - ref| <= 2^-8 |ref| + 2^-18 L max|a| max|b|.
 
 Workloads (E experts, M routed rows, K, N):
   dense projection   E=1, T=16384, d_in in {4096, 5120}, d_out in {48, 64, 512, 1024, 4096}
@@ -49,6 +54,39 @@ def inputs(wk):
     return _cache[wk.name]
 
 
+def tile_strata_rows_cols(off, n_out, rng):
+    """One random (row, col) in every 128-row x 64-column block of each expert's rows."""
+    rows, cols = [], []
+    ncb = (n_out + 63) // 64
+    c0 = np.arange(ncb, dtype=np.int64) * 64
+    clen = np.minimum(64, n_out - c0)
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 <= r0:
+            continue
+        starts = np.arange(r0, r1, 128, dtype=np.int64)
+        lens = np.minimum(128, r1 - starts)
+        rs = np.repeat(starts, ncb) + (rng.random(starts.size * ncb) * np.repeat(lens, ncb)).astype(np.int64)
+        cs = np.tile(c0, starts.size) + (rng.random(starts.size * ncb) * np.tile(clen, starts.size)).astype(np.int64)
+        rows.append(rs)
+        cols.append(cs)
+    return np.concatenate(rows), np.concatenate(cols)
+
+
+def tile_strata_wgrad(E, N, K, rng):
+    """One random (e, n, k) in every 128 x 64 block of every expert's dW [N, K]."""
+    n0 = np.arange(0, N, 128, dtype=np.int64)
+    k0 = np.arange(0, K, 64, dtype=np.int64)
+    nn, kk = np.meshgrid(n0, k0, indexing="ij")
+    nn, kk = nn.ravel(), kk.ravel()
+    es = np.repeat(np.arange(E, dtype=np.int64), nn.size)
+    nb = np.tile(nn, E)
+    kb = np.tile(kk, E)
+    ns = nb + (rng.random(nb.size) * np.minimum(128, N - nb)).astype(np.int64)
+    ks = kb + (rng.random(kb.size) * np.minimum(64, K - kb)).astype(np.int64)
+    return es, ns, ks
+
+
 def sample_rows_cols(off, n_out, rng, n=384):
     M = int(off[-1])
     rows = list(rng.integers(0, M, n))
@@ -61,7 +99,8 @@ def sample_rows_cols(off, n_out, rng, n=384):
     edge = np.array([0, n_out - 1, min(63, n_out - 1), min(64, n_out - 1), min(255, n_out - 1),
                      min(256, n_out - 1)], np.int64)
     cols[:edge.shape[0]] = edge
-    return rows, cols
+    sr, sc = tile_strata_rows_cols(off, n_out, rng)
+    return np.concatenate([rows, sr]), np.concatenate([cols, sc])
 
 
 def run_and_check(wk, pass_, out_dtype, det, rng, env=None, monkeypatch=None):
@@ -84,6 +123,8 @@ def run_and_check(wk, pass_, out_dtype, det, rng, env=None, monkeypatch=None):
         ns = rng.integers(0, wk.N, es.shape[0])
         ks = rng.integers(0, wk.K, es.shape[0])
         ns[:4], ks[:4] = [0, wk.N - 1, 0, wk.N - 1], [0, wk.K - 1, wk.K - 1, 0]
+        se, sn, sk = tile_strata_wgrad(wk.E, wk.N, wk.K, rng)
+        es, ns, ks = np.concatenate([es, se]), np.concatenate([ns, sn]), np.concatenate([ks, sk])
         ref = oracle.wgrad_at(Gb, Xb, off, wk.E, es, ns, ks)
         idx = torch.from_numpy(es * wk.N * wk.K + ns * wk.K + ks).cuda()
         got_t = out.view(-1)[idx]

@@ -1,8 +1,8 @@
 """Pins for the oracle's FP32 router GEMM (BF16x3 emulation), on the CPU.
 
 The dense projection family's FP32 router GEMM (flashinfer PR #8438,
-"Summary": "an FP32 router GEMM (256 experts, BF16x3 emulation)") computes
-logits Y = X W^T from FP32 X [T, K] and router weights W [R, K].  The reading
+"Summary", which names a router GEMM over 256 experts in FP32 emulated with
+three BF16 products) computes logits Y = X W^T from FP32 X [T, K] and router weights W [R, K].  The reading
 taken: v = hi + lo with hi = bf16(v) and lo = bf16(v - hi), round to nearest
 even, and Y ~= sum_k x_hi w_hi + x_hi w_lo + x_lo w_hi.  These tests tie the
 oracle to facts other than itself: the rounding rule at hand-picked ties and

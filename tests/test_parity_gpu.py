@@ -405,21 +405,83 @@ def test_wide_forward_and_data_gradient_bitwise_equal_to_256_wide(pass_, monkeyp
 @pytest.mark.parametrize("pass_", PASSES)
 def test_results_unchanged_next_to_a_spinner(pass_):
     """A bounded spinner on another stream holds 32 SMs for 5 ms: CTAs that start late find the
-    unit counter drained or take what is left; the output bits do not change."""
+    unit counter drained or take what is left.  Each result next to the spinner is within the
+    parity bound of the FP64 oracle and bitwise equal to the result without it."""
     import torch
     Xb, Wb, Gb, off = make_inputs([3000, 0, 5000, 1200], 512, 768, seed=26)
     X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
     ref = run(pass_, X, W, G, off, "fp32", 1)
+    ref64 = reference(pass_, Xb, Wb, Gb, off)
     side = torch.cuda.Stream()
-    for _ in range(2):
+    M = int(off[-1])
+    for i in range(2):
         assert gg.cake_gg_corun_spinner(32, 5_000_000, side.cuda_stream) == gg.CAKE_GG_OK
         out = run(pass_, X, W, G, off, "fp32", 1)
         torch.cuda.synchronize()
-        M = int(off[-1])
         a, b = (ref, out) if pass_ == "wgrad" else (ref[:M], out[:M])
+        assert_parity(pass_, out_to_f64(b), ref64, Xb, Wb, Gb, off, f"{pass_} next to a spinner, run {i}")
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
 def test_spinner_rejects_bad_arguments():
     assert gg.cake_gg_corun_spinner(0, 1000, 0) == gg.CAKE_GG_ERR_INVALID_ARG
     assert gg.cake_gg_corun_spinner(8, 20_000_000_000, 0) == gg.CAKE_GG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("det,env", [(1, {"CAKE_GG_SPLIT_CHUNK": "8"}), (0, {"CAKE_GG_SPLIT_CHUNK": "8"}),
+                                     (1, {"CAKE_GG_TAIL": "1"})])
+def test_ticketed_weight_gradient_replayed_from_a_cuda_graph(det, env, monkeypatch):
+    """Split tiles finish through tickets tagged with a per-call number that the workspace keeps
+    and each call advances on the device, so a call captured once in a CUDA graph and replayed
+    gets a fresh number every replay: each of three replays is within the oracle's bound (and,
+    deterministic, bitwise the eager call's result)."""
+    import torch
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    if "CAKE_GG_TAIL" in env:
+        sizes, N, K = [8300, 8200, 8192, 8100], 3072, 4096   # a split tail: 4 units x 8 pieces
+    else:
+        sizes, N, K = [3000, 0, 5000, 1200], 512, 768
+    Xb, Wb, Gb, off = make_inputs(sizes, N, K, seed=28)
+    X, G = to_dev(Xb), to_dev(Gb)
+    E, M = len(sizes), Xb.shape[0]
+    plan = gg.cake_gg_plan("wgrad", E, M, N, K, "fp32", det)
+    assert plan.split_chunk == 8 or plan.tail_splits > 1
+    ws = gg.make_workspace(plan, "cuda")
+    offs = torch.from_numpy(off).cuda()
+    out = torch.empty((E, N, K), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        assert gg.cake_gg_wgrad(plan, G, X, out, offs, "fp32", det, ws, stream=stream.cuda_stream) == gg.CAKE_GG_OK
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        rc = gg.cake_gg_wgrad(plan, G, X, out, offs, "fp32", det, ws, stream=stream.cuda_stream)
+    assert rc == gg.CAKE_GG_OK
+    if K > 1024:
+        # sampled: one element per 128 x 64 block of every expert's dW
+        rng = np.random.default_rng(3)
+        es = np.repeat(np.arange(E), (N // 128) * (K // 64))
+        nb = np.tile(np.repeat(np.arange(0, N, 128), K // 64), E)
+        kb = np.tile(np.tile(np.arange(0, K, 64), N // 128), E)
+        ns, ks = nb + rng.integers(0, 128, nb.size), kb + rng.integers(0, 64, kb.size)
+        ref = oracle.wgrad_at(Gb, Xb, off, E, es, ns, ks)
+        idx = torch.from_numpy(es * N * K + ns * K + ks).cuda()
+        ma = float(np.abs(oracle.bf16_bits_to_f64(Gb[:off[-1]])).max())
+        mb = float(np.abs(oracle.bf16_bits_to_f64(Xb[:off[-1]])).max())
+        tol = oracle.tolerance(ref, np.diff(off).astype(np.float64)[es], ma, mb)
+    else:
+        ref = oracle.wgrad(Gb, Xb, off, E)
+    for i in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        if K > 1024:
+            got = out.view(-1)[idx].double().cpu().numpy()
+            assert (np.abs(got - ref) <= tol).all(), f"replay {i}"
+        else:
+            assert_parity("wgrad", out_to_f64(out), ref, Xb, Wb, Gb, off, f"replay {i}")
+        if det:
+            assert torch.equal(out.view(torch.int32), eager.view(torch.int32)), f"replay {i}"
+    assert gg.cake_gg_check_status(ws, stream.cuda_stream) == gg.CAKE_GG_OK

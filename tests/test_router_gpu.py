@@ -1,7 +1,8 @@
 """GPU parity of the FP32 router GEMM (BF16x3 emulation) against the FP64 oracle.
 
-The dense projection family's router GEMM (flashinfer PR #8438, "Summary":
-"an FP32 router GEMM (256 experts, BF16x3 emulation)"): logits Y = X W^T from
+The dense projection family's router GEMM (flashinfer PR #8438, "Summary": a
+router GEMM over 256 experts in FP32, emulated with three BF16 products):
+logits Y = X W^T from
 FP32 X [T, K] and W [R, K].  Every call goes through the C ABI
 (cake_gg_router_plan / cake_gg_router_fp32).  The GPU result is compared with
 the oracle's emulation (same split, exact products, FP64 sum) under the FP32

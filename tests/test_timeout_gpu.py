@@ -57,3 +57,33 @@ def test_dropped_copy_times_out_and_context_survives(pass_, pair_env, monkeypatc
     f = lambda t: float(np.abs(oracle.bf16_bits_to_f64(t)).max())
     ma, mb = (f(Xb), f(Wb)) if pass_ == "fwd" else (f(Gb), f(Xb))
     assert (np.abs(got - ref) <= oracle.tolerance(ref, L, ma, mb)).all()
+
+
+def test_dropped_copy_in_a_cluster_split_times_out_and_context_survives():
+    """A thin weight gradient (d_out = 48, K = 1024, 4096 rows) runs each output tile as a
+    cluster of eight splits that push their FP32 partial slices into each other's shared memory.
+    Rank 0 of the first cluster loses its first copy: its MMA and epilogue give up, it lets the
+    slices its peers pushed to it land before retiring, and its peers -- which never receive rank
+    0's parts -- give up on their own bounded waits.  The call reports CAKE_GG_ERR_TIMEOUT and
+    the next regular call on the same tensors is correct."""
+    import torch
+    E, M, N, K = 1, 4096, 48, 1024
+    rng = np.random.default_rng(41)
+    Xb = wl.randn_bf16((M, K), 1.0, rng)
+    Gb = wl.randn_bf16((M, N), 1.0, rng)
+    off = wl.offsets_from_sizes([M])
+    X, G = wl.to_torch_bf16(Xb, "cuda"), wl.to_torch_bf16(Gb, "cuda")
+    offs = torch.from_numpy(off).cuda()
+    plan = gg.cake_gg_plan("wgrad", E, M, N, K, "fp32", 1)
+    assert plan.cluster_splits == 8 and plan.swap_ab == 1
+    plan.debug_flags = gg.CAKE_GG_DEBUG_DROP_FIRST_LOAD
+    plan.timeout_ns = 100_000_000  # 0.1 s
+    ws = gg.make_workspace(plan, "cuda")
+    out = torch.zeros((E, N, K), dtype=torch.float32, device="cuda")
+    assert gg.cake_gg_wgrad(plan, G, X, out, offs, "fp32", 1, ws) == gg.CAKE_GG_OK
+    assert gg.cake_gg_check_status(ws) == gg.CAKE_GG_ERR_TIMEOUT
+    good = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1)
+    torch.cuda.synchronize()
+    ref = oracle.wgrad(Gb, Xb, off, E)
+    f = lambda t: float(np.abs(oracle.bf16_bits_to_f64(t)).max())
+    assert (np.abs(good.double().cpu().numpy() - ref) <= oracle.tolerance(ref, M, f(Gb), f(Xb))).all()

@@ -6,7 +6,8 @@ and a stream, or a training loop that must not allocate once it runs).  It
 uses a fixed scratch array inside the library instead of a caller workspace.
 Here its output, on two calls in a row, must match cake_gg_wgrad's output on
 the same inputs within the parity bound the other tests use (and bitwise in
-deterministic mode, where both follow the same fixed summation order).
+deterministic mode, where both follow the same fixed summation order), and
+the FP64 oracle's within that bound.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
@@ -71,6 +72,8 @@ def test_noalloc_matches_workspace_entry_point(sizes, N, K, env, out_dtype, det,
     mb = float(np.abs(oracle.bf16_bits_to_f64(Xb[:off[-1]])).max())
     tol = oracle.tolerance(ref64, L, ma, mb)
     tdt = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+    oracle64 = oracle.wgrad(Gb, Xb, off, E)
+    tol_oracle = oracle.tolerance(oracle64, L, ma, mb)
     for call in range(2):
         dW = torch.full((E, N, K), float("nan"), dtype=tdt, device="cuda")
         rc = gg.cake_gg_wgrad_noalloc(plan, G, X, dW, offs, out_dtype, det)
@@ -78,6 +81,7 @@ def test_noalloc_matches_workspace_entry_point(sizes, N, K, env, out_dtype, det,
         torch.cuda.synchronize()
         got = _f64(dW)
         assert (np.abs(got - ref64) <= tol).all(), f"call {call}: outside the parity bound"
+        assert (np.abs(got - oracle64) <= tol_oracle).all(), f"call {call}: outside the oracle's parity bound"
         if det:
             assert torch.equal(dW.view(torch.int16 if out_dtype == "bf16" else torch.int32),
                                ref.view(torch.int16 if out_dtype == "bf16" else torch.int32)), f"call {call}"
@@ -98,12 +102,30 @@ def test_noalloc_with_a_split_tail_matches_bitwise(out_dtype, det):
     assert plan.tail_splits == 8 and plan.workspace_bytes <= gg.CAKE_GG_NOALLOC_SCRATCH_BYTES
     ref = gg.grouped_gemm("wgrad", G, X, offs, out_dtype=out_dtype, deterministic=det, plan=plan)
     iv = torch.int16 if out_dtype == "bf16" else torch.int32
+    # sampled outputs against the oracle: one element per 128 x 64 block of every expert's dW
+    rng = np.random.default_rng(24)
+    es, ns, ks = [], [], []
+    for e in range(E):
+        for n0 in range(0, N, 128):
+            for k0 in range(0, K, 64):
+                es.append(e)
+                ns.append(n0 + int(rng.integers(0, min(128, N - n0))))
+                ks.append(k0 + int(rng.integers(0, min(64, K - k0))))
+    es, ns, ks = (np.array(v, np.int64) for v in (es, ns, ks))
+    ref_s = oracle.wgrad_at(Gb, Xb, off, E, es, ns, ks)
+    L = np.diff(off).astype(np.float64)[es]
+    ma = float(np.abs(oracle.bf16_bits_to_f64(Gb[:off[-1]])).max())
+    mb = float(np.abs(oracle.bf16_bits_to_f64(Xb[:off[-1]])).max())
+    tol = oracle.tolerance(ref_s, L, ma, mb)
+    idx = torch.from_numpy(es * N * K + ns * K + ks).cuda()
     for call in range(2):
         dW = torch.full_like(ref, float("nan"))
         rc = gg.cake_gg_wgrad_noalloc(plan, G, X, dW, offs, out_dtype, det)
         assert rc == gg.CAKE_GG_OK, gg.cake_gg_strerror(rc)
         torch.cuda.synchronize()
         assert torch.equal(dW.view(iv), ref.view(iv)), f"call {call}"
+        got = _f64(dW.view(-1)[idx])
+        assert (np.abs(got - ref_s) <= tol).all(), f"call {call}: sampled outputs outside the oracle's bound"
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
