@@ -66,6 +66,10 @@ def parse_args():
                     help="pages: time the GB300 rows of the pages' per-row latency table")
     ap.add_argument("--grid-filter", default="", help="only rows whose 'shape op' contains this text")
     ap.add_argument("--grid-reps", type=int, default=7)
+    ap.add_argument("--no-thin", action="store_true",
+                    help="skip the dense projection records (thin 4096->48 passes, mid-size 4096->512 wgrad)")
+    ap.add_argument("--sustained-seconds", type=float, default=1.2,
+                    help="length of the second, longer timing of the step (0 = skip)")
     return ap.parse_args()
 
 
@@ -320,6 +324,35 @@ def run_ours(args, wk):
     value = flop_step * args.steps * ws / (elapsed_ms * 1e-3) / 1e12
     ms_per_step = elapsed_ms / args.steps
 
+    # ---- the same step timed again for >= 1 s (the sustained, power-capped regime) ----
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = max(args.steps, int(math.ceil(args.sustained_seconds * 1e3 / ms_per_step)))
+        sampler2 = ClockSampler(local) if rank == 0 else None
+        time.sleep(0.3 if sampler2 else 0.0)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        if sampler2:
+            sampler2.mark_start()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_sus):
+            for p in passes:
+                run_pass(p)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        if sampler2:
+            sampler2.mark_end()
+        sus_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+        sus_value = flop_step * n_sus * ws / (sus_ms * 1e-3) / 1e12
+        pk = measured_peaks()
+        sustained = {"steps": n_sus, "seconds": round(sus_ms / 1e3, 3), "value": round(sus_value, 2),
+                     "unit": UNIT, "ms_per_step": round(sus_ms / n_sus, 4),
+                     "frac_of_sustained_peak": round(sus_value / ws / pk["bf16_tflops_sustained"], 4),
+                     "peak_source": f"{pk['source']} bf16_tflops_sustained",
+                     "clocks": sampler2.finish() if sampler2 else None}
+
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs in from pinned host memory and all of its
     # outputs back out.  The copies run on their own streams and two device
@@ -472,6 +505,16 @@ def run_ours(args, wk):
             corun["ideal_slowdown"].append(round(n * spin_ms / nsm / elapsed_ms, 4))
             corun["spin_ms"].append(round(spin_ms, 3))
 
+    projection = {}
+    if not args.no_thin and args.workload == "moe_gate_up":
+        # the HBM-bound half of the target (thin projection) and the mid-size
+        # dense weight gradient, each timed in this process on its own inputs
+        if e2e is not None:
+            del ins, outs, houts
+        torch.cuda.empty_cache()
+        projection["thin"] = projection_record(gg, dev, local, rank, 4096, 48, ("wgrad", "fwd", "dgrad"))
+        projection["mid"] = projection_record(gg, dev, local, rank, 4096, 512, ("wgrad",))
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wk, X, W, G, passes, args.cpu_seconds)
@@ -491,12 +534,111 @@ def run_ours(args, wk):
                                               "staging_bufs")} for p in passes}},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             **({"corun": corun} if corun else {}),
-            "gpu_launches": len(passes) * args.steps, "clocks": clocks}
+            "gpu_launches": len(passes) * args.steps, "clocks": clocks,
+            "sustained": sustained, **projection}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def projection_record(gg, dev, local, rank, d_in, d_out, passes, seconds=0.4, per_graph=60, sets=3):
+    """Dense projection (T = 16384, E = 1) passes timed back to back: `per_graph` calls captured
+    once in a CUDA graph (no host launch gaps), rotating over `sets` input sets so that no call
+    finds its operands in L2 from the call before (each set is larger than the L2), replayed for
+    about `seconds` per pass with clocks sampled.  Weight gradient FP32 output, forward and data
+    gradient BF16 output (the dense configuration), deterministic."""
+    import torch
+    from moe_ragged_grouped_gb300 import workloads as wl
+    wk = wl.dense_projection(d_in, d_out)
+    M, E, N, K = wk.M, wk.E, wk.N, wk.K
+    data = [wk.make_torch(seed=s, device=dev) for s in range(sets)]
+    offs = torch.from_numpy(wk.offsets).to(dev)
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(dev)
+    out_rec = {"workload": wk.name, "T": M, "d_in": K, "d_out": N, "deterministic": True, "passes": {}}
+    for p in passes:
+        od = "fp32" if p == "wgrad" else "bf16"
+        plan = gg.cake_gg_plan(p, E, M, N, K, od, 1)
+        wsp = gg.make_workspace(plan, dev)
+        tdt = torch.float32 if od == "fp32" else torch.bfloat16
+        shape = {"fwd": (M, N), "dgrad": (M, K), "wgrad": (E, N, K)}[p]
+        out = torch.empty(shape, dtype=tdt, device=dev)
+        fn = {"fwd": gg.cake_gg_fwd, "dgrad": gg.cake_gg_dgrad, "wgrad": gg.cake_gg_wgrad}[p]
+
+        def launch(i):
+            X, W, G = data[i % sets]
+            a, b = {"fwd": (X, W), "dgrad": (G, W), "wgrad": (G, X)}[p]
+            rc = fn(plan, a, b, out, offs, od, 1, wsp, stream=stream.cuda_stream)
+            if rc != 0:
+                raise gg.CakeGGError(rc, f"{wk.name} {p}")
+
+        with torch.cuda.stream(stream):
+            for i in range(3 * sets):
+                launch(i)
+            torch.cuda.synchronize(dev)
+            st = gg.cake_gg_check_status(wsp, stream.cuda_stream)
+            if st != 0:
+                raise gg.CakeGGError(st, f"{wk.name} {p} device status")
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(per_graph):
+                    launch(i)
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            reps = max(3, int(seconds / max(a.elapsed_time(b) * 1e-3, 1e-6)))
+            sampler = ClockSampler(local) if rank == 0 else None
+            time.sleep(0.3 if sampler else 0.0)
+            torch.cuda.synchronize(dev)
+            if sampler:
+                sampler.mark_start()
+            a.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            if sampler:
+                sampler.mark_end()
+            st = gg.cake_gg_check_status(wsp, stream.cuda_stream)
+            if st != 0:
+                raise gg.CakeGGError(st, f"{wk.name} {p} device status")
+        n = reps * per_graph
+        sec = a.elapsed_time(b) * 1e-3 / n
+        ob = 4 if od == "fp32" else 2
+        alg = wk.algorithmic_bytes(p, ob)
+        flop = wk.flops(1)
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        if flop / alg < ridge:
+            ach, peak = alg / sec / 1e9, peaks["hbm_gbs"]
+            roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "peak_source": f"{peaks['source']} hbm_gbs (copy)"}
+        else:
+            ach, peak = flop / sec / 1e12, peaks["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                    "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
+        roof.update({"frac": round(ach / peak, 4), "traffic": traffic_for(wk.name, p, od, 1),
+                     "algorithmic_bytes": int(alg), "flop": int(flop)})
+        out_rec["passes"][p] = {
+            "out_dtype": od, "us_per_launch": round(sec * 1e6, 3), "launches": n,
+            "tflops": round(flop / sec / 1e12, 1), "gbs": round(alg / sec / 1e9, 1),
+            "plan": {k: v for k, v in plan.as_dict().items()
+                     if k in ("tile_n", "tile_k", "stages", "pair", "swap_ab", "split_chunk", "cluster_splits",
+                              "tail_units", "tail_splits", "staging_bufs")},
+            "roofline": roof, "clocks": sampler.finish() if sampler else None}
+        del wsp, out, graph
+    out_rec["launch"] = (f"CUDA graph of {per_graph} back-to-back calls, replayed; {sets} input sets "
+                         f"rotated ({sets * wk.M * wk.K * 2 / 1e6:.0f} MB of X) so no call's operands "
+                         "are in L2 from the call before")
+    del data
+    torch.cuda.empty_cache()
+    return out_rec
 
 
 def sizes_desc(wk):
@@ -628,10 +770,17 @@ def run_reference(args, wk):
 
 
 def run_pages_grid(args):
-    """One call per repetition, L2 flushed before it, CUDA events around it."""
+    """One call per repetition, L2 flushed before it, CUDA events around it.
+
+    "dW" is one cake_gg_wgrad call.  "ckpt" and "ckpt ES" go through the autograd API:
+    checkpointed_grouped_linear (grouped_linear in a non-reentrant torch checkpoint, early stop
+    off / on) forward, then backward with the upstream gradient G.  Before the start event a GPU
+    sleep of a few milliseconds is queued so that the host's enqueueing (autograd and checkpoint
+    bookkeeping) runs while the GPU sleeps: the events then bracket the device work alone."""
     import torch
     from moe_ragged_grouped_gb300 import cake_gg as gg
     from moe_ragged_grouped_gb300 import workloads as wl
+    from moe_ragged_grouped_gb300.autograd import checkpointed_grouped_linear
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     gg.load_library()
@@ -660,12 +809,19 @@ def run_pages_grid(args):
         wss = {p: gg.make_workspace(plans[p], dev) for p in plans}
         ops = {"fwd": (gg.cake_gg_fwd, X, W), "dgrad": (gg.cake_gg_dgrad, G, W), "wgrad": (gg.cake_gg_wgrad, G, X)}
 
+        Xl, Wl = X.detach().requires_grad_(), W.detach().requires_grad_()
+
         def call():
-            for p in passes:
-                fn, a, b = ops[p]
-                rc = fn(plans[p], a, b, outs[p], offs, od, 1, wss[p], stream=stream.cuda_stream)
-                if rc != 0:
-                    raise gg.CakeGGError(rc, p)
+            if op == "dW":
+                for p in passes:
+                    fn, a, b = ops[p]
+                    rc = fn(plans[p], a, b, outs[p], offs, od, 1, wss[p], stream=stream.cuda_stream)
+                    if rc != 0:
+                        raise gg.CakeGGError(rc, p)
+            else:
+                Xl.grad = Wl.grad = None
+                Y = checkpointed_grouped_linear(Xl, Wl, offs, early_stop=(op == "ckpt ES"))
+                Y.backward(G)
 
         for _ in range(2):
             call()
@@ -677,6 +833,7 @@ def run_pages_grid(args):
         times = []
         for _ in range(args.grid_reps):
             flush.zero_()
+            torch.cuda._sleep(6_000_000)   # ~3 ms at 2 GHz: the host enqueues meanwhile
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             call()
@@ -685,6 +842,7 @@ def run_pages_grid(args):
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
         line = {"grid": "pages_gb300", "shape": shape, "op": op, "out_dtype": od, "deterministic": True,
+                "path": "cake_gg_wgrad" if op == "dW" else "checkpointed_grouped_linear (autograd)",
                 "ms": round(ms, 4), "tflops": round(wk.flops(len(passes)) / (ms * 1e-3) / 1e12, 1),
                 "ms_min_max": [round(min(times), 4), round(max(times), 4)],
                 "pages_det_ms": det_ms, "vs_pages_det": round(det_ms / ms, 4),
@@ -693,7 +851,7 @@ def run_pages_grid(args):
         print(json.dumps(line), flush=True)
         for k in ("det", "nondet", "sota"):
             ratios.setdefault((op, k), []).append(line[f"vs_pages_{k}"])
-        del outs, wss
+        del outs, wss, Xl, Wl
     summary = {"grid": "pages_gb300", "summary": "geomean of (pages' latency / ours) per operation", "rows": len(rows)}
     for (op, k), v in sorted(ratios.items()):
         summary[f"{op} vs {k}"] = round(math.exp(sum(math.log(x) for x in v) / len(v)), 4)

@@ -8,6 +8,17 @@ MoE expert layer (flashinfer PR #8258, opening summary).  Under
 ``torch.utils.checkpoint`` the forward runs again before the backward: the
 pages' "ckpt" operation (forward + backward with the forward recomputed).
 
+    Y = checkpointed_grouped_linear(X, W, offsets, early_stop=True)
+
+is the pages' pair of checkpointed operations (PR #8258, "Operations and
+shapes": one grouped GEMM in a non-reentrant checkpoint, early stop off =
+"ckpt", on = "ckpt ES").  The backward needs only the layer's inputs, which
+the recompute saves again before anything else; with early stop on, the
+checkpoint stops the recompute as soon as those are saved, so the recomputed
+forward's output is never read and its GEMM is not launched (the pages credit
+their earlier PR #8114 with skipping that recompute).  With early stop off
+the recompute runs the forward GEMM, as stock checkpointing does.
+
 This module only marshals arguments: every pass runs in libcake_gg.so.  Plans
 and workspaces are cached per (pass, shape, dtype, mode, device, stream) and
 reused across calls, as the workspace contract allows (zero-filled once,
@@ -16,9 +27,14 @@ Rows at or past offsets[E] of Y and dX are left unwritten (uninitialised).
 """
 from __future__ import annotations
 
+import contextlib
+import threading
+
 from . import cake_gg as gg
 
 _cache: dict = {}
+# set while a checkpointed_grouped_linear with early stop recomputes its forward
+_recompute = threading.local()
 
 
 def _plan_ws(pass_, E, M, N, K, out_dtype, det, device, stream):
@@ -62,6 +78,10 @@ def _make_function():
                 raise ValueError("shapes: X [M, K], W [E, N, K], offsets [E+1]")
             ctx.save_for_backward(X, W, offsets)
             ctx.det, ctx.wgrad_dtype = bool(deterministic), wgrad_dtype
+            if getattr(_recompute, "skip_forward", False):
+                # an early-stopped recompute: only the saved inputs are kept, the
+                # output is discarded unread, so the GEMM is not launched
+                return torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
             return _run("fwd", X, W, offsets, (M, N), "bf16", ctx.det, E, M, N, K)
 
         @staticmethod
@@ -97,3 +117,35 @@ def grouped_linear(X, W, offsets, deterministic=True, wgrad_dtype="bf16"):
     if _fn is None:
         _fn = _make_function()
     return _fn.apply(X, W, offsets, deterministic, wgrad_dtype)
+
+
+@contextlib.contextmanager
+def _recompute_without_forward():
+    prev = getattr(_recompute, "skip_forward", False)
+    _recompute.skip_forward = True
+    try:
+        yield
+    finally:
+        _recompute.skip_forward = prev
+
+
+def checkpointed_grouped_linear(X, W, offsets, early_stop=True, deterministic=True, wgrad_dtype="bf16"):
+    """grouped_linear inside a non-reentrant ``torch.utils.checkpoint``.
+
+    ``early_stop`` False: the pages' "ckpt" -- forward, then in the backward the
+    forward recomputed, the data gradient and the weight gradient (2 x fwd + bwd).
+    ``early_stop`` True: "ckpt ES" -- the checkpoint stops its recompute once the
+    layer's inputs are saved again, which happens before the forward GEMM would
+    run, so the backward launches only the data and weight gradients.  Results
+    are bitwise those of the plain grouped_linear in deterministic mode.
+    """
+    import torch
+    from torch.utils.checkpoint import checkpoint, set_checkpoint_early_stop
+
+    def contexts():
+        return contextlib.nullcontext(), (_recompute_without_forward() if early_stop
+                                          else contextlib.nullcontext())
+
+    with set_checkpoint_early_stop(bool(early_stop)):
+        return checkpoint(grouped_linear, X, W, offsets, deterministic, wgrad_dtype,
+                          use_reentrant=False, context_fn=contexts)
