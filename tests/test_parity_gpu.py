@@ -327,8 +327,9 @@ def test_dynamic_and_static_unit_order_agree_bitwise(sizes, N, K, max_sms, monke
 
 
 def test_scheduler_words_return_to_zero():
-    """The unit counter and the retired-CTA counter in the workspace header are zero after every
-    call, so the workspace needs no clearing between calls."""
+    """The status word, the unit counter and the retired-CTA counter in the workspace header are
+    zero after every call, so the workspace needs no clearing between calls; the ticket tag
+    (header word 32, byte 128) advances by one per call."""
     import torch
     Xb, Wb, Gb, off = make_inputs([700, 0, 1300], 256, 512, seed=22)
     X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
@@ -336,11 +337,13 @@ def test_scheduler_words_return_to_zero():
     plans = [gg.cake_gg_plan("wgrad", E, M, 256, 512, od, 1, cap) for od in ("bf16", "fp32") for cap in (0, 4)]
     ws = torch.zeros(max(int(pl.workspace_bytes) for pl in plans), dtype=torch.uint8, device="cuda")
     offs = torch.from_numpy(off).cuda()
-    for cap in (0, 4, 0):
+    for i, cap in enumerate((0, 4, 0)):
         plan = gg.cake_gg_plan("wgrad", E, M, 256, 512, "bf16", 1, cap)
         gg.grouped_gemm("wgrad", G, X, offs, out_dtype="bf16", plan=plan, workspace=ws)
         torch.cuda.synchronize()
-        head = ws[:256].view(torch.int32).cpu().numpy()
+        head = ws[:256].view(torch.int32).cpu().numpy().copy()
+        assert head[32] == i + 1, head[32]
+        head[32] = 0
         assert (head == 0).all(), head.nonzero()
     ref = reference("wgrad", Xb, Wb, Gb, off)
     out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", plan=gg.cake_gg_plan("wgrad", E, M, 256, 512, "fp32", 1),
