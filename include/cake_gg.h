@@ -57,7 +57,10 @@
  *     2: wherever they fit), CAKE_GG_WIDE_FD=1 (512-wide forward / data-
  *     gradient tiles), CAKE_GG_SPLIT_CHUNK (k-blocks per split, 0 = no split),
  *     CAKE_GG_CSPLIT (0, or 2..8 cluster splits), CAKE_GG_TAIL=0 (no split
- *     tail), CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2);
+ *     tail), CAKE_GG_STREAMK (0: never, the default; 1: by the cost rule;
+ *     2: wherever the walk applies), CAKE_GG_STREAMK_KB (its segment length
+ *     in k-blocks),
+ *     CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2);
  *   read by each compute call, changing no result:
  *     CAKE_GG_PDL=0 (no programmatic dependent launch), CAKE_GG_DYN=0 (static
  *     unit order), CAKE_GG_SPIN_NS (an early split's poll for its tile's
@@ -134,7 +137,10 @@ typedef struct cake_gg_plan {
     int32_t tail_units;      /* weight gradient: the last tail_units units of the walk */
     int32_t tail_splits;     /* are each split into tail_splits pieces whose FP32
                                 partials are summed in split order (0 = no tail split) */
-    int32_t reserved[4];
+    int32_t streamk_kblocks; /* weight gradient of one expert: > 0 = stream-K walk, the
+                                work cut into segments of this many k-blocks that cross
+                                tile boundaries; a tile's pieces are summed in k order */
+    int32_t reserved[3];
 } cake_gg_plan_t;
 
 /* Debug flag (tests only): the CTA that takes the walk's first unit (its even

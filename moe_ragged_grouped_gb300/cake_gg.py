@@ -67,7 +67,8 @@ class CakeGGPlan(ctypes.Structure):
         ("cluster_splits", ctypes.c_int32),
         ("tail_units", ctypes.c_int32),
         ("tail_splits", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("streamk_kblocks", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
     def as_dict(self):

@@ -59,13 +59,19 @@ int env_int(const char *name, int dflt)
 // (expressed in k-block equivalents) -- returned as k-blocks per split
 // (0 = no split).  A pure function of the problem: never of the CTA count
 // a launch uses, so deterministic results do not depend on max_sms.
+// Cost of splitting a tile's reduction, in k-block equivalents: the FP32
+// partial tile's write and read (x2 margin) and the finish.
+double split_overhead_kb(int bn, int bk)
+{
+    const double kps = bk / 64.0;
+    const double partial_kb = 2.0 * 2.0 * 1024.0 * bn / ((16384.0 + 128.0 * bn) * kps);
+    return partial_kb + 4.0 / kps;
+}
+
 int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn, int bk, int64_t tail_s)
 {
     if (out_tiles <= 0 || kblocks_per_expert < 2 * kMinSplitChunk) return 0;
-    const double kps = bk / 64.0;
-    // partial-tile write + read (x2 margin) and the finish, in stage equivalents
-    const double partial_kb = 2.0 * 2.0 * 1024.0 * bn / ((16384.0 + 128.0 * bn) * kps);
-    const double c_split = partial_kb + 4.0 / kps;
+    const double c_split = split_overhead_kb(bn, bk);
     auto cost = [&](int64_t S) {
         const int64_t units = out_tiles * S;
         if (S == 1 && tail_s > 1) {
@@ -123,6 +129,42 @@ void choose_tail(int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn, int
     }
 }
 
+// Stream-K walk of a one-expert weight gradient whose pair tiles fill less
+// than two waves of the fixed 76-pair (152-CTA) wave: the n_tiles x KB
+// k-blocks of every m-unit are cut into V = 76 / m_units segments of equal
+// length L (the m-units of a segment run side by side, reading the same rows
+// of the wide operand), so every pair does about the same k-blocks where
+// whole or split tiles leave some pairs idle.  Returns L, or 0 when the
+// unit-wave model (the current split or split tail, or none) is as fast.
+int32_t choose_streamk(int32_t N, int32_t K, int64_t M_max, int32_t bn, int32_t bk, int32_t split_chunk,
+                       int32_t tail_units, int32_t tail_splits, int env)
+{
+    if (env == 0) return 0;
+    const Geom g = make_geom(kModeWgrad, 1, N, K, M_max, bn, 0, 0, 2, bk);
+    const int64_t mu = m_units_w(g);
+    const int64_t U = mu * g.n_tiles;
+    const int64_t P = kWaveCtas / 2;
+    const int64_t KB = (M_max + bk - 1) / bk;
+    if (mu > 4 || KB < 1 || ((KB < 16 || U >= 2 * P) && env != 2)) return 0;
+    const int64_t V = P / mu;
+    const int64_t W = g.n_tiles * KB;
+    if (W > (int64_t(1) << 30)) return 0;
+    const int64_t L = (W + V - 1) / V;
+    const double c_split = split_overhead_kb(bn, bk);
+    const double cost_sk = double(L) + ((L % KB != 0 || W % L != 0) ? c_split : 0.0);
+    double cost_cur;
+    if (split_chunk > 0) {
+        const int64_t S = (KB + split_chunk - 1) / split_chunk;
+        cost_cur = double((U * S + P - 1) / P) * (double(split_chunk) + c_split);
+    } else if (tail_splits > 1 && tail_units > 0) {
+        cost_cur = double(U / P) * double(KB) + double(KB) / tail_splits + c_split;
+    } else {
+        cost_cur = double((U + P - 1) / P) * double(KB);
+    }
+    if (env == 2 || cost_sk < 0.95 * cost_cur) return int32_t(L);
+    return 0;
+}
+
 int tmem_cols_for(int bn)
 {
     if (bn > 256) return 512;  // one 512-column accumulator
@@ -153,11 +195,27 @@ WsLayout ws_layout(const cake_gg_plan_t &pl)
     w.zero_bytes = kHeaderBytes;
     w.total = kHeaderBytes;
     const bool tail = pl.pass == CAKE_GG_WGRAD && pl.tail_splits > 1 && pl.tail_units > 0;
-    if (pl.pass != CAKE_GG_WGRAD || (pl.split_chunk <= 0 && !tail) || pl.cluster_splits > 0) return w;
+    const bool sk = pl.pass == CAKE_GG_WGRAD && pl.streamk_kblocks > 0;
+    if (pl.pass != CAKE_GG_WGRAD || (pl.split_chunk <= 0 && !tail && !sk) || pl.cluster_splits > 0) return w;
     const Geom g = make_geom(kModeWgrad, pl.E, pl.N, pl.K, pl.M_max, pl.tile_n, pl.swap_ab, pl.split_chunk, pl.pair,
                              pl.tile_k);
     const uint64_t tpe = uint64_t(g.m_tiles_w) * uint64_t(g.n_tiles);
     uint64_t n_tickets = 0, tile_bytes = 0, tmp = 0;
+    if (sk) {
+        // tickets for every output tile; FP32 partial slots per (tile, piece)
+        w.ok &= mul_ok(tpe, uint64_t(pl.E), &n_tickets);
+        w.ok &= mul_ok(uint64_t(kTileM) * 4u, uint64_t(pl.tile_n), &tile_bytes);
+        w.ok &= mul_ok(n_tickets, 8, &tmp);
+        w.tickets_bytes = align_up(tmp, 256);
+        w.partials_off = w.tickets_off + w.tickets_bytes;
+        const int64_t kb_max = (pl.M_max + pl.tile_k - 1) / pl.tile_k;
+        uint64_t slots = 0;
+        w.ok &= mul_ok(n_tickets, uint64_t(sk_slots_per_tile(int32_t(kb_max), pl.streamk_kblocks)), &slots);
+        w.ok &= mul_ok(slots, tile_bytes, &w.partials_bytes);
+        w.ok &= add_ok(w.partials_off, w.partials_bytes, &w.total);
+        w.zero_bytes = kHeaderBytes;
+        return w;
+    }
     if (tail) {
         // tickets for every output tile; FP32 partial slots per (tail unit, pair
         // rank, piece), written before they are read
@@ -316,6 +374,12 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         plan->tail_units < 0 || plan->tail_splits < 0 || plan->tail_splits == 1 || plan->tail_splits > kMaxTailSplits ||
         (plan->tail_splits > 1 && (pass != CAKE_GG_WGRAD || plan->swap_ab || plan->split_chunk > 0 ||
                                    plan->cluster_splits > 0)) ||
+        plan->streamk_kblocks < 0 ||
+        (plan->streamk_kblocks > 0 &&
+         (pass != CAKE_GG_WGRAD || plan->E != 1 || plan->swap_ab || plan->split_chunk > 0 || plan->tail_splits > 1 ||
+          plan->cluster_splits > 0 || plan->tile_n > 256 ||
+          int64_t((plan->K + plan->tile_n - 1) / plan->tile_n) * ((plan->M_max + plan->tile_k - 1) / plan->tile_k) >
+              (int64_t(1) << 30))) ||
         smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits,
                        plan->pair, plan->E) > kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
@@ -476,10 +540,12 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     // skewed experts balance, and when other work holds some SMs the CTAs that
     // run take the whole walk instead of waiting for their late peers' shares
     // (the cluster split keeps its static one-unit-per-cluster walk)
-    p.dyn = plan->cluster_splits == 0 && env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
+    p.sk = mode == kModeWgrad ? plan->streamk_kblocks : 0;
+    // (a stream-K walk passes its pieces to every role through the unit queue)
+    p.dyn = plan->cluster_splits == 0 && (env_int("CAKE_GG_DYN", 1) != 0 || p.sk > 0) ? 1 : 0;
     p.sched = reinterpret_cast<int32_t *>(wsb + kSchedOffset);
-    // tickets are in use (split tiles or a split tail): tag them per call
-    p.retire = p.dyn || ((mode == kModeWgrad) && (p.kchunk > 0 || plan->tail_splits > 1)) ? 1 : 0;
+    // tickets are in use (split tiles, a split tail, stream-K pieces): tag them per call
+    p.retire = p.dyn || ((mode == kModeWgrad) && (p.kchunk > 0 || plan->tail_splits > 1 || p.sk > 0)) ? 1 : 0;
     p.tail = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_units : 0;
     p.tail_s = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_splits : 0;
     if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
@@ -488,9 +554,12 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
     const int P = plan->pair;
     const int CL = p.csplit > 0 ? p.csplit : P;   // CTAs per cluster (one unit per cluster)
-    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk, p.csplit);
+    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk, p.csplit, 0, 0, p.sk);
     uint64_t unit_bound;
-    if (mode == kModeWgrad) {
+    if (mode == kModeWgrad && p.sk > 0) {
+        // virtual pairs of the walk at M_max rows (the most there can be)
+        unit_bound = uint64_t(sk_virtual(g, sk_kb(g, int32_t(plan->M_max))));
+    } else if (mode == kModeWgrad) {
         uint64_t splits = uint64_t(E);
         if (p.kchunk > 0) splits = M / (uint64_t(bk) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
         unit_bound = uint64_t(m_units_w(g)) * uint64_t(g.n_tiles) * splits +
@@ -775,6 +844,20 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->split_chunk == 0 && plan->cluster_splits == 0 &&
         env_int("CAKE_GG_TAIL", 1) != 0)
         choose_tail(E, N, K, M_max, bn, bk, plan->pair, &plan->tail_units, &plan->tail_splits);
+    // stream-K walk of a one-expert weight gradient (see choose_streamk); it
+    // replaces a split or a split tail
+    if (pass == CAKE_GG_WGRAD && E == 1 && !plan->swap_ab && plan->pair == 2 && bn <= 256 &&
+        plan->cluster_splits == 0) {
+        int32_t L = choose_streamk(N, K, M_max, bn, bk, plan->split_chunk, plan->tail_units,
+                                   plan->tail_splits, env_int("CAKE_GG_STREAMK", 0));
+        const int env_l = env_int("CAKE_GG_STREAMK_KB", 0);
+        if (env_l > 0) L = env_l;
+        if (L > 0) {
+            plan->streamk_kblocks = L;
+            plan->split_chunk = 0;
+            plan->tail_units = plan->tail_splits = 0;
+        }
+    }
     const int csp = plan->cluster_splits;
     int stages = kMaxStages;
     const int pr = plan->pair;
@@ -891,7 +974,7 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
     Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
                              mode == kModeWgrad ? plan->split_chunk : 0, plan->pair, plan->tile_k,
                              mode == kModeWgrad ? plan->cluster_splits : 0, tail ? plan->tail_units : 0,
-                             tail ? plan->tail_splits : 0);
+                             tail ? plan->tail_splits : 0, mode == kModeWgrad ? plan->streamk_kblocks : 0);
     std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
     for (int e = 0; e < E; ++e) {
         cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
@@ -908,9 +991,20 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
     }
     std::vector<int32_t> off_v(off, off + E + 1);
     if (g.tail > 0 && !tail_active(g, off_v.data(), order.data())) g.tail = g.tail_s = 0;
-    const int64_t units = walk_length(g, pref[E]);
+    int64_t units = walk_length(g, pref[E]);
+    // stream-K: unit ids v * pmax + piece over the virtual pairs (ids a segment
+    // does not use are skipped)
+    std::vector<int64_t> sk_ids;
+    if (g.sk > 0) {
+        const int32_t KB = sk_kb(g, off[1] - off[0]);
+        const int32_t pm = sk_pmax(g, KB);
+        for (int32_t v = 0; v < sk_virtual(g, KB); ++v)
+            for (int32_t pc = 0; pc < sk_pieces(g, KB, v); ++pc) sk_ids.push_back(int64_t(v) * pm + pc);
+        units = int64_t(sk_ids.size());
+    }
     int64_t n = 0;
-    for (int64_t t = 0; t < units; ++t) {
+    for (int64_t tt = 0; tt < units; ++tt) {
+        const int64_t t = g.sk > 0 ? sk_ids[size_t(tt)] : tt;
         const int ranks = g.csplit > 0 ? g.csplit : g.pair;
         for (int r = 0; r < ranks; ++r) {
             const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data(), r);

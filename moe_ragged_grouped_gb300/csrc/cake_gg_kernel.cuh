@@ -80,6 +80,7 @@ struct KParams {
     int32_t dyn;            // units fetched from a global counter (else a static stride)
     int32_t tail;           // weight gradient: split tail units ...
     int32_t tail_s;         // ... and pieces per tail unit (0 = none)
+    int32_t sk;             // weight gradient of one expert: stream-K segment length in k-blocks (0 = off)
     int32_t *sched;         // [0]: next unit, [32]: CTAs retired (zero between calls)
     uint64_t timeout_ns;
 };
@@ -523,7 +524,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     // instantiations compile none of that path)
     const int csplit = MODE == kModeWgrad && SWAP ? p.csplit : 0;
     Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit,
-                       MODE == kModeWgrad ? p.tail : 0, MODE == kModeWgrad ? p.tail_s : 0);
+                       MODE == kModeWgrad ? p.tail : 0, MODE == kModeWgrad ? p.tail_s : 0,
+                       MODE == kModeWgrad && !SWAP ? p.sk : 0);
     // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + r
     // as one 256-row MMA (the even CTA issues it; each CTA holds its A rows and
     // half of the B tile); a cluster split (csplit CTAs) computes one tile,
@@ -738,7 +740,16 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             bool ok = true;
             UnitSeq us{0, 0};
             int32_t nxt = 0;
-            if (p.dyn && leader) nxt = atomicAdd(p.sched, 1);
+            // stream-K: the leader walks its own virtual pairs (unit0, unit0 + unit_step, ...)
+            // and their pieces in order; no counter
+            const bool skw = MODE == kModeWgrad && g.sk > 0;
+            int32_t sk_K = 0, sk_pm = 1, sk_nv = 0, sk_v = int32_t(unit0), sk_pc = 0;
+            if (skw) {
+                sk_K = sk_kb(g, t_off[1] - t_off[0]);
+                sk_pm = sk_pmax(g, sk_K);
+                sk_nv = sk_virtual(g, sk_K);
+            }
+            if (p.dyn && leader && !skw) nxt = atomicAdd(p.sched, 1);
             while (ok) {
                 int64_t t;
                 if (!p.dyn) {
@@ -754,7 +765,19 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         ok = false;
                         break;
                     }
-                    t = int64_t(nxt) < total ? int64_t(nxt) : -1;
+                    if (skw) {
+                        t = -1;
+                        while (sk_v < sk_nv) {
+                            if (sk_pc < sk_pieces(g, sk_K, sk_v)) {
+                                t = int64_t(sk_v) * sk_pm + sk_pc++;
+                                break;
+                            }
+                            sk_v += int32_t(unit_step);
+                            sk_pc = 0;
+                        }
+                    } else {
+                        t = int64_t(nxt) < total ? int64_t(nxt) : -1;
+                    }
                     c->uq[slot] = t;
                     mbar_arrive(smem_u32(&c->uq_full[slot]));
                     // the odd CTA's slot: data and signal in one asynchronous store
@@ -787,7 +810,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 // has taken its first unit (fetching at once would let the first
                 // pairs to start hold two units while late ones find none)
                 const int32_t fetch_kb = ti.kb1 - (p.stages + 1) > ti.kb0 ? ti.kb1 - (p.stages + 1) : ti.kb0;
-                bool fetched = !(p.dyn && leader);
+                bool fetched = !(p.dyn && leader) || skw;
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                     if (!fetched && kb == fetch_kb) {
                         nxt = atomicAdd(p.sched, 1);  // in flight while the copies go out
@@ -1067,7 +1090,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             const bool row_ok = lrow < rows_valid;
             // cluster split: this CTA's float4 columns [q0, q1) of the tile's nq
             const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
-            const int per = csplit > 0 ? (nq + csplit - 1) / csplit : 0;
+            const int per_c = csplit > 0 ? (nq + csplit - 1) / csplit : 1;
+            const int per = per_c > 0 ? per_c : 1;   // (>= 1: also keeps pruned code free of a zero divisor)
             const int q0 = rank * per;
             const int q1 = q0 + per < nq ? q0 + per : nq;
             if (csplit > 0) {

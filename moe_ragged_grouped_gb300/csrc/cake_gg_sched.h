@@ -65,15 +65,17 @@ struct Geom {
     int32_t csplit;       // weight gradient: splits of a tile run by one cluster (0 = off)
     int32_t tail;         // weight gradient: the last `tail` units of the walk are split ...
     int32_t tail_s;       // ... into tail_s pieces each (0 = no tail split)
+    int32_t sk;           // weight gradient, one expert: stream-K segment length in k-blocks (0 = off)
 };
 
 CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
                        int32_t swap, int32_t kchunk, int32_t pair = 1, int32_t bk = kTileK,
-                       int32_t csplit = 0, int32_t tail = 0, int32_t tail_s = 0)
+                       int32_t csplit = 0, int32_t tail = 0, int32_t tail_s = 0, int32_t sk = 0)
 {
     Geom g;
+    g.sk = mode == kModeWgrad ? sk : 0;
     g.tail = tail_s > 1 ? tail : 0;
     g.tail_s = tail_s > 1 ? tail_s : 0;
     g.pair = pair;
@@ -135,6 +137,51 @@ CAKE_HD int32_t expert_cost(const Geom &g, int32_t rows)
 }
 
 CAKE_HD bool walk_is_sorted(const Geom &g) { return g.mode == kModeWgrad && g.E <= kSortMaxE; }
+
+// ---- stream-K walk (weight gradient of one expert) ----
+//
+// The work is n_tiles x KB k-blocks per m-unit (KB = the expert's k-blocks).
+// It is cut into segments of sk consecutive k-blocks in (n-tile, k-block)
+// order; segment j is processed by m_units virtual pairs at once, one per
+// m-unit (v = j * m_units + mu), so the m-units of an n-tile read the same
+// rows of the wide operand at the same time.  A segment covers the end of
+// one n-tile and the start of the next (or more): each such piece is its own
+// unit, and a tile's pieces are summed in k order through partial slots.  A
+// unit id is v * pmax + piece.  The walk depends on the plan and the offsets
+// only, never on which pair runs a virtual pair.
+
+// k-blocks of the expert (at least 1, so an empty expert still writes its zero tiles)
+CAKE_HD int32_t sk_kb(const Geom &g, int32_t rows)
+{
+    const int32_t kb = ceil_div_i(rows, g.bk);
+    return kb > 0 ? kb : 1;
+}
+
+// Largest number of pieces of one segment.
+CAKE_HD int32_t sk_pmax(const Geom &g, int32_t KB) { return ceil_div_i(g.sk, KB) + 1; }
+
+// Segments (each run by m_units virtual pairs).
+CAKE_HD int32_t sk_segments(const Geom &g, int32_t KB) { return ceil_div_i(g.n_tiles * KB, g.sk); }
+
+// Virtual pairs of the walk.
+CAKE_HD int32_t sk_virtual(const Geom &g, int32_t KB)
+{
+    return ceil_div_i(g.m_tiles_w, g.pair) * sk_segments(g, KB);
+}
+
+// Pieces of virtual pair v's segment.
+CAKE_HD int32_t sk_pieces(const Geom &g, int32_t KB, int32_t v)
+{
+    const int32_t j = v / ceil_div_i(g.m_tiles_w, g.pair);
+    const int32_t a = j * g.sk;
+    const int32_t w = g.n_tiles * KB;
+    const int32_t b = a + g.sk < w ? a + g.sk : w;
+    return (b - 1) / KB - a / KB + 1;
+}
+
+// Partial slots reserved per output tile: the most pieces a tile of at most
+// KB_max k-blocks can have.
+CAKE_HD int32_t sk_slots_per_tile(int32_t KB_max, int32_t sk) { return (KB_max > 0 ? KB_max - 1 : 0) / sk + 2; }
 
 // One unit of work.
 struct Tile {
@@ -223,6 +270,33 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
         ti.ticket = (e * g.m_tiles_w + ti.mt) * g.n_tiles + ti.nt;
         ti.slot = 0;
         ti.valid = ti.mt < g.m_tiles_w;
+    } else if (g.mode == kModeWgrad && g.sk > 0) {
+        // stream-K piece: unit id = v * pmax + piece (see sk_kb)
+        const int32_t KB = sk_kb(g, r1 - r0);
+        const int32_t pmax = sk_pmax(g, KB);
+        const int32_t mu_n = ceil_div_i(g.m_tiles_w, g.pair);
+        const int32_t v = int32_t(t / pmax);
+        const int32_t pc = int32_t(t - int64_t(v) * pmax);
+        const int32_t mu = v % mu_n;
+        const int32_t j = v / mu_n;
+        const int32_t a = j * g.sk;
+        const int32_t w = g.n_tiles * KB;
+        const int32_t b = a + g.sk < w ? a + g.sk : w;
+        const int32_t nt = a / KB + pc;
+        const int32_t base = nt * KB;
+        ti.nt = nt;
+        ti.mt = mu * g.pair + rank;
+        ti.kb0 = (a > base ? a : base) - base;
+        ti.kb1 = (b < base + KB ? b : base + KB) - base;
+        // cuts (multiples of sk) inside the tile before this piece, and in all of it
+        ti.s = (base + ti.kb0) / g.sk - base / g.sk;
+        ti.S = ceil_div_i(base + KB, g.sk) - base / g.sk;
+        ti.row0 = r0;
+        ti.ticket = (e * g.m_tiles_w + ti.mt) * g.n_tiles + ti.nt;
+        const int32_t spt = sk_slots_per_tile(int32_t((g.M_max + g.bk - 1) / g.bk), g.sk);
+        ti.slot = int64_t(ti.ticket) * spt + ti.s;
+        ti.valid = ti.mt < g.m_tiles_w;
+        ti.tail = true;   // partials in slots, summed in piece order in both modes
     } else if (g.mode == kModeWgrad) {
         const int32_t S = expert_splits(g, r1 - r0);
         const int32_t nkb_e = ceil_div_i(r1 - r0, g.bk);

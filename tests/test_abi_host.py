@@ -230,6 +230,57 @@ def test_tile_walk_split_tail():
     assert not [t for t in tiles if t[4] > 1]
 
 
+@pytest.mark.parametrize("sizes,N,K,force", [([16384], 512, 4096, False), ([16384], 1024, 5120, False),
+                                             ([16300], 512, 4096, False), ([1000], 512, 1024, True),
+                                             ([300], 384, 2048, True)])
+def test_tile_walk_streamk(sizes, N, K, force):
+    """Stream-K walk of a one-expert weight gradient: every output tile is covered once by pieces
+    that partition its k-blocks in order; every virtual pair does at most L k-blocks; the m-units
+    of a segment get the same (n-tile, k-range) pieces (they read the same operand rows)."""
+    env = {"CAKE_GG_STREAMK": "2" if force else "1"}
+    plan, tiles = _check_walk_coverage("wgrad", sizes, N=N, K=K, env=env)
+    L = plan.streamk_kblocks
+    assert L > 0 and plan.split_chunk == 0 and plan.tail_splits == 0
+    KB = -(-sizes[0] // plan.tile_k)
+    n_tiles = -(-K // plan.tile_n)
+    m_units = -(-(-(-N // 128)) // 2)
+    # each m-unit's pieces (its even CTA's tiles) as linear k-block ranges of [0, n_tiles * KB)
+    per_v = {}
+    for e, mt, nt, s, S, kb0, kb1, _ in tiles:
+        if mt % 2 == 0:
+            per_v.setdefault(mt // 2, []).append((nt * KB + kb0, nt * KB + kb1))
+    assert len(per_v) == m_units
+    # the linear k-block ranges of each m-unit tile the work [0, n_tiles * KB) and cut it every L
+    for mu, ranges in per_v.items():
+        ranges.sort()
+        assert ranges[0][0] == 0 and ranges[-1][1] == n_tiles * KB
+        for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+            assert a1 == b0
+        cuts = sorted({r[0] for r in ranges} | {n_tiles * KB})
+        for c in cuts:
+            assert c % L == 0 or c % KB == 0
+        # a segment's pieces sum to L k-blocks (the last one to the remainder)
+        seg = {}
+        for a0, a1 in ranges:
+            seg[a0 // L] = seg.get(a0 // L, 0) + (a1 - a0)
+        assert max(seg.values()) <= L
+    assert len({tuple(sorted(r)) for r in per_v.values()}) == 1   # the m-units run the same pieces
+
+
+def test_tile_walk_streamk_empty_expert_writes_zero_tiles():
+    """No rows at run time (the plan was made for more): every tile is one piece of one k-block
+    whose rows all lie past the expert's end (zeroed), so dW is written as exact zeros."""
+    os.environ["CAKE_GG_STREAMK"] = "2"
+    try:
+        plan = gg.cake_gg_plan("wgrad", 1, 4096, 512, 1024, "fp32", 1)
+    finally:
+        del os.environ["CAKE_GG_STREAMK"]
+    assert plan.streamk_kblocks > 0
+    tiles = gg.cake_gg_tile_walk(plan, np.array([0, 0], np.int32))
+    assert {(t[1], t[2]) for t in tiles} == {(m, n) for m in range(4) for n in range(1024 // plan.tile_n)}
+    assert all(t[5] == 0 and t[6] == 1 for t in tiles)
+
+
 # ---- FP32 router GEMM (BF16x3) planning, host side -----------------------------------------
 
 

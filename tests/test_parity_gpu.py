@@ -488,3 +488,49 @@ def test_ticketed_weight_gradient_replayed_from_a_cuda_graph(det, env, monkeypat
         if det:
             assert torch.equal(out.view(torch.int32), eager.view(torch.int32)), f"replay {i}"
     assert gg.cake_gg_check_status(ws, stream.cuda_stream) == gg.CAKE_GG_OK
+
+
+@pytest.mark.parametrize("sizes,N,K", [([3000], 384, 1024), ([1000], 512, 2048), ([5000], 256, 768)])
+@pytest.mark.parametrize("det,out_dtype", [(1, "fp32"), (0, "bf16"), (1, "bf16")])
+def test_streamk_weight_gradient(sizes, N, K, det, out_dtype, monkeypatch):
+    """Stream-K walk forced on small one-expert shapes (segments of a few k-blocks cross several
+    tile boundaries; a ragged last k-block; NaN rows past the expert): every element against the
+    oracle, guard bands intact."""
+    monkeypatch.setenv("CAKE_GG_STREAMK", "2")
+    plan = gg.cake_gg_plan("wgrad", 1, sum(sizes) + 3, N, K, out_dtype, det)
+    assert plan.streamk_kblocks > 0
+    check_case("wgrad", sizes, N, K, out_dtype, det, seed=29, extra_rows=3)
+
+
+def test_streamk_bitwise_across_sm_caps_and_equal_pieces(monkeypatch):
+    """The stream-K pieces are a function of the plan and the offsets alone: SM caps 7, 100, 148
+    and the full device give the same bits; exact-integer inputs give the oracle's bits."""
+    import torch
+    monkeypatch.setenv("CAKE_GG_STREAMK", "2")
+    Xb, Wb, Gb, off = make_inputs([3000], 384, 1024, seed=30, extra_rows=3)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    ref = run("wgrad", X, W, G, off, "fp32", 1)
+    for cap in (7, 100, 148, 0):
+        out = run("wgrad", X, W, G, off, "fp32", 1, max_sms=cap)
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"max_sms={cap}"
+    # small integers: every FP32 sum is exact, so the pieces' sum is the oracle's value exactly
+    rng = np.random.default_rng(31)
+    Xi = wl.f32_to_bf16_bits(rng.integers(-2, 3, Xb.shape).astype(np.float32))
+    Gi = wl.f32_to_bf16_bits(rng.integers(-2, 3, Gb.shape).astype(np.float32))
+    for det in (1, 0):
+        out = run("wgrad", to_dev(Xi), W, to_dev(Gi), off, "fp32", det)
+        assert np.array_equal(out.double().cpu().numpy(), oracle.wgrad(Gi, Xi, off, 1))
+
+
+def test_streamk_with_no_rows_writes_zeros(monkeypatch):
+    import torch
+    monkeypatch.setenv("CAKE_GG_STREAMK", "2")
+    Xb, Wb, Gb, _ = make_inputs([2000], 512, 1024, seed=32)
+    X, G = to_dev(Xb), to_dev(Gb)
+    plan = gg.cake_gg_plan("wgrad", 1, 2000, 512, 1024, "fp32", 1)
+    assert plan.streamk_kblocks > 0
+    offs = torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = torch.full((1, 512, 1024), float("nan"), device="cuda")
+    gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", plan=plan, out=out)
+    torch.cuda.synchronize()
+    assert bool((out == 0).all())
