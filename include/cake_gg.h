@@ -59,8 +59,9 @@
  *     CAKE_GG_CSPLIT (0, or 2..8 cluster splits), CAKE_GG_TAIL=0 (no split
  *     tail), CAKE_GG_STREAMK (0: never, the default; 1: by the cost rule;
  *     2: wherever the walk applies), CAKE_GG_STREAMK_KB (its segment length
- *     in k-blocks),
- *     CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2);
+ *     in k-blocks), CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2),
+ *     CAKE_GG_DECIDED=0 (the non-deterministic planner ignores its table of
+ *     measured points where a plan rule failed the decision protocol);
  *   read by each compute call, changing no result:
  *     CAKE_GG_PDL=0 (no programmatic dependent launch), CAKE_GG_DYN=0 (static
  *     unit order), CAKE_GG_SPIN_NS (an early split's poll for its tile's

@@ -165,6 +165,34 @@ int32_t choose_streamk(int32_t N, int32_t K, int64_t M_max, int32_t bn, int32_t 
     return 0;
 }
 
+// Plan rules the decision protocol dropped at measured points, for the
+// non-deterministic planner (the pages apply their rule -- a paired sign test
+// at the op, at most 3 % slower next to a kernel holding 8 / 16 / 32 SMs, the
+// backward and checkpointed step at most 1.3 % slower -- to the planner of
+// deterministic=False only; the deterministic variant's plans are kept).
+// Measured with `bench.py --decide RULE --det 0` on GB300; at these points
+// the rule failed the co-run condition, so the baseline plan runs.
+enum DecidedRule { kRuleSplit = 1, kRuleTail = 2, kRuleWide = 4 };
+struct DecidedPoint {
+    int32_t E, N, K;
+    int64_t M_lo, M_hi;     // M_max range of the point (+- 5 % of the measured rows)
+    int drop;               // DecidedRule bits dropped there
+};
+constexpr DecidedPoint kDecidedPoints[] = {
+    {1, 512, 4096, 15565, 17203, kRuleSplit},      // dense 4096 -> 512, T = 16384
+    {1, 1024, 5120, 15565, 17203, kRuleTail},      // dense 5120 -> 1024, T = 16384
+    {1, 4096, 4096, 15565, 17203, kRuleWide},      // dense 4096 -> 4096, T = 16384
+    {8, 4096, 6144, 124518, 137626, kRuleTail},    // gate_up E8 M131072 (N 4096, K 6144), balanced
+};
+
+int decided_drop(int32_t E, int32_t N, int32_t K, int64_t M_max)
+{
+    int drop = 0;
+    for (const DecidedPoint &d : kDecidedPoints)
+        if (d.E == E && d.N == N && d.K == K && M_max >= d.M_lo && M_max <= d.M_hi) drop |= d.drop;
+    return drop;
+}
+
 int tmem_cols_for(int bn)
 {
     if (bn > 256) return 512;  // one 512-column accumulator
@@ -769,7 +797,10 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // (only when those tiles fill at least half a wave of pairs: fewer, larger
     // units leave SMs idle or force a split whose finish the single
     // accumulator cannot overlap)
-    const int env_wide = env_int("CAKE_GG_WIDE", 1);   // 0 off, 1 by the rule, 2 wherever they fit
+    // the non-deterministic planner drops rules at points where they failed the decision protocol
+    const int drop = (pass == CAKE_GG_WGRAD && !deterministic && env_int("CAKE_GG_DECIDED", 1) != 0)
+                         ? decided_drop(E, N, K, M_max) : 0;
+    const int env_wide = (drop & kRuleWide) ? 0 : env_int("CAKE_GG_WIDE", 1);   // 0 off, 1 by the rule, 2 wherever they fit
     const int64_t wide_units = int64_t(E) * ((N + 2 * kTileM - 1) / (2 * kTileM)) * ((int64_t(K) + 511) / 512);
     if (pass == CAKE_GG_WGRAD && plan->pair == 2 && !plan->swap_ab && bn == 256 && K >= 1024 &&
         M_max / E >= 8192 && (wide_units >= kWaveCtas / 2 || env_wide == 2) && env_wide != 0) {
@@ -812,9 +843,9 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         if (tpe * E > INT32_MAX) return CAKE_GG_ERR_OVERFLOW;
         // the unsplit alternative may finish its last partial wave as a split tail
         int32_t tu = 0, ts = 0;
-        if (!plan->swap_ab && env_int("CAKE_GG_TAIL", 1) != 0)
+        if (!plan->swap_ab && env_int("CAKE_GG_TAIL", 1) != 0 && !(drop & kRuleTail))
             choose_tail(E, N, K, M_max, bn, bk, plan->pair, &tu, &ts);
-        plan->split_chunk = choose_split_chunk(tpe * E, (M_max / E + bk - 1) / bk, bn, bk, ts);
+        plan->split_chunk = (drop & kRuleSplit) ? 0 : choose_split_chunk(tpe * E, (M_max / E + bk - 1) / bk, bn, bk, ts);
         const char *es = std::getenv("CAKE_GG_SPLIT_CHUNK");
         if (es && *es) {
             const int v = std::atoi(es);
@@ -842,7 +873,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     }
     // split tail of an unsplit weight gradient (see choose_tail)
     if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->split_chunk == 0 && plan->cluster_splits == 0 &&
-        env_int("CAKE_GG_TAIL", 1) != 0)
+        env_int("CAKE_GG_TAIL", 1) != 0 && !(drop & kRuleTail))
         choose_tail(E, N, K, M_max, bn, bk, plan->pair, &plan->tail_units, &plan->tail_splits);
     // stream-K walk of a one-expert weight gradient (see choose_streamk); it
     // replaces a split or a split tail

@@ -281,6 +281,30 @@ def test_tile_walk_streamk_empty_expert_writes_zero_tiles():
     assert all(t[5] == 0 and t[6] == 1 for t in tiles)
 
 
+@pytest.mark.parametrize("E,M,N,K,od,field,det_value", [
+    (1, 16384, 512, 4096, "fp32", "split_chunk", 64),     # split dropped
+    (1, 16384, 1024, 5120, "fp32", "tail_splits", 8),     # split tail dropped
+    (1, 16384, 4096, 4096, "fp32", "tile_n", 512),        # 256 x 512 tiles dropped
+    (8, 131072, 4096, 6144, "bf16", "tail_splits", 2),    # split tail dropped
+])
+def test_nondeterministic_planner_drops_rules_that_failed_the_decision_protocol(E, M, N, K, od, field, det_value):
+    """At points where a plan rule failed the pages' decision protocol (measured with bench.py
+    --decide), the non-deterministic planner runs the baseline plan; the deterministic planner keeps
+    the rule; CAKE_GG_DECIDED=0 restores the rule for non-deterministic plans."""
+    det = gg.cake_gg_plan("wgrad", E, M, N, K, od, 1).as_dict()
+    nd = gg.cake_gg_plan("wgrad", E, M, N, K, od, 0).as_dict()
+    assert det[field] == det_value
+    assert nd[field] != det_value
+    os.environ["CAKE_GG_DECIDED"] = "0"
+    try:
+        nd_rule = gg.cake_gg_plan("wgrad", E, M, N, K, od, 0).as_dict()
+    finally:
+        del os.environ["CAKE_GG_DECIDED"]
+    choices = ("tile_n", "tile_k", "stages", "pair", "swap_ab", "split_chunk", "cluster_splits", "tail_units",
+               "tail_splits", "staging_bufs", "streamk_kblocks")
+    assert {k: nd_rule[k] for k in choices} == {k: det[k] for k in choices}
+
+
 # ---- FP32 router GEMM (BF16x3) planning, host side -----------------------------------------
 
 
