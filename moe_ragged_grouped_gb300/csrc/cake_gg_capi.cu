@@ -20,7 +20,6 @@ using namespace cakegg;
 
 namespace {
 
-constexpr int kWaveCtas = 152;              // GB300 SMs: the wave size the split model assumes
 constexpr int kMinSplitChunk = 4;           // k-blocks (256 rows) per split at least
 constexpr int kMaxClusterSplit = 8;         // portable cluster size
 constexpr size_t kSmemLimit = kSmemOptInLimit;
@@ -1021,7 +1020,7 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
         spref[i + 1] = spref[i] + expert_splits(g, off[i + 1] - off[i]);
     }
     std::vector<int32_t> off_v(off, off + E + 1);
-    if (g.tail > 0 && !tail_active(g, off_v.data(), order.data())) g.tail = g.tail_s = 0;
+    if (g.tail > 0 && tail_fits_whole(g, off_v.data(), order.data(), kWaveCtas / g.pair)) g.tail = g.tail_s = 0;
     int64_t units = walk_length(g, pref[E]);
     // stream-K: unit ids v * pmax + piece over the virtual pairs (ids a segment
     // does not use are skipped)

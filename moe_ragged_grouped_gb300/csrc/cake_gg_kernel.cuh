@@ -106,6 +106,7 @@ struct __align__(16) Ctrl {
     int32_t last_flag;
     int32_t claim;          // split finish: the slice the epilogue claimed last
     uint32_t epoch;         // this call's ticket tag (read from the workspace at set-up)
+    int32_t tail_whole;     // weight gradient: the split tail runs whole (slack placement, decided at set-up)
 };
 
 // Walk tables after the control block, sized by the launch's E: off[E+1]
@@ -702,6 +703,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     }
     // the set-up temporaries in the ring are overwritten by TMA (async proxy) later
     fence_proxy_async_smem();
+    if (MODE == kModeWgrad && g.tail > 0) {
+        // slack placement of the split tail, from the walk tables (one thread)
+        __syncthreads();
+        if (tid == 0) c->tail_whole = !c->bad && tail_fits_whole(g, t_off, t_order, int32_t(kWaveCtas / PAIR)) ? 1 : 0;
+    }
     tc_fence_before_sync();
     __syncthreads();
     if (c->bad) {
@@ -723,7 +729,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     }
     tc_fence_after_sync();
 
-    if (MODE == kModeWgrad && g.tail > 0 && !tail_active(g, t_off, t_order)) g.tail = g.tail_s = 0;
+    if (MODE == kModeWgrad && g.tail > 0 && c->tail_whole) g.tail = g.tail_s = 0;
     const int64_t total = walk_length(g, t_pref[E]);
     const uint32_t tmem_base = c->tmem_base;
     const uint32_t acc_stride = uint32_t(p.tmem_cols) / 2;

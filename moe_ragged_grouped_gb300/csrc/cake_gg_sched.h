@@ -200,11 +200,30 @@ struct Tile {
     bool tail;        // a piece of a split tail unit (partials in slots, also when non-deterministic)
 };
 
-// A split tail pays only when the walk's last units are full length: with
-// skewed experts the last units (the lightest expert's, heaviest-first order)
-// are short already.  On: the lightest expert costs at least 80% of the
-// heaviest.  A function of the offsets alone, so every CTA (and the host
-// walk) decides alike.
+// Slack placement of the split tail (flashinfer PR #8258, opening summary,
+// 2nd paragraph: while the full-wave tiles run, the clusters are ranked by
+// load; if the less-loaded ones have room -- each stays within the largest
+// load plus one tail share -- every tail tile goes whole to one of them, with
+// no tail sums; otherwise the split tail runs).  Here the loads are projected
+// from the offsets, not measured: the walk's units are taken in walk order by
+// the first of P pairs to become free (what the unit counter does on equal-
+// speed pairs), a unit lasting its k-blocks, up to the last g.tail units.
+// Then each tail unit in turn goes to a least-loaded pair, which must stay
+// within the largest load plus one tail share (the unit's k-blocks /
+// g.tail_s) plus what splitting itself costs (split_overhead_kblocks: the
+// pages' test alone split the tail on ragged "random" workloads where the
+// decision protocol measured the split slower).  True: the tail units run
+// whole.  A function of the offsets and
+// the fixed wave P alone, so every CTA (and the host walk) decides alike and
+// deterministic results do not depend on max_sms.  Loads are kept as at most
+// kSlackClasses (load, pairs) classes; more distinct loads -> the split tail.
+constexpr int kSlackClasses = 48;
+constexpr int kWaveCtas = 152;      // GB300 SMs: the fixed wave plans and projections assume
+constexpr int kSlackMaxE = 64;      // projection only up to this many experts (else the 80 % rule below)
+
+// The cheaper rule used above kSlackMaxE experts: the tail stays split when the
+// walk's last units are about as long as its first (the lightest expert costs
+// at least 80 % of the heaviest).
 CAKE_HD bool tail_active(const Geom &g, const int32_t *off, const int32_t *order)
 {
     if (g.mode != kModeWgrad || g.tail <= 0) return false;
@@ -212,6 +231,91 @@ CAKE_HD bool tail_active(const Geom &g, const int32_t *off, const int32_t *order
     const int64_t c_hi = expert_cost(g, off[e_hi + 1] - off[e_hi]);
     const int64_t c_lo = expert_cost(g, off[e_lo + 1] - off[e_lo]);
     return 5 * c_lo >= 4 * c_hi;
+}
+
+CAKE_HD void slack_add(int64_t *val, int32_t *cnt, int &nc, int64_t v, int32_t k)
+{
+    int i = 0;
+    while (i < nc && val[i] < v) ++i;
+    if (i < nc && val[i] == v) {
+        cnt[i] += k;
+        return;
+    }
+    for (int j = nc; j > i; --j) {
+        val[j] = val[j - 1];
+        cnt[j] = cnt[j - 1];
+    }
+    val[i] = v;
+    cnt[i] = k;
+    ++nc;
+}
+
+// What splitting a unit costs on top of its pieces, in k-blocks: the FP32
+// partial tile's write and read (x2 margin) and the finish -- the cost the
+// planner's split model charges (rounded up).
+CAKE_HD int64_t split_overhead_kblocks(int32_t bn, int32_t bk)
+{
+    const int64_t num = int64_t(4096) * bn * 64;
+    const int64_t den = (int64_t(16384) + int64_t(128) * bn) * bk;
+    return (num + den - 1) / den + (4 * 64 + bk - 1) / bk;
+}
+
+CAKE_HD bool tail_fits_whole(const Geom &g, const int32_t *off, const int32_t *order, int32_t P)
+{
+    if (g.mode != kModeWgrad || g.tail <= 0 || g.tail_s <= 1) return true;
+    if (g.E > kSlackMaxE) return !tail_active(g, off, order);
+    int64_t val[kSlackClasses + 1];
+    int32_t cnt[kSlackClasses + 1];
+    int nc = 1;
+    val[0] = 0;
+    cnt[0] = P;
+    int64_t units = 0;
+    for (int i = 0; i < g.E; ++i) units += expert_tiles(g, off[order[i] + 1] - off[order[i]]);
+    int64_t before = units - g.tail;   // units of the walk ahead of the tail
+    for (int i = 0; i < g.E; ++i) {
+        const int32_t rows = off[order[i] + 1] - off[order[i]];
+        const int64_t c = ceil_div_i(rows, g.bk);   // k-blocks of a whole unit of this expert
+        int64_t n = expert_tiles(g, rows);
+        while (n > 0) {
+            if (before > 0) {
+                // the next units of the walk go to the least-loaded pairs
+                int64_t k = n < cnt[0] ? n : cnt[0];
+                if (k > before) k = before;
+                const int64_t v = val[0] + c;
+                cnt[0] -= int32_t(k);
+                if (cnt[0] == 0) {
+                    for (int j = 0; j + 1 < nc; ++j) {
+                        val[j] = val[j + 1];
+                        cnt[j] = cnt[j + 1];
+                    }
+                    --nc;
+                }
+                slack_add(val, cnt, nc, v, int32_t(k));
+                if (nc > kSlackClasses) return false;
+                n -= k;
+                before -= k;
+            } else {
+                // a tail unit, whole, on a least-loaded pair: within the largest
+                // load plus one tail share -- the share a piece would take, with
+                // what splitting costs on top of the pieces?
+                const int64_t vmax = val[nc - 1];
+                const int64_t ovh = split_overhead_kblocks(g.bn, g.bk);
+                if ((val[0] + c - vmax - ovh) * g.tail_s > c) return false;
+                const int64_t v = val[0] + c;
+                if (--cnt[0] == 0) {
+                    for (int j = 0; j + 1 < nc; ++j) {
+                        val[j] = val[j + 1];
+                        cnt[j] = cnt[j + 1];
+                    }
+                    --nc;
+                }
+                slack_add(val, cnt, nc, v, 1);
+                if (nc > kSlackClasses) return false;
+                --n;
+            }
+        }
+    }
+    return true;
 }
 
 // Positions in the walk: the weight gradient's last g.tail units each take

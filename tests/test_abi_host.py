@@ -305,6 +305,52 @@ def test_nondeterministic_planner_drops_rules_that_failed_the_decision_protocol(
     assert {k: nd_rule[k] for k in choices} == {k: det[k] for k in choices}
 
 
+def _slack_rule_reference(sizes, plan):
+    """Independent restatement of the slack-placement rule (PR #8258, opening summary, 2nd
+    paragraph): walk the experts heaviest first (ties by index); every unit of an expert lasts its
+    k-blocks; the walk's units go, in order, to whichever of the 76 pairs becomes free first (a heap
+    of pair loads); each of the last tail_units units must fit on the least-loaded pair within the
+    largest load plus one tail share (k-blocks / tail_splits) plus the split's own cost.  True: the
+    tail runs whole."""
+    import heapq
+    bk = plan.tile_k
+    m_units = -(-(-(-plan.N // 128)) // 2)
+    n_tiles = -(-plan.K // plan.tile_n)
+    kb = [-(-s_ // bk) for s_ in sizes]
+    order = sorted(range(len(sizes)), key=lambda e: (-kb[e], e))
+    walk = [kb[e] for e in order for _ in range(m_units * n_tiles)]
+    T = plan.tail_units
+    loads = [0] * 76
+    heapq.heapify(loads)
+    for c in walk[:len(walk) - T]:
+        heapq.heappush(loads, heapq.heappop(loads) + c)
+    # what a split costs on top of its pieces, in k-blocks: partial tile write + read (x2) and the
+    # finish, as the planner's split model charges it
+    ovh = -(-(4096 * plan.tile_n * 64) // ((16384 + 128 * plan.tile_n) * bk)) + -(-(4 * 64) // bk)
+    for c in walk[len(walk) - T:]:
+        lo = heapq.heappop(loads)
+        if (lo + c - max(loads + [lo]) - ovh) * plan.tail_splits > c:
+            return False
+        heapq.heappush(loads, lo + c)
+    return True
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_split_tail_slack_placement_matches_a_heap_schedule(seed):
+    """The walk's decision (tail pieces present or not) equals the reference rule above on ragged
+    experts around the planned size (the plan assumes balanced experts: 4 x 8192 rows)."""
+    rng = np.random.default_rng(seed)
+    plan = gg.cake_gg_plan("wgrad", 4, 4 * 8192 + 5, 3072, 4096, "bf16", 1)
+    assert plan.tail_splits > 1
+    spread = [0.0, 0.01, 0.05, 0.2, 0.5, 0.9][seed % 6]
+    sizes = [max(0, int(8192 * (1 + spread * rng.uniform(-1, 1)))) for _ in range(4)]
+    scale = (4 * 8192) / max(1, sum(sizes))
+    sizes = [int(x * scale) for x in sizes]
+    tiles = gg.cake_gg_tile_walk(plan, wl.offsets_from_sizes(sizes))
+    has_pieces = bool((tiles[:, 4] > 1).any())
+    assert has_pieces == (not _slack_rule_reference(sizes, plan)), sizes
+
+
 # ---- FP32 router GEMM (BF16x3) planning, host side -----------------------------------------
 
 
