@@ -486,6 +486,20 @@ static __device__ __noinline__ void zero_stale_rows(uint8_t *ring, uint32_t ring
     fence_proxy_async_smem();
 }
 
+// A CTA counts itself retired; the last one of the call leaves the unit
+// counter at zero for the next call (every CTA's fetches are done when it
+// counts itself) and stores this call's ticket tag (every CTA read the old one
+// at its set-up).
+__device__ __forceinline__ void retire_cta(const KParams &p, uint32_t epoch)
+{
+    __threadfence();
+    if (atomicAdd(p.sched + 32, 1) == int32_t(gridDim.x) - 1) {
+        atomicExch(p.sched, 0);
+        atomicExch(reinterpret_cast<unsigned int *>(p.epoch_word), epoch);
+        atomicExch(p.sched + 32, 0);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int KMODE, bool SWAP, bool OUT_F32, int PAIR>
@@ -585,6 +599,10 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     // start its own part 1
     grid_dependency_wait();
     grid_launch_dependents();
+    // the producer's first unit from the counter: its round trip overlaps the
+    // offsets load and the table build (a stream-K walk takes no counter units)
+    int32_t first_fetch = 0;
+    if (tid == 0 && p.dyn && leader && !(MODE == kModeWgrad && g.sk > 0)) first_fetch = atomicAdd(p.sched, 1);
     if (tid == 32 && p.retire) {
         // this call's ticket tag: one past the last call's, which the previous
         // call's last CTA wrote (a call replayed from a CUDA graph advances too)
@@ -712,7 +730,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     __syncthreads();
     if (c->bad) {
         // every CTA (and every CTA of a cluster) sees the same offsets and leaves here
-        if (tid == 0) atomicCAS(p.status, 0, kStatusBadOffsets);
+        // (counting itself retired, so the counters are zero again after the call)
+        if (tid == 0) {
+            atomicCAS(p.status, 0, kStatusBadOffsets);
+            if (p.retire) retire_cta(p, c->epoch);
+        }
         if (warp == 1) {
             tc_fence_after_sync();
             tmem_dealloc<PAIR>(c->tmem_base, uint32_t(p.tmem_cols));
@@ -755,7 +777,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 sk_pm = sk_pmax(g, sk_K);
                 sk_nv = sk_virtual(g, sk_K);
             }
-            if (p.dyn && leader && !skw) nxt = atomicAdd(p.sched, 1);
+            if (p.dyn && leader && !skw) nxt = first_fetch;
             while (ok) {
                 int64_t t;
                 if (!p.dyn) {
@@ -1448,17 +1470,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         tc_fence_after_sync();
         tmem_dealloc<2>(tmem_base, uint32_t(p.tmem_cols));
     }
-    if (p.retire && tid == 0) {
-        // the last CTA to retire leaves the unit counter at zero for the next
-        // call (every CTA's fetches are done when it counts itself) and stores
-        // this call's ticket tag (every CTA read the old one at its set-up)
-        __threadfence();
-        if (atomicAdd(p.sched + 32, 1) == int32_t(gridDim.x) - 1) {
-            atomicExch(p.sched, 0);
-            atomicExch(reinterpret_cast<unsigned int *>(p.epoch_word), c->epoch);
-            atomicExch(p.sched + 32, 0);
-        }
-    }
+    if (p.retire && tid == 0) retire_cta(p, c->epoch);
 }
 
 }  // namespace cakegg
