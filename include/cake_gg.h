@@ -53,7 +53,7 @@
  *   read by cake_gg_plan(), recorded in the plan it fills (a deterministic
  *   plan's summation order follows them):
  *     CAKE_GG_TILE_N (64..256), CAKE_GG_TILE_K (64, 128, 256), CAKE_GG_PAIR=0
- *     (single CTAs only), CAKE_GG_WIDE (0: no 256 x 512 weight-gradient tiles,
+ *     (single CTAs only) or 2 (pairs wherever the tile allows), CAKE_GG_WIDE (0: no 256 x 512 weight-gradient tiles,
  *     2: wherever they fit), CAKE_GG_WIDE_FD=1 (512-wide forward / data-
  *     gradient tiles), CAKE_GG_SPLIT_CHUNK (k-blocks per split, 0 = no split),
  *     CAKE_GG_CSPLIT (0, or 2..8 cluster splits), CAKE_GG_TAIL=0 (no split

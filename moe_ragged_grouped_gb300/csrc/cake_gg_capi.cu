@@ -788,6 +788,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
                   !(pass != CAKE_GG_WGRAD && red_fd <= 64)) ? 2 : 1;
     const int env_pair = env_int("CAKE_GG_PAIR", -1);
     if (env_pair == 0) plan->pair = 1;
+    if (env_pair == 2 && bn % 128 == 0 && !(pass == CAKE_GG_WGRAD && plan->swap_ab)) plan->pair = 2;
     // long weight-gradient units: a pair takes a 256 x 512 tile (two N = 256
     // MMAs sharing each A stage; TMEM holds one accumulator): a quarter fewer
     // operand bytes per flop, and a wave covers twice an expert's tile area
