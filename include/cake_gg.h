@@ -63,7 +63,9 @@
  *     CAKE_GG_DECIDED=0 (the non-deterministic planner ignores its table of
  *     measured points where a plan rule failed the decision protocol);
  *   read by each compute call, changing no result:
- *     CAKE_GG_PDL=0 (no programmatic dependent launch), CAKE_GG_DYN=0 (static
+ *     CAKE_GG_PDL=0 (no programmatic dependent launch), CAKE_GG_ROUTER_STAGGER
+ *     (the router's per-unit k-order stagger, default 7, 0 = in order;
+ *     changes the router's summation order), CAKE_GG_DYN=0 (static
  *     unit order), CAKE_GG_SPIN_NS (an early split's poll for its tile's
  *     other partials, default 6000), CAKE_GG_PREFETCH (L2 prefetch distance
  *     in stages), CAKE_GG_STACK=0 and CAKE_GG_TMA_STORE=0 (plainer copy and

@@ -635,7 +635,9 @@ int router_plan(cake_gg_plan_t *plan, int64_t T, int32_t R, int32_t K, int32_t m
     plan->tile_n = bn;
     plan->pair = bn % 128 == 0 ? 2 : 1;
     plan->tile_k = 64;
-    int stages = kMaxStages;
+    // (at most 4 stages: each stage's split A tile takes 64 of the 256 TMEM
+    // columns after the accumulator)
+    int stages = 4;
     while (stages > 2 && smem_bytes_for(bn, stages, 1, 1, 0, plan->pair, 1, true) > kSmemLimit) --stages;
     if (smem_bytes_for(bn, stages, 1, 1, 0, plan->pair, 1, true) > kSmemLimit) return CAKE_GG_ERR_UNSUPPORTED;
     plan->stages = stages;
@@ -689,6 +691,9 @@ int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, f
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
     p.prefetch = env_int("CAKE_GG_PREFETCH", 0);
     if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
+    p.kstagger = env_int("CAKE_GG_ROUTER_STAGGER", 7);
+    if (p.kstagger < 0) p.kstagger = 0;
+    if (p.kstagger > 0) p.prefetch = 0;   // (prefetches assume the in-order walk)
 
     const Geom g = make_geom(kModeFwd, 1, N, K, plan->M_max, bn, 0, 0, P, 64);
     const uint64_t unit_bound = (M / (uint64_t(kTileM) * P) + 2) * uint64_t(g.n_tiles);

@@ -81,6 +81,7 @@ struct KParams {
     int32_t tail;           // weight gradient: split tail units ...
     int32_t tail_s;         // ... and pieces per tail unit (0 = none)
     int32_t sk;             // weight gradient of one expert: stream-K segment length in k-blocks (0 = off)
+    int32_t kstagger;       // router: unit t walks its k-blocks from (t * kstagger) mod their count (0 = in order)
     int32_t *sched;         // [0]: next unit, [32]: CTAs retired (zero between calls)
     uint64_t timeout_ns;
 };
@@ -448,6 +449,19 @@ __device__ __forceinline__ void stage_and_store(uint8_t *staging, int &buf, int 
     if (staging_bufs == 2) buf ^= 1;
 }
 
+// Router: the four K = 16 MMAs of a 64-deep stage with A in tensor memory
+// (8 columns per step from a_tmem) and K-major B in shared memory (32 bytes per
+// step along the 128-byte swizzled row).
+template <int CG>
+__device__ __forceinline__ void issue_stage_mmas_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bd0, uint32_t idesc,
+                                                    bool first)
+{
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+        umma_bf16_ta<CG>(d_tmem, a_tmem + uint32_t(ks) * 8u, bd0 + uint64_t((uint32_t(ks) * 32u) >> 4), idesc,
+                         (!first || ks > 0) ? 1u : 0u);
+}
+
 // All MMAs of one stage: 4 * KPS k-steps of 16.  Descriptors are built once
 // per stage and advanced by adding (byte offset >> 4) to the 14-bit start
 // address field (shared-memory addresses stay below 2^18, so no carry).
@@ -755,8 +769,10 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     const int64_t total = walk_length(g, t_pref[E]);
     const uint32_t tmem_base = c->tmem_base;
     const uint32_t acc_stride = uint32_t(p.tmem_cols) / 2;
-    // a 512-wide tile fills TMEM: one accumulator, released before the next unit
-    const int nacc = p.bn > 256 ? 1 : 2;
+    // a 512-wide tile fills TMEM: one accumulator, released before the next unit;
+    // the router keeps one accumulator (columns 0..255) and the split A tiles of
+    // its stages in the columns after it (64 per stage: high, then low parts)
+    const int nacc = (p.bn > 256 || RT) ? 1 : 2;
 
     if (warp == 0) {
         // ======================= TMA producer =======================
@@ -860,7 +876,15 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         const int nb = p.bn / 64;
                         const int jb0 = PAIR == 2 ? rank * nb / 2 : 0;
                         const int jb1 = PAIR == 2 ? (rank + 1) * nb / 2 : nb;
-                        const int32_t k0 = kb * p.bk;      // first reduction element of the stage
+                        // (the router staggers each unit's k order: with one output-column
+                        // tile every pair reads the same weight slices, and in lock step
+                        // they would all read the same lines at once)
+                        int32_t kbr = kb;
+                        if (RT && p.kstagger > 0) {
+                            const int32_t nk = ti.kb1 - ti.kb0;
+                            kbr = ti.kb0 + int32_t((int64_t(kb - ti.kb0) + (t * p.kstagger) % nk) % nk);
+                        }
+                        const int32_t k0 = kbr * p.bk;      // first reduction element of the stage
                         if (MODE == kModeWgrad) {
                             const int32_t r = ti.row0 + k0;
                             // both operands stream once per unit from rows far apart in
@@ -1019,12 +1043,13 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         const uint64_t bd0 = B_MN ? smem_desc_sw128(sb, atom_b, 1024) : smem_desc_sw128(sb, 16, 1024);
                         const bool first = kb == ti.kb0;
                         if (RT) {
-                            // x_hi w_hi + x_hi w_lo + x_lo w_hi into one accumulator
-                            const uint64_t al = smem_desc_sw128(sa + kRouterABytes / 2, 16, 1024);
+                            // x_hi w_hi + x_hi w_lo + x_lo w_hi into one accumulator; the
+                            // split A tile of this stage is in TMEM (high parts, then low)
+                            const uint32_t a_hi = tmem_base + 256u + uint32_t(stage) * 64u;
                             const uint64_t bl = smem_desc_sw128(sb + uint32_t(p.bn / PAIR) * 128u, 16, 1024);
-                            issue_stage_mmas<1, false, false, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
-                            issue_stage_mmas<1, false, false, PAIR>(d_tmem, ad0, bl, idesc, false, chunk_b);
-                            issue_stage_mmas<1, false, false, PAIR>(d_tmem, al, bd0, idesc, false, chunk_b);
+                            issue_stage_mmas_ta<PAIR>(d_tmem, a_hi, bd0, idesc, first);
+                            issue_stage_mmas_ta<PAIR>(d_tmem, a_hi, bl, idesc, false);
+                            issue_stage_mmas_ta<PAIR>(d_tmem, a_hi + 32u, bd0, idesc, false);
                         } else if (p.bn > 256) {
                             // this CTA's halves of the two 256-column B tiles sit 2 * (128 / PAIR / 64) atoms apart
                             const uint32_t half = uint32_t(256 / 64 / PAIR) * atom_b;
@@ -1390,13 +1415,14 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         }
     } else {
         // ================== converters (router: warps 6..9) ==================
-        // Thread `crow` owns A row crow of every stage: its 64 FP32 values (one
+        // Thread `crow` owns A row crow of every stage -- the TMEM lane it may
+        // write (warp w reaches lanes 32 (w % 4) .. + 31): its 64 FP32 values (one
         // 128-byte row in each of the two 32-column boxes, 128-byte swizzle)
-        // become a 128-byte row of BF16 high parts written over the first box
-        // and one of low parts over the second -- the K-major, 128-byte
-        // swizzled layout of a 64-deep BF16 A tile.  A thread reads only its
-        // own row before writing it, so the split needs no barrier inside.
-        const int crow = (warp - 6) * 32 + lane;
+        // become 32 columns of BF16 high parts and 32 of low parts in the
+        // stage's A slot of tensor memory (two K elements per 32-bit column,
+        // the lower index in the lower half), which the MMAs read as their A
+        // operand; shared memory keeps the FP32 tile unchanged.
+        const int crow = (warp & 3) * 32 + lane;
         const int sw = crow & 7;
         int stage = 0;
         uint32_t phase = 0;
@@ -1426,15 +1452,14 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     const float h0 = __uint_as_float(hi[j] << 16), h1 = __uint_as_float(hi[j] & 0xFFFF0000u);
                     lo[j] = pack_bf16x2(v[2 * j] - h0, v[2 * j + 1] - h1);      // v - hi is exact in FP32
                 }
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    *reinterpret_cast<uint4 *>(row_a + ((ch ^ sw) << 4)) =
-                        make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
-                    *reinterpret_cast<uint4 *>(row_b + ((ch ^ sw) << 4)) =
-                        make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
-                }
-                // generic-proxy writes -> visible to the tensor cores' reads
-                fence_proxy_async_smem();
+                // the stage's A slot (its last readers, the MMAs of the stage's
+                // previous use, completed before the producer refilled the stage)
+                const uint32_t ta = tmem_base + (uint32_t((warp & 3) * 32) << 16) + 256u + uint32_t(stage) * 64u;
+                tmem_st_32x32b_x32(ta, hi);
+                tmem_st_32x32b_x32(ta + 32u, lo);
+                tmem_st_wait();
+                // tensor-memory stores -> ordered before the MMA warp's reads
+                tc_fence_before_sync();
                 named_bar_sync(2, 128);
                 if (warp == 6 && lane == 0) {
                     if (leader) mbar_arrive(smem_u32(&c->conv[stage]));
