@@ -59,9 +59,11 @@ def parse_args():
                          "back), per-pass times from a separate loop")
     ap.add_argument("--graph", action="store_true",
                     help="replay each pass from a captured CUDA graph (removes host launch overhead)")
-    ap.add_argument("--corun", default="",
-                    help="comma list of SM counts (e.g. 8,16,32): after the timed region, time the same "
-                         "steps again while a spinner on another stream holds that many SMs")
+    ap.add_argument("--corun", default="8,16,32",
+                    help="comma list of SM counts (default 8,16,32; empty = skip): after the timed region, "
+                         "time the same steps again while a spinner on another stream holds that many SMs")
+    ap.add_argument("--no-pages-sample", action="store_true",
+                    help="skip the pages' grid sample (dW, ckpt, ckpt ES of gate_up E8 M131072 bal)")
     ap.add_argument("--grid", default="", choices=["", "pages"],
                     help="pages: time the GB300 rows of the pages' per-row latency table")
     ap.add_argument("--grid-filter", default="", help="only rows whose 'shape op' contains this text")
@@ -521,6 +523,13 @@ def run_ours(args, wk):
         projection["thin"] = projection_record(gg, dev, local, rank, 4096, 48, ("wgrad", "fwd", "dgrad"))
         projection["mid"] = projection_record(gg, dev, local, rank, 4096, 512, ("wgrad",))
 
+    if not args.no_pages_sample and args.workload == "moe_gate_up" and ws == 1:
+        # a sample of the pages' latency table, ckpt / ckpt ES through the autograd API
+        projection["pages_sample"] = {
+            "rows": pages_rows(PAGES_SAMPLE, 5, dev),
+            "note": "one call per repetition, cold L2, median of 5; the pages' latencies are their GB300 "
+                    "table's, measured on their machine with their kernels (context, not a target)"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wk, X, W, G, passes, args.cpu_seconds)
@@ -775,27 +784,31 @@ def run_reference(args, wk):
     print(json.dumps(line), flush=True)
 
 
-def run_pages_grid(args):
-    """One call per repetition, L2 flushed before it, CUDA events around it.
+PAGES_SAMPLE = [("gate_up E8 M131072 bal", "dW"), ("gate_up E8 M131072 bal", "ckpt"),
+                ("gate_up E8 M131072 bal", "ckpt ES")]
 
-    "dW" is one cake_gg_wgrad call.  "ckpt" and "ckpt ES" go through the autograd API:
+
+def pages_rows(rows, reps, dev):
+    """Time rows of the pages' GB300 latency table (PR #8269) the way it was measured: one call
+    per repetition, L2 flushed (256 MB written) before it, CUDA events around it, median over
+    `reps`.  "dW" is one cake_gg_wgrad call.  "ckpt" and "ckpt ES" go through the autograd API:
     checkpointed_grouped_linear (grouped_linear in a non-reentrant torch checkpoint, early stop
     off / on) forward, then backward with the upstream gradient G.  Before the start event a GPU
     sleep of a few milliseconds is queued so that the host's enqueueing (autograd and checkpoint
-    bookkeeping) runs while the GPU sleeps: the events then bracket the device work alone."""
+    bookkeeping) runs while the GPU sleeps: the events then bracket the device work alone.
+    Returns one dict per row."""
     import torch
     from moe_ragged_grouped_gb300 import cake_gg as gg
     from moe_ragged_grouped_gb300 import workloads as wl
     from moe_ragged_grouped_gb300.autograd import checkpointed_grouped_linear
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     gg.load_library()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # twice the L2
     stream = torch.cuda.current_stream(dev)
-    rows = [r for r in wl.PAGES_GB300_ROWS if args.grid_filter in f"{r[0]} {r[1]}"]
+    table = {(r[0], r[1]): r for r in wl.PAGES_GB300_ROWS}
     cur_shape, tensors = None, None
-    ratios = {}
-    for shape, op, det_ms, sota_ms, sota_key, nd_ms in rows:
+    out_rows = []
+    for shape, op in rows:
+        _, _, det_ms, sota_ms, sota_key, nd_ms = table[(shape, op)]
         wk, od_dw = wl.pages_workload(shape)
         if shape != cur_shape:
             tensors = None
@@ -808,22 +821,17 @@ def run_pages_grid(args):
         passes = wl.PAGES_OPS[op]
         od = od_dw if op == "dW" else "bf16"
         tdt = torch.float32 if od == "fp32" else torch.bfloat16
-        outs = {"fwd": torch.empty((wk.M, wk.N), dtype=tdt, device=dev),
-                "dgrad": torch.empty((wk.M, wk.K), dtype=tdt, device=dev) if "dgrad" in passes else None,
-                "wgrad": torch.empty((wk.E, wk.N, wk.K), dtype=tdt, device=dev)}
-        plans = {p: gg.cake_gg_plan(p, wk.E, wk.M, wk.N, wk.K, od, 1) for p in set(passes)}
+        outs = {"wgrad": torch.empty((wk.E, wk.N, wk.K), dtype=tdt, device=dev)} if op == "dW" else {}
+        plans = {p: gg.cake_gg_plan(p, wk.E, wk.M, wk.N, wk.K, od, 1) for p in set(passes)} if op == "dW" else {}
         wss = {p: gg.make_workspace(plans[p], dev) for p in plans}
-        ops = {"fwd": (gg.cake_gg_fwd, X, W), "dgrad": (gg.cake_gg_dgrad, G, W), "wgrad": (gg.cake_gg_wgrad, G, X)}
-
         Xl, Wl = X.detach().requires_grad_(), W.detach().requires_grad_()
 
         def call():
             if op == "dW":
-                for p in passes:
-                    fn, a, b = ops[p]
-                    rc = fn(plans[p], a, b, outs[p], offs, od, 1, wss[p], stream=stream.cuda_stream)
-                    if rc != 0:
-                        raise gg.CakeGGError(rc, p)
+                rc = gg.cake_gg_wgrad(plans["wgrad"], G, X, outs["wgrad"], offs, od, 1, wss["wgrad"],
+                                      stream=stream.cuda_stream)
+                if rc != 0:
+                    raise gg.CakeGGError(rc, "wgrad")
             else:
                 Xl.grad = Wl.grad = None
                 Y = checkpointed_grouped_linear(Xl, Wl, offs, early_stop=(op == "ckpt ES"))
@@ -837,7 +845,7 @@ def run_pages_grid(args):
             if st != 0:
                 raise gg.CakeGGError(st, f"{shape} {p} device status")
         times = []
-        for _ in range(args.grid_reps):
+        for _ in range(reps):
             flush.zero_()
             torch.cuda._sleep(6_000_000)   # ~3 ms at 2 GHz: the host enqueues meanwhile
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -847,17 +855,32 @@ def run_pages_grid(args):
             torch.cuda.synchronize(dev)
             times.append(e0.elapsed_time(e1))
         ms = statistics.median(times)
-        line = {"grid": "pages_gb300", "shape": shape, "op": op, "out_dtype": od, "deterministic": True,
-                "path": "cake_gg_wgrad" if op == "dW" else "checkpointed_grouped_linear (autograd)",
-                "ms": round(ms, 4), "tflops": round(wk.flops(len(passes)) / (ms * 1e-3) / 1e12, 1),
-                "ms_min_max": [round(min(times), 4), round(max(times), 4)],
-                "pages_det_ms": det_ms, "vs_pages_det": round(det_ms / ms, 4),
-                "pages_nondet_ms": nd_ms, "vs_pages_nondet": round(nd_ms / ms, 4),
-                "pages_sota_ms": sota_ms, "pages_sota": sota_key, "vs_pages_sota": round(sota_ms / ms, 4)}
+        out_rows.append({"grid": "pages_gb300", "shape": shape, "op": op, "out_dtype": od, "deterministic": True,
+                         "path": "cake_gg_wgrad" if op == "dW" else "checkpointed_grouped_linear (autograd)",
+                         "ms": round(ms, 4), "tflops": round(wk.flops(len(passes)) / (ms * 1e-3) / 1e12, 1),
+                         "ms_min_max": [round(min(times), 4), round(max(times), 4)],
+                         "pages_det_ms": det_ms, "vs_pages_det": round(det_ms / ms, 4),
+                         "pages_nondet_ms": nd_ms, "vs_pages_nondet": round(nd_ms / ms, 4),
+                         "pages_sota_ms": sota_ms, "pages_sota": sota_key, "vs_pages_sota": round(sota_ms / ms, 4)})
+        del outs, wss, Xl, Wl
+    del tensors, flush
+    torch.cuda.empty_cache()
+    return out_rows
+
+
+def run_pages_grid(args):
+    """The 100 GB300 rows of the pages' latency table (or those matching --grid-filter)."""
+    import torch
+    from moe_ragged_grouped_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rows = [(r[0], r[1]) for r in wl.PAGES_GB300_ROWS if args.grid_filter in f"{r[0]} {r[1]}"]
+    ratios = {}
+    lines = pages_rows(rows, args.grid_reps, dev)
+    for line in lines:
         print(json.dumps(line), flush=True)
         for k in ("det", "nondet", "sota"):
-            ratios.setdefault((op, k), []).append(line[f"vs_pages_{k}"])
-        del outs, wss, Xl, Wl
+            ratios.setdefault((line["op"], k), []).append(line[f"vs_pages_{k}"])
     summary = {"grid": "pages_gb300", "summary": "geomean of (pages' latency / ours) per operation", "rows": len(rows)}
     for (op, k), v in sorted(ratios.items()):
         summary[f"{op} vs {k}"] = round(math.exp(sum(math.log(x) for x in v) / len(v)), 4)
