@@ -500,10 +500,11 @@ static __device__ __noinline__ void zero_stale_rows(uint8_t *ring, uint32_t ring
     fence_proxy_async_smem();
 }
 
-// A CTA counts itself retired; the last one of the call leaves the unit
-// counter at zero for the next call (every CTA's fetches are done when it
-// counts itself) and stores this call's ticket tag (every CTA read the old one
-// at its set-up).
+// A CTA counts itself retired once it will not touch the unit counter again
+// (after its last fetch, or at set-up if it takes no units from it); the last
+// one of the call leaves the counter at zero for the next call (every CTA's
+// fetches are done when it counts itself) and stores this call's ticket tag
+// (every CTA read the old one at its set-up, before counting itself).
 __device__ __forceinline__ void retire_cta(const KParams &p, uint32_t epoch)
 {
     __threadfence();
@@ -616,7 +617,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     // the producer's first unit from the counter: its round trip overlaps the
     // offsets load and the table build (a stream-K walk takes no counter units)
     int32_t first_fetch = 0;
-    if (tid == 0 && p.dyn && leader && !(MODE == kModeWgrad && g.sk > 0)) first_fetch = atomicAdd(p.sched, 1);
+    const bool fetcher = p.dyn && leader && !(MODE == kModeWgrad && g.sk > 0);   // takes units from the counter
+    if (tid == 0 && fetcher) first_fetch = atomicAdd(p.sched, 1);
     if (tid == 32 && p.retire) {
         // this call's ticket tag: one past the last call's, which the previous
         // call's last CTA wrote (a call replayed from a CUDA graph advances too)
@@ -755,6 +757,10 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         }
         return;
     }
+    // a CTA that takes no units from the counter counts itself retired now (it
+    // has read the ticket tag); a fetching one right after its last fetch --
+    // both off the kernel's tail
+    if (tid == 0 && p.retire && !fetcher) retire_cta(p, c->epoch);
     // peers' barriers must exist before a commit signal or a remote arrive reaches
     // them: warps that reach into peers (all of a pair; the epilogue of a
     // cluster split) wait here, the others only at teardown
@@ -969,6 +975,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 // a unit without k-blocks (an empty expert's zero tile) fetches here
                 if (!fetched && ok) nxt = atomicAdd(p.sched, 1);
             }
+            // the counter's last use by this CTA is behind it
+            if (fetcher && p.retire) retire_cta(p, c->epoch);
             if (!ok) {
                 // drain: the most recent issue into each stage must land before exit
                 const int64_t n = issued < p.stages ? issued : p.stages;
@@ -1495,7 +1503,6 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         tc_fence_after_sync();
         tmem_dealloc<2>(tmem_base, uint32_t(p.tmem_cols));
     }
-    if (p.retire && tid == 0) retire_cta(p, c->epoch);
 }
 
 }  // namespace cakegg
