@@ -378,6 +378,26 @@ int encode_stacked(CUtensorMap *m, const void *base, uint64_t rows, uint64_t wid
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Clusters of S pairs (2 S CTAs, 192 threads, one CTA per SM) resident at
+// once on a 152-SM part (measured with cudaOccupancyMaxActiveClusters: the
+// GPCs do not divide into whole clusters of 4, 6 or 8).
+int resident_pair_clusters(int S)
+{
+    return S == 2 ? 36 : S == 3 ? 23 : S == 4 ? 15 : 0;
+}
+
+// A cluster split: swapped single CTAs (a receive buffer of their own), or
+// pairs of at most 256-column tiles whose receive buffer fits their ring (the
+// cluster, 2 CTAs per split, within the portable size).
+bool cluster_split_fits(const cake_gg_plan_t &pl)
+{
+    const int S = pl.cluster_splits;
+    if (pl.swap_ab) return pl.pair == 1 && S <= kMaxClusterSplit;
+    return pl.pair == 2 && pl.tile_n <= 256 && 2 * S <= kMaxClusterSplit &&
+           pair_csplit_ring_bytes(pl.tile_n, S, pl.out_dtype == CAKE_GG_FP32) <=
+               size_t(pl.stages) * stage_bytes_for(pl.tile_n, pl.tile_k / 64, 2);
+}
+
 // Checks shared by the three compute calls.
 int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *b, void *out,
                const int32_t *offsets, int out_dtype, int deterministic, void *ws, size_t ws_bytes)
@@ -397,7 +417,7 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
         (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
         plan->cluster_splits > kMaxClusterSplit ||
-        (plan->cluster_splits > 0 && (pass != CAKE_GG_WGRAD || !plan->swap_ab || plan->pair != 1)) ||
+        (plan->cluster_splits > 0 && (pass != CAKE_GG_WGRAD || plan->split_chunk > 0 || !cluster_split_fits(*plan))) ||
         plan->tail_units < 0 || plan->tail_splits < 0 || plan->tail_splits == 1 || plan->tail_splits > kMaxTailSplits ||
         (plan->tail_splits > 1 && (pass != CAKE_GG_WGRAD || plan->swap_ab || plan->split_chunk > 0 ||
                                    plan->cluster_splits > 0)) ||
@@ -580,7 +600,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
     const int P = plan->pair;
-    const int CL = p.csplit > 0 ? p.csplit : P;   // CTAs per cluster (one unit per cluster)
+    const int CL = P * (p.csplit > 0 ? p.csplit : 1);   // CTAs per cluster (one unit per cluster)
     const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk, p.csplit, 0, 0, p.sk);
     uint64_t unit_bound;
     if (mode == kModeWgrad && p.sk > 0) {
@@ -842,6 +862,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // deeper stages only while at least two of them fit
     while (bk > 64 && smem_bytes_for(bn, 2, bk / 64, 1, 0, plan->pair, E) > kSmemLimit) bk /= 2;
     plan->tile_k = bk;
+    const int env_cs = env_int("CAKE_GG_CSPLIT", -1);
     if (pass == CAKE_GG_WGRAD) {
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, plan->swap_ab, 0);
         const int64_t tpe = int64_t(g.m_tiles_w) * g.n_tiles;
@@ -867,7 +888,6 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
                 plan->split_chunk = 0;
             }
         }
-        const int env_cs = env_int("CAKE_GG_CSPLIT", -1);
         if (env_cs == 0 && plan->cluster_splits > 0) {
             plan->split_chunk = int32_t(((M_max / E + bk - 1) / bk + plan->cluster_splits - 1) / plan->cluster_splits);
             plan->cluster_splits = 0;
@@ -928,6 +948,30 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     const int env_st = env_int("CAKE_GG_STAGES", 0);
     if (env_st >= 2 && env_st <= stages) stages = env_st;
     plan->stages = stages;
+
+    // pairs reduce a split tile on chip too when the clusters of all tiles (2
+    // CTAs per split) are resident at once: a tile's split pairs form one
+    // cluster, sum their partials through distributed shared memory into their
+    // operand rings and store the tile once (no workspace partials, tickets or
+    // finish) -- automatically for one expert and a planned split;
+    // CAKE_GG_CSPLIT = S forces it
+    const char *env_chunk = std::getenv("CAKE_GG_SPLIT_CHUNK");
+    const bool auto_cs = E == 1 && !(env_chunk && *env_chunk) && env_cs != 0 && plan->split_chunk > 0 &&
+                         plan->tail_splits == 0 && plan->streamk_kblocks == 0;
+    if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->pair == 2 && bn <= 256 && (auto_cs || env_cs >= 2)) {
+        const int64_t kbe = (M_max / E + bk - 1) / bk;
+        const int64_t S = env_cs >= 2 ? env_cs : (kbe + plan->split_chunk - 1) / plan->split_chunk;
+        const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, 0, 0, 2, bk);
+        const int64_t units = int64_t(m_units_w(g)) * g.n_tiles * E;
+        if (S >= 2 && 2 * S <= kMaxClusterSplit && (units <= resident_pair_clusters(int(S)) || env_cs >= 2)) {
+            const cake_gg_plan_t keep = *plan;
+            plan->cluster_splits = int32_t(S);
+            plan->split_chunk = 0;
+            plan->tail_units = plan->tail_splits = 0;
+            plan->streamk_kblocks = 0;
+            if (!cluster_split_fits(*plan)) *plan = keep;
+        }
+    }
 
     const WsLayout w = ws_layout(*plan);
     if (!w.ok) return CAKE_GG_ERR_OVERFLOW;
@@ -1041,7 +1085,7 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
     int64_t n = 0;
     for (int64_t tt = 0; tt < units; ++tt) {
         const int64_t t = g.sk > 0 ? sk_ids[size_t(tt)] : tt;
-        const int ranks = g.csplit > 0 ? g.csplit : g.pair;
+        const int ranks = g.pair * (g.csplit > 0 ? g.csplit : 1);
         for (int r = 0; r < ranks; ++r) {
             const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data(), r);
             if (!ti.valid) continue;

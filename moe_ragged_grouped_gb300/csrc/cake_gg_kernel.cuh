@@ -97,7 +97,9 @@ struct __align__(16) Ctrl {
     uint64_t conv[kMaxStages];  // router: the stage's A tile is split into BF16 hi | lo (both CTAs of a pair)
     uint64_t drain;
     uint64_t red_ready;     // cluster split: every split's part of this CTA's slice has arrived
-    uint64_t red_consumed;  // cluster split: every peer has read this CTA's partial
+    uint64_t red_consumed;  // cluster split: every peer has read this CTA's partial (pairs: every
+                            // owner's ring is free for this tile's parts)
+    uint64_t ring_free;     // cluster split of pairs: this CTA's slice is summed, its ring free for copies
     uint64_t uq_full[kUQ];  // unit queue slot written (by the even CTA's producer)
     uint64_t uq_empty[kUQ]; // (even CTA) every role of the cluster has read the slot
     int64_t uq[kUQ];        // unit ids, -1 = no more
@@ -131,17 +133,33 @@ __host__ __device__ constexpr uint32_t stage_bytes_for(int bn, int kps = 1, int 
 
 // Cluster split: the receive buffer of this CTA's slice of a tile's float4
 // columns, one copy per split (S x ceil(cols4 / S) <= cols4 + S - 1 columns of
-// 128 rows x 16 bytes).
-__host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit)
+// 128 rows x 16 bytes).  Pairs receive into their operand ring instead (idle
+// between a tile's last MMA and the next tile's first copy).
+__host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit, int pair = 1)
 {
-    return csplit > 0 ? size_t(kTileM) * 16u * size_t(bn / 4 + csplit) : 0u;
+    return csplit > 0 && pair == 1 ? size_t(kTileM) * 16u * size_t(bn / 4 + csplit) : 0u;
+}
+
+// Cluster split of pairs: float4 columns of a tile's slice owned by one split
+// (whole 128-byte output rows per owner: 8 float4 columns for FP32, 16 for BF16)
+// and the ring bytes it takes: the receive buffer (the S - 1 peers' parts of
+// the slice), then the slice's output staged for TMA stores (per warp, one 4 KB slab of
+// 32 rows x 128 bytes per 128-byte row chunk).
+__host__ __device__ constexpr int pair_csplit_per(int cols4, int csplit, bool out_f32)
+{
+    return ((cols4 + csplit - 1) / csplit + (out_f32 ? 8 : 16) - 1) / (out_f32 ? 8 : 16) * (out_f32 ? 8 : 16);
+}
+__host__ __device__ constexpr size_t pair_csplit_ring_bytes(int bn, int csplit, bool out_f32)
+{
+    return size_t(csplit - 1) * size_t(pair_csplit_per(bn / 4, csplit, out_f32)) * size_t(kTileM) * 16u +
+           4u * size_t(pair_csplit_per(bn / 4, csplit, out_f32) / (out_f32 ? 8 : 16)) * 4096u;
 }
 
 __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps, int staging_bufs, int csplit,
                                                     int pair, int E, bool router = false)
 {
     return 1024 + size_t(stages) * stage_bytes_for(bn, kps, pair, router) + size_t(staging_bufs) * kStagingBytes +
-           csplit_bytes_for(bn, csplit) + sizeof(Ctrl) + tables_bytes_for(E);
+           csplit_bytes_for(bn, csplit, pair) + sizeof(Ctrl) + tables_bytes_for(E);
 }
 
 // Bounded wait on one mbarrier phase, by every lane of the calling warp;
@@ -245,7 +263,8 @@ struct UnitSeq {
 // A consuming warp (MMA / relay, epilogue) takes the next unit; false = none
 // left (or abort: ok = false).
 __device__ __forceinline__ bool warp_next_unit(UnitSeq &u, int64_t unit0, int64_t unit_step, int64_t total,
-                                               bool leader, int lane, Ctrl *c, const KParams &p, bool &ok)
+                                               bool leader, uint32_t lead, int lane, Ctrl *c, const KParams &p,
+                                               bool &ok)
 {
     if (!p.dyn) {
         u.t = u.pos == 0 ? unit0 : u.t + unit_step;
@@ -264,7 +283,7 @@ __device__ __forceinline__ bool warp_next_unit(UnitSeq &u, int64_t unit0, int64_
     __syncwarp();
     if (lane == 0) {
         if (leader) mbar_arrive(smem_u32(&c->uq_empty[slot]));
-        else mbar_arrive_remote(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
+        else mbar_arrive_remote(map_to_cta(smem_u32(&c->uq_empty[slot]), lead));
     }
     ++u.pos;
     return u.t >= 0;
@@ -540,7 +559,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     const uint32_t chunk_b = uint32_t(p.bn / PAIR) * 128u;  // K-major B: one 64-deep chunk of this CTA's rows
     uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
     float *red_buf = reinterpret_cast<float *>(staging + size_t(p.staging_bufs) * kStagingBytes);
-    Ctrl *c = reinterpret_cast<Ctrl *>(reinterpret_cast<uint8_t *>(red_buf) + csplit_bytes_for(p.bn, p.csplit));
+    Ctrl *c = reinterpret_cast<Ctrl *>(reinterpret_cast<uint8_t *>(red_buf) + csplit_bytes_for(p.bn, p.csplit, PAIR));
     int32_t *const t_off = reinterpret_cast<int32_t *>(c + 1);
     int32_t *const t_order = t_off + (p.E + 1);
     int32_t *const t_pref = t_order + p.E;
@@ -550,22 +569,26 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int E = p.E;
-    // (cluster splits exist only for swapped weight gradients: the other
-    // instantiations compile none of that path)
-    const int csplit = MODE == kModeWgrad && SWAP ? p.csplit : 0;
+    // (cluster splits exist only for weight gradients, swapped single CTAs or
+    // pairs: the other instantiations compile none of that path)
+    const int csplit = MODE == kModeWgrad && (SWAP || PAIR == 2) ? p.csplit : 0;
     Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit,
                        MODE == kModeWgrad ? p.tail : 0, MODE == kModeWgrad ? p.tail_s : 0,
                        MODE == kModeWgrad && !SWAP ? p.sk : 0);
-    // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + r
+    // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + h
     // as one 256-row MMA (the even CTA issues it; each CTA holds its A rows and
-    // half of the B tile); a cluster split (csplit CTAs) computes one tile,
-    // rank r taking the r-th chunk of its reduction
-    const int cl = PAIR == 2 ? 2 : (csplit > 0 ? csplit : 1);
+    // half of the B tile); a cluster split (csplit CTAs, or csplit pairs)
+    // computes one tile, split s taking the s-th chunk of its reduction.  A
+    // pair is two CTAs whose cluster ranks differ in bit 0.
+    const int cl = PAIR * (csplit > 0 ? csplit : 1);
     const int rank = cl > 1 ? int(cluster_ctarank()) : 0;
+    const int half = PAIR == 2 ? (rank & 1) : 0;   // this CTA's half of its pair
+    const uint32_t lead = uint32_t(rank - half);  // cluster rank of its pair's even CTA
+    const int srank = rank / PAIR;                // cluster split: this CTA's split
     const int64_t unit0 = blockIdx.x / cl;
     const int64_t unit_step = gridDim.x / cl;
-    constexpr uint16_t kPairMask = 0x3;
-    const bool leader = PAIR == 1 || rank == 0;     // issues the MMAs (and owns full / tempty)
+    const uint16_t pair_mask = uint16_t(0x3u << lead);
+    const bool leader = PAIR == 1 || half == 0;     // issues the MMAs (and owns full / tempty)
 
     // ---- setup, part 1: TMEM, barriers and tensor maps (no global loads) ----
     // runs while the previous kernel in the stream may still be finishing; the
@@ -587,9 +610,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         for (int s = 0; s < p.stages; ++s) {
             // the even CTA of a pair also counts its peer's "stage loaded" relay
             // (router: the relay is the peer converters' "stage split" on conv)
-            mbar_init(smem_u32(&c->full[s]), PAIR == 2 && rank == 0 && !RT ? 2u : 1u);
+            mbar_init(smem_u32(&c->full[s]), PAIR == 2 && leader && !RT ? 2u : 1u);
             mbar_init(smem_u32(&c->empty[s]), 1);
-            if (RT) mbar_init(smem_u32(&c->conv[s]), PAIR == 2 && rank == 0 ? 2u : 1u);
+            if (RT) mbar_init(smem_u32(&c->conv[s]), PAIR == 2 && leader ? 2u : 1u);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c->tfull[a]), 1);
@@ -603,8 +626,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             mbar_init(smem_u32(&c->uq_empty[i]), (PAIR == 2 ? 11u : 5u) + (RT ? 4u * PAIR : 0u));
         }
         if (csplit > 0) {
-            mbar_init(smem_u32(&c->red_ready), 1u);   // this CTA's arrival; the peers' bytes as tx
+            // single CTAs: this CTA's arrival, the peers' bytes as tx; pairs: this
+            // CTA's arrival and one release arrival per pushing thread of every peer
+            mbar_init(smem_u32(&c->red_ready), PAIR == 2 ? 1u + uint32_t(csplit - 1) * 128u : 1u);
             mbar_init(smem_u32(&c->red_consumed), uint32_t(csplit));
+            mbar_init(smem_u32(&c->ring_free), 1u);
         }
         fence_barrier_init();
     }
@@ -807,6 +833,13 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     us.t = t;
                     ++us.pos;
                     if (t >= total) break;
+                    // cluster split of pairs: the previous tile's parts were received
+                    // in this ring; its copies wait until that slice is summed
+                    if (PAIR == 2 && csplit > 0 && us.pos > 1 &&
+                        !thread_wait(smem_u32(&c->ring_free), uint32_t((us.pos - 2) & 1), c, p, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
                 } else if (leader) {
                     // fetch: publish the unit to every role of the cluster
                     const int slot = int(us.pos % kUQ);
@@ -833,8 +866,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     // the odd CTA's slot: data and signal in one asynchronous store
                     // (that CTA armed its barrier for these 8 bytes)
                     if (PAIR == 2)
-                        st_async_b64(map_to_cta(smem_u32(&c->uq[slot]), 1), t,
-                                     map_to_cta(smem_u32(&c->uq_full[slot]), 1));
+                        st_async_b64(map_to_cta(smem_u32(&c->uq[slot]), lead + 1u), t,
+                                     map_to_cta(smem_u32(&c->uq_full[slot]), lead + 1u));
                     ++us.pos;
                     if (t < 0) break;
                 } else {
@@ -850,7 +883,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     }
                     t = *reinterpret_cast<volatile int64_t *>(&c->uq[slot]);
                     if (t >= 0) mbar_arrive_expect_tx(smem_u32(&c->uq_full[slot]), 8u);
-                    mbar_arrive_remote(map_to_cta(smem_u32(&c->uq_empty[slot]), 0));
+                    mbar_arrive_remote(map_to_cta(smem_u32(&c->uq_empty[slot]), lead));
                     ++us.pos;
                     if (t < 0) break;
                 }
@@ -880,8 +913,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     if (!drop) {
                         // B atoms this CTA loads: all of them, or its half of a pair's
                         const int nb = p.bn / 64;
-                        const int jb0 = PAIR == 2 ? rank * nb / 2 : 0;
-                        const int jb1 = PAIR == 2 ? (rank + 1) * nb / 2 : nb;
+                        const int jb0 = PAIR == 2 ? half * nb / 2 : 0;
+                        const int jb1 = PAIR == 2 ? (half + 1) * nb / 2 : nb;
                         // (the router staggers each unit's k order: with one output-column
                         // tile every pair reads the same weight slices, and in lock step
                         // they would all read the same lines at once)
@@ -911,8 +944,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                             if (p.stack_b && p.bn > 256) {
                                 // a 512-wide tile: this CTA's half of each 256-column MMA tile
                                 const int hb = 256 / 64 / PAIR;   // atoms per half per CTA
-                                tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + rank * hb);
-                                tma_load_3d(sb + uint32_t(hb) * atom_b, &mapB, fb, 0, r, ti.nt * nb + 4 + rank * hb);
+                                tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + half * hb);
+                                tma_load_3d(sb + uint32_t(hb) * atom_b, &mapB, fb, 0, r, ti.nt * nb + 4 + half * hb);
                             } else if (p.stack_b) {
                                 tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + jb0);
                             } else {
@@ -931,7 +964,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                                 tma_prefetch_l2_2d(&mapA, k0 + p.prefetch * 64, ti.row0);
                                 tma_prefetch_l2_2d(&mapA, k0 + p.prefetch * 64 + 32, ti.row0);
                             }
-                            const int32_t wrow = ti.nt * p.bn + rank * (p.bn / PAIR);
+                            const int32_t wrow = ti.nt * p.bn + half * (p.bn / PAIR);
                             tma_load_3d(sb, &mapB, fb, k0, wrow, 0);
                             tma_load_3d(sb + uint32_t(p.bn / PAIR) * 128u, &mapB, fb, p.K + k0, wrow, 0);
                         } else {
@@ -941,12 +974,12 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                             if (MODE == kModeFwd && p.bn > 256) {
                                 // a 512-wide tile: this CTA's half of each 256-row W block
                                 // (K-major: 256 / PAIR rows of 128 bytes per block)
-                                const int32_t wrow = ti.nt * p.bn + rank * (256 / PAIR);
+                                const int32_t wrow = ti.nt * p.bn + half * (256 / PAIR);
                                 tma_load_3d(sb, &mapB, fb, k0, wrow, ti.e);
                                 tma_load_3d(sb + uint32_t(256 / PAIR) * 128u, &mapB, fb, k0, wrow + 256, ti.e);
                             } else if (MODE == kModeFwd) {
                                 // this CTA's rows of the W tile: all bn, or its half of a pair's
-                                const int32_t wrow = ti.nt * p.bn + rank * (p.bn / PAIR);
+                                const int32_t wrow = ti.nt * p.bn + half * (p.bn / PAIR);
                                 if (p.chunk_b)
                                     tma_load_4d(sb, &mapB, fb, 0, wrow, kb * kps, ti.e);
                                 else
@@ -954,8 +987,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                             } else if (p.stack_b && p.bn > 256) {
                                 // a 512-wide tile: this CTA's half of each 256-column MMA tile
                                 const int hb = 256 / 64 / PAIR;
-                                tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb + rank * hb, ti.e);
-                                tma_load_4d(sb + uint32_t(hb) * atom_b, &mapB, fb, 0, k0, ti.nt * nb + 4 + rank * hb,
+                                tma_load_4d(sb, &mapB, fb, 0, k0, ti.nt * nb + half * hb, ti.e);
+                                tma_load_4d(sb + uint32_t(hb) * atom_b, &mapB, fb, 0, k0, ti.nt * nb + 4 + half * hb,
                                             ti.e);
                             } else if (p.stack_b) {
                                 // W as {64, N, K/64, E}: this CTA's atoms of one bk-row block in one box
@@ -999,7 +1032,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         int it = 0;
         bool ok = true;
         bool any_mma = false;
-        for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, ok); ++it) {
+        for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lead, lane, c, p, ok); ++it) {
             const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
             const int acc = nacc == 2 ? (it & 1) : 0;
@@ -1070,12 +1103,12 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         else if (kps == 2) issue_stage_mmas<2, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                         else issue_stage_mmas<4, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc, first, chunk_b);
                         // the stage is free again in both CTAs once these MMAs complete
-                        if (PAIR == 2) umma_commit_mc<2>(smem_u32(&c->empty[stage]), kPairMask);
+                        if (PAIR == 2) umma_commit_mc<2>(smem_u32(&c->empty[stage]), pair_mask);
                         else umma_commit<1>(smem_u32(&c->empty[stage]));
                     }
                     any_mma = true;
                 } else if (lane == 0 && !RT) {
-                    mbar_arrive_remote(map_to_cta(smem_u32(&c->full[stage]), 0));
+                    mbar_arrive_remote(map_to_cta(smem_u32(&c->full[stage]), lead));
                 }
                 __syncwarp();
                 if (++stage == p.stages) {
@@ -1085,7 +1118,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             }
             if (!ok) break;
             if (leader && lane == 0) {
-                if (PAIR == 2) umma_commit_mc<2>(smem_u32(&c->tfull[acc]), kPairMask);
+                if (PAIR == 2) umma_commit_mc<2>(smem_u32(&c->tfull[acc]), pair_mask);
                 else umma_commit<1>(smem_u32(&c->tfull[acc]));
             }
             __syncwarp();
@@ -1111,7 +1144,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         // peers may push into it) and whether this CTA has armed it
         uint32_t cs_expect = 0;
         bool cs_open = false, cs_armed = false;
-        for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, qok); ++it) {
+        for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lead, lane, c, p, qok); ++it) {
             const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
             const int acc = nacc == 2 ? (it & 1) : 0;
@@ -1150,10 +1183,12 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             if (cols_valid > p.bn) cols_valid = p.bn;
             const bool row_ok = lrow < rows_valid;
             // cluster split: this CTA's float4 columns [q0, q1) of the tile's nq
+            // (pairs: whole 128-byte output rows per owner, stored by TMA)
             const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
-            const int per_c = csplit > 0 ? (nq + csplit - 1) / csplit : 1;
+            const int per_c = csplit > 0 ? (PAIR == 2 ? pair_csplit_per(nq, csplit, OUT_F32) : (nq + csplit - 1) / csplit)
+                                         : 1;
             const int per = per_c > 0 ? per_c : 1;   // (>= 1: also keeps pruned code free of a zero divisor)
-            const int q0 = rank * per;
+            const int q0 = srank * per;
             const int q1 = q0 + per < nq ? q0 + per : nq;
             if (csplit > 0) {
                 cs_expect = uint32_t(csplit - 1) * uint32_t(q1 > q0 ? q1 - q0 : 0) * kTileM * 16u;
@@ -1169,23 +1204,190 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
 
             if (csplit > 0) {
                 // ---- cluster split: partial slices pushed to their owners, summed there ----
-                // CTA r of the cluster owns float4 columns [r per, (r + 1) per) of the
-                // tile.  Every CTA pushes its partial's part of each slice into the
-                // owner's receive buffer rec[s][q][row] (s = the pushing CTA's split)
-                // with st.async, counted in bytes on the owner's red_ready; the owner
-                // sums rec[0 .. S-1] in split order and stores its slice.  Before
-                // pushing a tile's slices a CTA waits until every owner has summed
-                // the previous tile's (red_consumed).
-                if (cs_it > 0) {
-                    bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t((cs_it - 1) & 1), c, p);
+                // Split s of the cluster owns float4 columns [s per, (s + 1) per) of the
+                // tile (in a pair, of its half's 128 rows); the owner sums every
+                // split's part of its slice in split order and stores it.
+                // Single CTAs: every CTA pushes its partial's part of each slice into
+                // the owner's receive buffer rec[s][q][row] (s = the pushing CTA's
+                // split; the owner writes its own part too) with st.async, counted in
+                // bytes on the owner's red_ready; before pushing a tile's slices a CTA
+                // waits until every owner has summed the previous tile's
+                // (red_consumed).
+                // Pairs receive into their operand ring: an owner arms its receive
+                // phase and signals red_consumed once its pair's MMAs of the tile
+                // are complete (this CTA's tfull), pushers wait for every owner's
+                // signal, and the owner's producer copies the next tile into the ring
+                // only after the slice is summed (ring_free).
+                constexpr bool kRing = PAIR == 2;
+                uint8_t *rec = kRing ? ring : reinterpret_cast<uint8_t *>(red_buf);
+                const uint32_t rec_u32 = smem_u32(rec);
+                if (kRing) {
+                    if (etid == 0) {
+                        mbar_arrive(smem_u32(&c->red_ready));
+                        for (int j = 0; j < csplit; ++j)
+                            mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_consumed), uint32_t(j * PAIR + half)));
+                    }
+                    cs_armed = true;
+                    bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t(cs_it & 1), c, p);
                     if (!named_bar_and(1, 128, okc)) break;
+                    // Pairs: each owner's slice of the other splits' partials goes out
+                    // straight from TMEM (whole 32-column chunks: per is a multiple of 8)
+                    // as plain stores into the owner's ring, rec[s'][q - q_owner][row]
+                    // with s' the pusher's split among the owner's S - 1 peers; the
+                    // owner's own part stays in TMEM until its sum.
+                    for (int o = 0; o < csplit; ++o) {
+                        if (o == srank) continue;
+                        const int qa = o * per;
+                        const int qb = qa + per < nq ? qa + per : nq;
+                        const int slot = srank < o ? srank : srank - 1;
+                        const uint32_t rbase = map_to_cta(
+                            rec_u32 + uint32_t((slot * per * kTileM + lrow) * 16), uint32_t(o * PAIR + half));
+                        for (int qc = qa; qc < qb; qc += 16) {   // two 32-column chunks per TMEM wait
+                            uint32_t r0[32], r1[32];
+                            const bool two = qc + 8 < qb;
+                            if (empty_tile) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                            } else {
+                                tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc), r0);
+                                if (two) tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc + 32), r1);
+                                tmem_ld_wait();
+                            }
+#pragma unroll
+                            for (int j4 = 0; j4 < 16; ++j4) {
+                                const uint32_t *rr = j4 < 8 ? r0 : r1;
+                                const int jj = j4 & 7;
+                                if (qc + j4 < qb)
+                                    st_cluster_v4(rbase + uint32_t((qc + j4 - qa) * kTileM * 16),
+                                                  make_float4(__uint_as_float(rr[4 * jj]), __uint_as_float(rr[4 * jj + 1]),
+                                                              __uint_as_float(rr[4 * jj + 2]),
+                                                              __uint_as_float(rr[4 * jj + 3])));
+                            }
+                        }
+                    }
+                    // plain stores, made visible by one release arrival per thread on
+                    // every other owner (fewer barrier updates than a byte count per store)
+                    for (int j = 0; j < csplit; ++j)
+                        if (j != srank)
+                            mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), uint32_t(j * PAIR + half)));
+                    bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
+                    if (!named_bar_and(1, 128, okr)) break;
+                    cs_open = false;   // every peer's part of the slice has landed
+                    // My slice, summed over the splits in split order (s = 0, 1, ..., S - 1;
+                    // this CTA's own part from TMEM), staged per warp in the ring after the
+                    // receive buffer as 4 KB slabs (32 rows x one 128-byte output row chunk)
+                    // whose TMA stores go out back to back.
+                    constexpr int CW = OUT_F32 ? 32 : 64;   // columns per 128-byte output row
+                    constexpr int C4 = CW / 4;
+                    const uint32_t ostg = rec_u32 + uint32_t(csplit - 1) * uint32_t(per) * kTileM * 16u +
+                                          uint32_t(q) * uint32_t(per / C4) * 4096u;
+                    const bool stage_out = p.tma_store && ti.valid && q * 32 < rows_valid;
+                    for (int qc = q0; qc < q1; qc += C4) {
+                        // this CTA's own part of the row chunk, from TMEM
+                        uint32_t own[CW];
+                        if (empty_tile) {
+#pragma unroll
+                            for (int j = 0; j < CW; ++j) own[j] = 0u;
+                        } else {
+                            tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc), *reinterpret_cast<uint32_t(*)[32]>(own));
+                            if (CW == 64)
+                                tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc + 32),
+                                                   *reinterpret_cast<uint32_t(*)[32]>(own + (CW == 64 ? 32 : 0)));
+                            tmem_ld_wait();
+                        }
+                        const int col = qc * 4;
+                        const bool live = ti.valid && col < cols_valid;
+                        uint32_t w[32];   // the chunk's 128-byte output row
+                        const uint32_t src0 = rec_u32 + uint32_t(((qc - q0) * kTileM + lrow) * 16);
+#pragma unroll
+                        for (int j = 0; j < C4; ++j) {
+                            float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            if (qc + j < q1) {
+                                const float4 mine = make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                                                __uint_as_float(own[4 * j + 2]),
+                                                                __uint_as_float(own[4 * j + 3]));
+#pragma unroll
+                                for (int sp = 0; sp < 4; ++sp) {   // (at most 4 splits of pairs in a cluster of 8)
+                                    if (sp < csplit) {
+                                        const int sl = sp < srank ? sp : sp - 1;
+                                        const float4 b =
+                                            sp == srank ? mine
+                                                        : lds_v4(src0 + uint32_t(j * kTileM * 16) +
+                                                                 uint32_t(sl) * uint32_t(per) * kTileM * 16u);
+                                        if (sp == 0) {
+                                            a = b;
+                                        } else {
+                                            a.x += b.x;
+                                            a.y += b.y;
+                                            a.z += b.z;
+                                            a.w += b.w;
+                                        }
+                                    }
+                                }
+                            }
+                            if (OUT_F32) {
+                                w[4 * j] = __float_as_uint(a.x);
+                                w[4 * j + 1] = __float_as_uint(a.y);
+                                w[4 * j + 2] = __float_as_uint(a.z);
+                                w[4 * j + 3] = __float_as_uint(a.w);
+                            } else {
+                                w[2 * j] = pack_bf16x2(a.x, a.y);
+                                w[2 * j + 1] = pack_bf16x2(a.z, a.w);
+                            }
+                            // (no TMA stores: each float4 column straight to its row)
+                            if (!p.tma_store && live && row_ok && qc + j < q1 && col + 4 * j < cols_valid) {
+                                const int64_t o = out_base + int64_t(lrow) * ld + col + 4 * j;
+                                if (OUT_F32)
+                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o) = a;
+                                else
+                                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + o) =
+                                        make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+                            }
+                        }
+                        if (stage_out && live) {
+                            // a 4 KB slab: 32 rows x 128 bytes, 128-byte swizzle (rows past the
+                            // output and columns past the slice's end are clipped by the map)
+                            const uint32_t slab = ostg + uint32_t((qc - q0) / C4) * 4096u;
+                            const uint32_t rowp = slab + uint32_t(lane) * 128u;
+#pragma unroll
+                            for (int ch = 0; ch < 8; ++ch)
+                                sts_v4(rowp + uint32_t((ch ^ (lane & 7)) << 4), w[4 * ch], w[4 * ch + 1], w[4 * ch + 2],
+                                       w[4 * ch + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&mapOut, slab, ti.nt * p.bn + col, ti.mt * kTileM + q * 32, ti.e);
+                                bulk_commit_group();
+                            }
+                            __syncwarp();
+                        }
+                    }
+                    // the accumulator is read: free for the MMA warp (of the even CTA)
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader) mbar_arrive(smem_u32(&c->tempty[acc]));
+                        else mbar_arrive_remote(map_to_cta(smem_u32(&c->tempty[acc]), lead));
+                    }
+                    // the slice is read and the slabs' stores have read them: the ring
+                    // takes the next tile's copies
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
+                    if (etid == 0) mbar_arrive(smem_u32(&c->ring_free));
+                    ++cs_it;
+                    continue;
+                } else {
+                    if (cs_it > 0) {
+                        bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t((cs_it - 1) & 1), c, p);
+                        if (!named_bar_and(1, 128, okc)) break;
+                    }
+                    // this CTA's arrival on its own red_ready, expecting the other splits' bytes
+                    if (etid == 0) mbar_arrive_expect_tx(smem_u32(&c->red_ready), cs_expect);
+                    cs_armed = true;
                 }
                 // only the float4 columns that reach the output travel
-                uint8_t *rec = reinterpret_cast<uint8_t *>(red_buf);
-                const uint32_t rec_u32 = smem_u32(rec);
-                // this CTA's arrival on its own red_ready, expecting the other splits' bytes
-                if (etid == 0) mbar_arrive_expect_tx(smem_u32(&c->red_ready), cs_expect);
-                cs_armed = true;
                 for (int c0 = 0; c0 < 4 * nq; c0 += 32) {
                     float v[32];
                     if (empty_tile) {
@@ -1198,24 +1400,35 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                     }
+                    // owner of the chunk's first float4 column and its place in that
+                    // owner's slice: one division per 32 columns, then counting
+                    int owner = (c0 >> 2) / per;
+                    int rel = (c0 >> 2) - owner * per;
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         const int qi = (c0 >> 2) + j4;   // float4 column of the tile
                         if (qi < nq) {
-                            const int owner = qi / per;
-                            const uint32_t off = uint32_t(((rank * per + qi - owner * per) * kTileM + lrow) * 16);
+                            const uint32_t off = uint32_t(((srank * per + rel) * kTileM + lrow) * 16);
                             const float4 x = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
-                            if (owner == rank)
+                            const uint32_t dst = uint32_t(owner * PAIR + half);   // the owner's CTA of this half
+                            if (owner == srank)
                                 *reinterpret_cast<float4 *>(rec + off) = x;
                             else
-                                st_async_v4(map_to_cta(rec_u32 + off, uint32_t(owner)), x,
-                                            map_to_cta(smem_u32(&c->red_ready), uint32_t(owner)));
+                                st_async_v4(map_to_cta(rec_u32 + off, dst), x,
+                                            map_to_cta(smem_u32(&c->red_ready), dst));
+                        }
+                        if (++rel == per) {
+                            rel = 0;
+                            ++owner;
                         }
                     }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&c->tempty[acc]));
+                if (lane == 0) {
+                    if (leader) mbar_arrive(smem_u32(&c->tempty[acc]));
+                    else mbar_arrive_remote(map_to_cta(smem_u32(&c->tempty[acc]), lead));
+                }
                 named_bar_sync(1, 128);   // this CTA's own part of its slice is in place
                 bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
                 if (!named_bar_and(1, 128, okr)) break;
@@ -1225,12 +1438,15 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 for (int q = q0; q < q1; ++q) {
                     const uint8_t *src = rec + (size_t(q - q0) * kTileM + lrow) * 16;
                     float4 a = *reinterpret_cast<const float4 *>(src);
-                    for (int sp = 1; sp < csplit; ++sp) {
-                        const float4 b = *reinterpret_cast<const float4 *>(src + size_t(sp) * per * kTileM * 16);
-                        a.x += b.x;
-                        a.y += b.y;
-                        a.z += b.z;
-                        a.w += b.w;
+#pragma unroll
+                    for (int sp = 1; sp < 8; ++sp) {   // (at most 8 splits in a cluster)
+                        if (sp < csplit) {
+                            const float4 b = *reinterpret_cast<const float4 *>(src + size_t(sp) * per * kTileM * 16);
+                            a.x += b.x;
+                            a.y += b.y;
+                            a.z += b.z;
+                            a.w += b.w;
+                        }
                     }
                     const int col = q * 4;
                     if (row_ok && ti.valid && col < cols_valid) {
@@ -1342,7 +1558,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             __syncwarp();
             if (lane == 0) {
                 if (leader) mbar_arrive(smem_u32(&c->tempty[acc]));
-                else mbar_arrive_remote(map_to_cta(smem_u32(&c->tempty[acc]), 0));
+                else mbar_arrive_remote(map_to_cta(smem_u32(&c->tempty[acc]), lead));
             }
 
             if (split) {
@@ -1411,13 +1627,14 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 }
             }
         }
-        if (csplit > 0 && cs_open && etid == 0) {
+        if (csplit > 0 && cs_open && etid == 0 && (PAIR == 1 || cs_armed)) {
             // left on an abort while a tile's receive phase was open: peers may
             // have pushed (or be pushing) their parts of this CTA's slice, and
             // asynchronous stores into it must land before the CTA retires.  Arm
             // the phase if this CTA had not, then wait for it with a short limit
             // (a peer that gave up before pushing never completes it; a peer
-            // pushes all of its parts of a tile or none).
+            // pushes all of its parts of a tile or none).  Pairs push only after
+            // the owner armed and signalled.
             if (!cs_armed) mbar_arrive_expect_tx(smem_u32(&c->red_ready), cs_expect);
             drain_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), 2000000ull);
         }
@@ -1435,7 +1652,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lane, c, p, ok);) {
+        for (UnitSeq us{0, 0}; ok && warp_next_unit(us, unit0, unit_step, total, leader, lead, lane, c, p, ok);) {
             const Tile ti = decode_tile(g, us.t, t_off, t_order, t_pref, t_spref, rank);
             for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                 if (!warp_wait(smem_u32(&c->full[stage]), phase, c, p)) {
@@ -1471,7 +1688,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 named_bar_sync(2, 128);
                 if (warp == 6 && lane == 0) {
                     if (leader) mbar_arrive(smem_u32(&c->conv[stage]));
-                    else mbar_arrive_cluster(map_to_cta(smem_u32(&c->conv[stage]), 0));
+                    else mbar_arrive_cluster(map_to_cta(smem_u32(&c->conv[stage]), lead));
                 }
                 if (++stage == p.stages) {
                     stage = 0;

@@ -37,8 +37,8 @@ cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
         attr_set[dev] = true;
     }
     if (smem > kSmemOptInLimit) return cudaErrorInvalidValue;
-    // clusters: a CTA pair, or the CTAs of a cluster split
-    const int cluster = PAIR == 2 ? 2 : (p.csplit > 0 ? p.csplit : 1);
+    // clusters: a CTA pair, the CTAs of a cluster split, or its pairs
+    const int cluster = PAIR * (p.csplit > 0 ? p.csplit : 1);
     if (grid % cluster != 0) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];

@@ -168,6 +168,28 @@ __device__ __forceinline__ void st_shared_cluster_b64(uint32_t cluster_addr, int
 // semantics: a cheap count for pipeline signals whose data is tracked by the
 // barrier itself (TMA bytes, tensor-core commits) rather than by generic
 // stores.
+// Plain 16-byte store into a peer CTA's shared memory (address from mapa); its
+// visibility to the peer comes with a later release arrival of this thread.
+__device__ __forceinline__ void st_cluster_v4(uint32_t remote_addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote_addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// 16-byte shared-memory load / store at a shared-window address.
+__device__ __forceinline__ float4 lds_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

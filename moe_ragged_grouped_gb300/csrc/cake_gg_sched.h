@@ -359,17 +359,19 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
     ti.e = e;
     ti.row_end = r1;
     if (g.mode == kModeWgrad && g.csplit > 0) {
-        // one unit per output tile; cluster rank r takes the r-th of csplit
-        // contiguous k-block chunks (possibly empty for a short expert)
+        // one unit per output tile (per pair tile); cluster rank r is split
+        // s = r / pair, which takes the s-th of csplit contiguous k-block chunks
+        // (possibly empty for a short expert), and half r % pair of a pair
         const int32_t S = g.csplit;
+        const int32_t s = rank / g.pair;
         const int32_t nkb_e = ceil_div_i(r1 - r0, g.bk);
         const int32_t chunk = ceil_div_i(nkb_e, S);
         ti.nt = local % g.n_tiles;
-        ti.mt = local / g.n_tiles;
-        ti.s = rank;
+        ti.mt = (local / g.n_tiles) * g.pair + (rank - s * g.pair);
+        ti.s = s;
         ti.S = S;
-        ti.kb0 = rank * chunk < nkb_e ? rank * chunk : nkb_e;
-        ti.kb1 = (rank + 1) * chunk < nkb_e ? (rank + 1) * chunk : nkb_e;
+        ti.kb0 = s * chunk < nkb_e ? s * chunk : nkb_e;
+        ti.kb1 = (s + 1) * chunk < nkb_e ? (s + 1) * chunk : nkb_e;
         ti.row0 = r0;
         ti.ticket = (e * g.m_tiles_w + ti.mt) * g.n_tiles + ti.nt;
         ti.slot = 0;

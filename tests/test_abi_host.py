@@ -180,6 +180,28 @@ def test_tile_walk_thin_swap():
     assert len(tiles) == 32 * plan.cluster_splits
 
 
+def test_tile_walk_pair_cluster_split():
+    """4096 -> 512 weight gradient at T = 16384: 32 pair tiles of 256 x 256, each split in two
+    by a cluster of two pairs (4 CTAs) that reduces on chip -- every (m-tile, n-tile) once, the
+    two splits contiguous halves of the 128 k-blocks, no workspace partials."""
+    plan, tiles = _check_walk_coverage("wgrad", [16384], N=512, K=4096)
+    assert plan.pair == 2 and plan.cluster_splits == 2 and plan.split_chunk == 0 and plan.swap_ab == 0
+    assert plan.workspace_bytes == 256
+    assert len(tiles) == 4 * 16 * 2
+    assert {(t[5], t[6]) for t in tiles} == {(0, 64), (64, 128)}
+
+
+def test_tile_walk_pair_cluster_split_with_small_and_empty_experts():
+    plan, _ = _check_walk_coverage("wgrad", [0, 100, 3000, 65, 1], N=512, K=512, env={"CAKE_GG_CSPLIT": "3"})
+    assert plan.pair == 2 and plan.cluster_splits == 3
+
+
+def test_pair_cluster_split_needs_every_cluster_resident():
+    # 5120 -> 512: 40 pair tiles, more two-pair clusters than fit at once -> global split slots
+    plan = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
+    assert plan.cluster_splits == 0 and plan.split_chunk > 0
+
+
 def test_tile_walk_cluster_split_with_small_and_empty_experts():
     _check_walk_coverage("wgrad", [0, 100, 3000, 65, 1], N=48, K=512, env={"CAKE_GG_CSPLIT": "4"})
 
@@ -282,7 +304,7 @@ def test_tile_walk_streamk_empty_expert_writes_zero_tiles():
 
 
 @pytest.mark.parametrize("E,M,N,K,od,field,det_value", [
-    (1, 16384, 512, 4096, "fp32", "split_chunk", 64),     # split dropped
+    (1, 16384, 512, 4096, "fp32", "cluster_splits", 2),   # split (on chip, two-pair clusters) dropped
     (1, 16384, 1024, 5120, "fp32", "tail_splits", 8),     # split tail dropped
     (1, 16384, 4096, 4096, "fp32", "tile_n", 512),        # 256 x 512 tiles dropped
     (8, 131072, 4096, 6144, "bf16", "tail_splits", 2),    # split tail dropped

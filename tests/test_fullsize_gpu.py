@@ -247,3 +247,22 @@ def test_split_tail_bitwise_across_sm_caps():
     for cap in (100, 148, 7, 0):
         out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1, max_sms=cap)
         assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"max_sms={cap}"
+
+
+def test_pair_cluster_split_bitwise_across_reductions_and_sm_caps(monkeypatch):
+    """4096 -> 512 at T = 16384: 32 pair tiles, each split in two by a cluster of two pairs that
+    reduces on chip; the same bits as the workspace-slot reduction of the same splits, and under
+    SM caps that leave fewer clusters than tiles."""
+    import torch
+    wk = wl.dense_projection(4096, 512)
+    X, W, G, _ = inputs(wk)
+    offs = torch.from_numpy(wk.offsets).cuda()
+    plan = gg.cake_gg_plan("wgrad", 1, wk.M, wk.N, wk.K, "fp32", 1)
+    assert plan.pair == 2 and plan.cluster_splits == 2
+    ref = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1)
+    for cap in (100, 148, 8):
+        out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1, max_sms=cap)
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"max_sms={cap}"
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "0")
+    slots = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1)
+    assert torch.equal(slots.view(torch.int32), ref.view(torch.int32))

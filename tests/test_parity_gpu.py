@@ -271,6 +271,36 @@ def test_cluster_split_weight_gradient(csplit, det, out_dtype, monkeypatch):
     check_case("wgrad", [0, 100, 3000, 65, 1], 48, 512, out_dtype, det, seed=18, extra_rows=6)
 
 
+@pytest.mark.parametrize("csplit,det,out_dtype", [("2", 1, "fp32"), ("3", 1, "fp32"), ("4", 0, "fp32"),
+                                                  ("2", 0, "bf16"), ("4", 1, "bf16")])
+@pytest.mark.parametrize("max_sms", [0, 8])
+def test_pair_cluster_split_weight_gradient(csplit, det, out_dtype, max_sms, monkeypatch):
+    """Weight gradient of 256-row pair tiles whose splits run as one cluster of pairs and reduce
+    into their operand rings: experts empty, shorter than one stage and long; a partial last
+    column tile (320 = 256 + 64); on 8 SMs one or two clusters take every tile in turn (each
+    tile's copies wait until the previous tile's slice is summed)."""
+    monkeypatch.setenv("CAKE_GG_CSPLIT", csplit)
+    plan = gg.cake_gg_plan("wgrad", 5, 3200, 512, 320, out_dtype, det)
+    assert plan.pair == 2 and plan.cluster_splits == int(csplit)
+    check_case("wgrad", [0, 100, 3000, 65, 1], 512, 320, out_dtype, det, seed=29, extra_rows=6, max_sms=max_sms)
+
+
+@pytest.mark.parametrize("out_dtype", ["fp32", "bf16"])
+def test_pair_cluster_split_bitwise_equal_to_workspace_slots(out_dtype, monkeypatch):
+    """Two splits summed on chip give the bits of the same two splits summed from workspace slots
+    (p0 + p1, one rounding): the reduction's place never changes a result."""
+    import torch
+    Xb, Wb, Gb, off = make_inputs([3000], 512, 512, seed=30, extra_rows=2)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "2")
+    on_chip = run("wgrad", X, W, G, off, out_dtype, 1)
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "0")
+    monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", str(-(-(-(-3000 // 128)) // 2)))
+    slots = run("wgrad", X, W, G, off, out_dtype, 1)
+    i = torch.int32 if out_dtype == "fp32" else torch.int16
+    assert torch.equal(on_chip.view(i), slots.view(i))
+
+
 @pytest.mark.parametrize("det", [1, 0])
 def test_thin_weight_gradient_through_workspace_slots(det, monkeypatch):
     """The same thin shape with the cluster reduction disabled: partials through the workspace."""
