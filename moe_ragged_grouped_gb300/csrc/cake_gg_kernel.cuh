@@ -1299,31 +1299,31 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         const bool live = ti.valid && col < cols_valid;
                         uint32_t w[32];   // the chunk's 128-byte output row
                         const uint32_t src0 = rec_u32 + uint32_t(((qc - q0) * kTileM + lrow) * 16);
+                        const uint32_t sstride = uint32_t(per) * kTileM * 16u;   // between peers' parts
 #pragma unroll
                         for (int j = 0; j < C4; ++j) {
-                            float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                            if (qc + j < q1) {
-                                const float4 mine = make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
-                                                                __uint_as_float(own[4 * j + 2]),
-                                                                __uint_as_float(own[4 * j + 3]));
-#pragma unroll
-                                for (int sp = 0; sp < 4; ++sp) {   // (at most 4 splits of pairs in a cluster of 8)
-                                    if (sp < csplit) {
-                                        const int sl = sp < srank ? sp : sp - 1;
-                                        const float4 b =
-                                            sp == srank ? mine
-                                                        : lds_v4(src0 + uint32_t(j * kTileM * 16) +
-                                                                 uint32_t(sl) * uint32_t(per) * kTileM * 16u);
-                                        if (sp == 0) {
-                                            a = b;
-                                        } else {
-                                            a.x += b.x;
-                                            a.y += b.y;
-                                            a.z += b.z;
-                                            a.w += b.w;
-                                        }
-                                    }
+                            float4 a = make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                                   __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]));
+                            const uint32_t sj = src0 + uint32_t(j * kTileM * 16);
+                            if (csplit == 2) {
+                                // two splits: p0 + p1 == p1 + p0 (one rounding either way)
+                                const float4 b = lds_v4(sj);
+                                a.x += b.x;
+                                a.y += b.y;
+                                a.z += b.z;
+                                a.w += b.w;
+                            } else {
+                                // split order s = 0, 1, ..., S - 1 with this CTA's own part at srank
+                                float4 t = srank == 0 ? a : lds_v4(sj);
+#pragma unroll 1
+                                for (int sp = 1; sp < csplit; ++sp) {
+                                    const float4 b = sp == srank ? a : lds_v4(sj + uint32_t(sp - (sp > srank)) * sstride);
+                                    t.x += b.x;
+                                    t.y += b.y;
+                                    t.z += b.z;
+                                    t.w += b.w;
                                 }
+                                a = t;
                             }
                             if (OUT_F32) {
                                 w[4 * j] = __float_as_uint(a.x);
@@ -1334,14 +1334,19 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                                 w[2 * j] = pack_bf16x2(a.x, a.y);
                                 w[2 * j + 1] = pack_bf16x2(a.z, a.w);
                             }
-                            // (no TMA stores: each float4 column straight to its row)
-                            if (!p.tma_store && live && row_ok && qc + j < q1 && col + 4 * j < cols_valid) {
+                        }
+                        if (!p.tma_store && live && row_ok) {
+                            // no TMA stores: the row chunk's float4 columns straight to its row
+#pragma unroll
+                            for (int j = 0; j < C4; ++j) {
+                                if (qc + j >= q1 || col + 4 * j >= cols_valid) continue;
                                 const int64_t o = out_base + int64_t(lrow) * ld + col + 4 * j;
                                 if (OUT_F32)
-                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o) = a;
+                                    *reinterpret_cast<uint4 *>(static_cast<float *>(p.out) + o) =
+                                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                                 else
                                     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + o) =
-                                        make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+                                        make_uint2(w[2 * j], w[2 * j + 1]);
                             }
                         }
                         if (stage_out && live) {
