@@ -143,7 +143,9 @@ typedef struct cake_gg_plan {
     int32_t streamk_kblocks; /* weight gradient of one expert: > 0 = stream-K walk, the
                                 work cut into segments of this many k-blocks that cross
                                 tile boundaries; a tile's pieces are summed in k order */
-    int32_t reserved[3];
+    int32_t epi_groups;      /* forward / data gradient: 2 = a second epilogue warpgroup
+                                takes every other tile (short reductions); else 1 */
+    int32_t reserved[2];
 } cake_gg_plan_t;
 
 /* Debug flag (tests only): the CTA that takes the walk's first unit (its even

@@ -68,7 +68,8 @@ class CakeGGPlan(ctypes.Structure):
         ("tail_units", ctypes.c_int32),
         ("tail_splits", ctypes.c_int32),
         ("streamk_kblocks", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("epi_groups", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
     def as_dict(self):

@@ -427,7 +427,9 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
           plan->cluster_splits > 0 || plan->tile_n > 256 ||
           int64_t((plan->K + plan->tile_n - 1) / plan->tile_n) * ((plan->M_max + plan->tile_k - 1) / plan->tile_k) >
               (int64_t(1) << 30))) ||
-        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64, plan->staging_bufs, plan->cluster_splits,
+        plan->epi_groups < 0 || plan->epi_groups > 2 || (plan->epi_groups == 2 && pass == CAKE_GG_WGRAD) ||
+        smem_bytes_for(plan->tile_n, plan->stages, plan->tile_k / 64,
+                       plan->staging_bufs * (plan->epi_groups == 2 ? 2 : 1), plan->cluster_splits,
                        plan->pair, plan->E) > kSmemLimit)
         return CAKE_GG_ERR_INVALID_ARG;
     if (plan->N % 8 != 0 || plan->K % 8 != 0) return CAKE_GG_ERR_ALIGNMENT;
@@ -580,6 +582,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.chunk_b = chunk_b ? 1 : 0;
     p.pdl = env_int("CAKE_GG_PDL", 1) != 0 ? 1 : 0;
     p.staging_bufs = plan->staging_bufs;
+    p.epi_groups = mode != kModeWgrad && plan->epi_groups == 2 ? 2 : 1;
     p.csplit = mode == kModeWgrad ? plan->cluster_splits : 0;
     p.debug_flags = plan->debug_flags;
     p.prefetch = mode == kModeWgrad && !plan->swap_ab ? env_int("CAKE_GG_PREFETCH", 0) : 0;
@@ -620,7 +623,7 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     grid -= grid % CL;
     if (grid < CL) grid = CL;
 
-    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs, p.csplit, P, E);
+    const size_t smem = smem_bytes_for(bn, plan->stages, kps, plan->staging_bufs * p.epi_groups, p.csplit, P, E);
     cudaError_t err;
     if (mode == kModeFwd) err = launch_fwd(out_f32, P, ma, mb, mo, p, grid, smem, stream);
     else if (mode == kModeDgrad) err = launch_dgrad(out_f32, P, ma, mb, mo, p, grid, smem, stream);
@@ -662,6 +665,7 @@ int router_plan(cake_gg_plan_t *plan, int64_t T, int32_t R, int32_t K, int32_t m
     if (smem_bytes_for(bn, stages, 1, 1, 0, plan->pair, 1, true) > kSmemLimit) return CAKE_GG_ERR_UNSUPPORTED;
     plan->stages = stages;
     plan->staging_bufs = 1;
+    plan->epi_groups = 1;
     plan->workspace_bytes = kHeaderBytes;
     return CAKE_GG_OK;
 }
@@ -704,6 +708,7 @@ int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, f
     p.epoch_word = reinterpret_cast<uint32_t *>(wsb + kEpochOffset);
     p.pdl = env_int("CAKE_GG_PDL", 1) != 0 ? 1 : 0;
     p.staging_bufs = plan->staging_bufs;
+    p.epi_groups = 1;
     p.debug_flags = plan->debug_flags;
     p.dyn = env_int("CAKE_GG_DYN", 1) != 0 ? 1 : 0;
     p.retire = p.dyn;
@@ -945,6 +950,19 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         }
     }
     plan->staging_bufs = staging_bufs;
+    // the same short reductions: a second epilogue warpgroup takes every other
+    // tile (two accumulators), its own staging buffers at the cost of ring depth
+    plan->epi_groups = 1;
+    const int env_eg = env_int("CAKE_GG_EPI_GROUPS", 0);
+    if (pass != CAKE_GG_WGRAD && bn <= 256 &&
+        (((red_len + bk - 1) / bk <= 4 && env_eg != 1) || env_eg == 2)) {
+        int st2 = stages;
+        while (st2 > 2 && smem_bytes_for(bn, st2, bk / 64, 2 * staging_bufs, csp, pr, E) > kSmemLimit) --st2;
+        if (smem_bytes_for(bn, st2, bk / 64, 2 * staging_bufs, csp, pr, E) <= kSmemLimit) {
+            plan->epi_groups = 2;
+            stages = st2;
+        }
+    }
     const int env_st = env_int("CAKE_GG_STAGES", 0);
     if (env_st >= 2 && env_st <= stages) stages = env_st;
     plan->stages = stages;

@@ -38,9 +38,13 @@ namespace cakegg {
 
 constexpr int kThreads = 192;
 constexpr int kThreadsRouter = 320;   // + 4 converter warps
+constexpr int kThreadsEpi2 = 320;     // forward / data gradient: + a second epilogue warpgroup
 constexpr uint32_t kRouterABytes = kTileM * 64 * 4;   // 32 KB: a 128 x 64 FP32 A tile, later its BF16 hi | lo
 
-__host__ __device__ constexpr int threads_for(int kmode) { return kmode == kModeRouter ? kThreadsRouter : kThreads; }
+__host__ __device__ constexpr int threads_for(int kmode)
+{
+    return kmode == kModeRouter ? kThreadsRouter : kmode == kModeWgrad ? kThreads : kThreadsEpi2;
+}
 constexpr int kMaxStages = 8;
 constexpr int kMaxCsplit = 8;   // largest cluster split (portable cluster size)
 constexpr int kStatusBadOffsets = 7;
@@ -74,6 +78,7 @@ struct KParams {
     int32_t chunk_b;        // K-major B (forward W) through a {64, N, K/64, E} map
     int32_t pdl;            // launched with programmatic stream serialization
     int32_t staging_bufs;   // epilogue staging buffers per warp (1 or 2)
+    int32_t epi_groups;     // forward / data gradient: epilogue warpgroups taking alternate tiles (1 or 2)
     int32_t csplit;         // weight gradient: splits per tile reduced on chip by one cluster (0 = off)
     int32_t debug_flags;
     int32_t prefetch;       // weight gradient: L2 prefetch distance in stages (0 = off)
@@ -558,7 +563,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     const uint32_t atom_b = atom_a;
     const uint32_t chunk_b = uint32_t(p.bn / PAIR) * 128u;  // K-major B: one 64-deep chunk of this CTA's rows
     uint8_t *staging = ring + size_t(p.stages) * stage_bytes;  // 1024-aligned
-    float *red_buf = reinterpret_cast<float *>(staging + size_t(p.staging_bufs) * kStagingBytes);
+    float *red_buf = reinterpret_cast<float *>(staging + size_t(p.staging_bufs) * (p.epi_groups == 2 ? 2 : 1) *
+                                               kStagingBytes);
     Ctrl *c = reinterpret_cast<Ctrl *>(reinterpret_cast<uint8_t *>(red_buf) + csplit_bytes_for(p.bn, p.csplit, PAIR));
     int32_t *const t_off = reinterpret_cast<int32_t *>(c + 1);
     int32_t *const t_order = t_off + (p.E + 1);
@@ -621,9 +627,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         mbar_init(smem_u32(&c->drain), 1);
         for (int i = 0; i < kUQ; ++i) {
             mbar_init(smem_u32(&c->uq_full[i]), 1);
-            // readers of a slot: MMA (or relay) warp, 4 epilogue warps, the
-            // odd CTA's producer in a pair, and the router's 4 converter warps
-            mbar_init(smem_u32(&c->uq_empty[i]), (PAIR == 2 ? 11u : 5u) + (RT ? 4u * PAIR : 0u));
+            // readers of a slot: MMA (or relay) warp, 4 epilogue warps (8 with a
+            // second group), the odd CTA's producer in a pair, and the router's 4
+            // converter warps
+            mbar_init(smem_u32(&c->uq_empty[i]),
+                      (PAIR == 2 ? 11u : 5u) + (RT ? 4u * PAIR : 0u) + (p.epi_groups == 2 ? 4u * PAIR : 0u));
         }
         if (csplit > 0) {
             // single CTAs: this CTA's arrival, the peers' bytes as tx; pairs: this
@@ -1131,10 +1139,17 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             __syncwarp();
         }
     } else if (!RT || warp < 6) {
-        // ======================= epilogue (warps 2..5) =======================
+        // ======================= epilogue (warps 2..5; 6..9) =======================
+        // (forward / data gradient with a short reduction: a second warpgroup,
+        // warps 6..9, takes every other tile -- the odd accumulator -- so two
+        // warps per SM sub-partition overlap the latency of the stores)
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int lrow = q * 32 + lane;    // tile row held by this thread
-        const int etid = tid - 64;         // 0..127
+        const int eg = (warp - 2) >> 2;    // epilogue group
+        const int ngroups = p.epi_groups == 2 && nacc == 2 ? 2 : 1;
+        const uint32_t ebar = eg == 0 ? 1u : 3u;   // the group's named barrier
+        const int etid = (tid - 64) & 127; // 0..127 within the group
+        uint8_t *const stg_base = staging + size_t(eg) * p.staging_bufs * kStagingBytes;
         int it = 0;
         int cs_it = 0;                     // cluster-split tiles reduced so far
         int stg_buf = 0;                   // staging buffer this warp writes next
@@ -1145,6 +1160,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         uint32_t cs_expect = 0;
         bool cs_open = false, cs_armed = false;
         for (UnitSeq us{0, 0}; warp_next_unit(us, unit0, unit_step, total, leader, lead, lane, c, p, qok); ++it) {
+            if (it % ngroups != eg) continue;   // the other group's tile
             const int64_t t = us.t;
             const Tile ti = decode_tile(g, t, t_off, t_order, t_pref, t_spref, rank);
             const int acc = nacc == 2 ? (it & 1) : 0;
@@ -1198,7 +1214,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
 
             // (in a pair the even CTA's MMA commit arrives on both CTAs' tfull)
             bool ok = warp_wait(smem_u32(&c->tfull[acc]), acc_phase, c, p);
-            ok = named_bar_and(1, 128, ok);
+            ok = named_bar_and(ebar, 128, ok);
             if (!ok) break;
             tc_fence_after_sync();
 
@@ -1229,7 +1245,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     }
                     cs_armed = true;
                     bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t(cs_it & 1), c, p);
-                    if (!named_bar_and(1, 128, okc)) break;
+                    if (!named_bar_and(ebar, 128, okc)) break;
                     // Pairs: each owner's slice of the other splits' partials goes out
                     // straight from TMEM (whole 32-column chunks: per is a multiple of 8)
                     // as plain stores into the owner's ring, rec[s'][q - q_owner][row]
@@ -1271,7 +1287,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         if (j != srank)
                             mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), uint32_t(j * PAIR + half)));
                     bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
-                    if (!named_bar_and(1, 128, okr)) break;
+                    if (!named_bar_and(ebar, 128, okr)) break;
                     cs_open = false;   // every peer's part of the slice has landed
                     // My slice, summed over the splits in split order (s = 0, 1, ..., S - 1;
                     // this CTA's own part from TMEM), staged per warp in the ring after the
@@ -1379,14 +1395,14 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     fence_proxy_async_smem();
-                    named_bar_sync(1, 128);
+                    named_bar_sync(ebar, 128);
                     if (etid == 0) mbar_arrive(smem_u32(&c->ring_free));
                     ++cs_it;
                     continue;
                 } else {
                     if (cs_it > 0) {
                         bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t((cs_it - 1) & 1), c, p);
-                        if (!named_bar_and(1, 128, okc)) break;
+                        if (!named_bar_and(ebar, 128, okc)) break;
                     }
                     // this CTA's arrival on its own red_ready, expecting the other splits' bytes
                     if (etid == 0) mbar_arrive_expect_tx(smem_u32(&c->red_ready), cs_expect);
@@ -1434,9 +1450,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     if (leader) mbar_arrive(smem_u32(&c->tempty[acc]));
                     else mbar_arrive_remote(map_to_cta(smem_u32(&c->tempty[acc]), lead));
                 }
-                named_bar_sync(1, 128);   // this CTA's own part of its slice is in place
+                named_bar_sync(ebar, 128);   // this CTA's own part of its slice is in place
                 bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
-                if (!named_bar_and(1, 128, okr)) break;
+                if (!named_bar_and(ebar, 128, okr)) break;
                 cs_open = false;   // every peer's part of the slice has landed
                 // my slice, summed over the splits in split order (s = 0, 1, ..., S - 1)
                 constexpr bool kTr = MODE == kModeWgrad && SWAP;   // transposed output
@@ -1468,7 +1484,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 // every push has landed once its owner's wait ended, and the teardown
                 // cluster barrier keeps every peer alive)
                 if (t + unit_step < total) {
-                    named_bar_sync(1, 128);
+                    named_bar_sync(ebar, 128);
                     if (etid == 0)
                         for (int j = 0; j < csplit; ++j)
                             mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_consumed), j));
@@ -1517,10 +1533,10 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     }
                     const int32_t x = ti.nt * p.bn + c0;
                     if (MODE == kModeWgrad)
-                        stage_and_store<MODE>(staging, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
+                        stage_and_store<MODE>(stg_base, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
                                               ti.mt * kTileM + q * 32, ti.e);
                     else
-                        stage_and_store<MODE>(staging, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
+                        stage_and_store<MODE>(stg_base, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
                                               ti.row0 + q * 32, 0);
                 }
             }
@@ -1577,7 +1593,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 // S arrivals of this call (count - S = the slice); the next claim is
                 // issued before the current slice is reduced, hiding its latency.
                 __syncwarp();
-                named_bar_sync(1, 128);
+                named_bar_sync(ebar, 128);
                 if (etid == 0) {
                     __threadfence();
                     const uint32_t before = ticket_arrive(p.tickets + ti.ticket, c->epoch, p.status);
@@ -1592,9 +1608,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     c->last_flag = all_in;
                 }
                 __syncwarp();
-                named_bar_sync(1, 128);
+                named_bar_sync(ebar, 128);
                 const bool all_in = c->last_flag != 0;
-                named_bar_sync(1, 128);  // everyone read last_flag before the next tile rewrites it
+                named_bar_sync(ebar, 128);  // everyone read last_flag before the next tile rewrites it
                 if (all_in) {
                     __threadfence();
                     float *base0 = slots ? p.partials + (ti.slot - ti.s) * int64_t(kTileM) * p.bn
@@ -1608,9 +1624,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     constexpr int kCB = kTr ? 8 : 16;
                     uint64_t *tk = p.tickets + ti.ticket;
                     if (etid == 0) c->claim = int32_t(uint32_t(ticket_claim(tk)) - uint32_t(ti.S));
-                    named_bar_sync(1, 128);
+                    named_bar_sync(ebar, 128);
                     int sl = c->claim;
-                    named_bar_sync(1, 128);  // everyone read the claim before it is replaced
+                    named_bar_sync(ebar, 128);  // everyone read the claim before it is replaced
                     while (sl >= 0 && sl < nsl) {
                         unsigned long long nxt = 0;
                         if (etid == 0) nxt = ticket_claim(tk);  // in flight while this slice is reduced
@@ -1625,9 +1641,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                             finish_split_row<kCB / 4, 4, OUT_F32, kTr>(base0, nsum, slot_stride, !slots, c4b, c4e,
                                                                        lrow, row_ok, cols_valid, p.out, out_base, ld);
                         if (etid == 0) c->claim = int32_t(uint32_t(nxt) - uint32_t(ti.S));
-                        named_bar_sync(1, 128);
+                        named_bar_sync(ebar, 128);
                         sl = c->claim;
-                        named_bar_sync(1, 128);
+                        named_bar_sync(ebar, 128);
                     }
                 }
             }

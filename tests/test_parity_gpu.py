@@ -301,6 +301,36 @@ def test_pair_cluster_split_bitwise_equal_to_workspace_slots(out_dtype, monkeypa
     assert torch.equal(on_chip.view(i), slots.view(i))
 
 
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+@pytest.mark.parametrize("red", [192, 48])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("max_sms", [2, 6, 0])
+def test_two_epilogue_groups(pass_, red, out_dtype, max_sms, monkeypatch):
+    """A short reduction (192: three 64-deep k-blocks, 2-SM pairs; 48: one partial k-block,
+    single CTAs) gives the forward / data gradient a second epilogue warpgroup that takes every
+    other tile: ragged groups with a NaN tail, a partial last column tile (640 = 2 x 256 + 128),
+    and one or three pairs running every tile in turn (both groups' accumulator and staging
+    phases carried across tiles)."""
+    N, K = (640, red) if pass_ == "fwd" else (red, 640)
+    plan = gg.cake_gg_plan(pass_, 4, 3200, N, K, out_dtype, 1)
+    assert plan.epi_groups == 2 and plan.pair == (2 if red > 64 else 1)
+    check_case(pass_, [0, 777, 2048, 301], N, K, out_dtype, 1, seed=31, extra_rows=5, max_sms=max_sms)
+
+
+@pytest.mark.parametrize("pass_", ["fwd", "dgrad"])
+def test_two_epilogue_groups_bitwise_equal_to_one(pass_, monkeypatch):
+    """Which warpgroup stores a tile never changes its bits."""
+    import torch
+    N, K = (640, 192) if pass_ == "fwd" else (192, 640)
+    Xb, Wb, Gb, off = make_inputs([0, 777, 2048, 301], N, K, seed=32, extra_rows=3)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    two = run(pass_, X, W, G, off, "bf16", 1)
+    monkeypatch.setenv("CAKE_GG_EPI_GROUPS", "1")
+    one = run(pass_, X, W, G, off, "bf16", 1)
+    M = int(off[-1])
+    assert torch.equal(two[:M].view(torch.int16), one[:M].view(torch.int16))
+
+
 @pytest.mark.parametrize("det", [1, 0])
 def test_thin_weight_gradient_through_workspace_slots(det, monkeypatch):
     """The same thin shape with the cluster reduction disabled: partials through the workspace."""
