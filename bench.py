@@ -72,7 +72,7 @@ def parse_args():
                     help="skip the dense projection records (thin 4096->48 passes, mid-size 4096->512 wgrad)")
     ap.add_argument("--sustained-seconds", type=float, default=1.2,
                     help="length of the second, longer timing of the step (0 = skip)")
-    ap.add_argument("--decide", default="", choices=["", "tail", "streamk", "split", "wide"],
+    ap.add_argument("--decide", default="", choices=["", "tail", "streamk", "split", "wide", "csplit"],
                     help="run the planner decision protocol for one plan rule (candidate vs baseline)")
     ap.add_argument("--decide-points", default="", help="comma list of points (workload names) to test")
     ap.add_argument("--decide-runs", type=int, default=2)
@@ -904,6 +904,8 @@ DECIDE_RULES = {
               ["dense_4096to512", "dense_5120to512", "dense_4096to64"]),
     # 256 x 512 weight-gradient tiles vs 256 x 256
     "wide": ({}, {"CAKE_GG_WIDE": "0"}, ["moe_gate_up", "pages:gate_up E4 M112576 bal", "dense_4096to4096"]),
+    # a split tile reduced on chip by its cluster vs the same splits through workspace slots
+    "csplit": ({}, {"CAKE_GG_CSPLIT": "0"}, ["dense_4096to512", "dense_4096to48", "dense_4096to64"]),
 }
 
 

@@ -171,7 +171,9 @@ int32_t choose_streamk(int32_t N, int32_t K, int64_t M_max, int32_t bn, int32_t 
 // deterministic=False only; the deterministic variant's plans are kept).
 // Measured with `bench.py --decide RULE --det 0` on GB300; at these points
 // the rule failed the co-run condition, so the baseline plan runs.
-enum DecidedRule { kRuleSplit = 1, kRuleTail = 2, kRuleWide = 4 };
+// (kRuleCsplit: a split tile's reduction on chip by its cluster, dropped for
+// the same splits through workspace slots)
+enum DecidedRule { kRuleSplit = 1, kRuleTail = 2, kRuleWide = 4, kRuleCsplit = 8 };
 struct DecidedPoint {
     int32_t E, N, K;
     int64_t M_lo, M_hi;     // M_max range of the point (+- 5 % of the measured rows)
@@ -182,6 +184,7 @@ constexpr DecidedPoint kDecidedPoints[] = {
     {1, 1024, 5120, 15565, 17203, kRuleTail},      // dense 5120 -> 1024, T = 16384
     {1, 4096, 4096, 15565, 17203, kRuleWide},      // dense 4096 -> 4096, T = 16384
     {8, 4096, 6144, 124518, 137626, kRuleTail},    // gate_up E8 M131072 (N 4096, K 6144), balanced
+    {1, 48, 4096, 15565, 17203, kRuleCsplit},      // dense 4096 -> 48, T = 16384
 };
 
 int decided_drop(int32_t E, int32_t N, int32_t K, int64_t M_max)
@@ -885,7 +888,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
         // thin weight gradients reduce their splits on chip: the splits of a tile
         // run as one cluster and sum their partials through distributed shared
         // memory (no workspace partials, no tickets)
-        if (plan->swap_ab && plan->pair == 1 && plan->split_chunk > 0) {
+        if (plan->swap_ab && plan->pair == 1 && plan->split_chunk > 0 && !(drop & kRuleCsplit)) {
             const int64_t kbe = (M_max / E + bk - 1) / bk;
             const int64_t S = (kbe + plan->split_chunk - 1) / plan->split_chunk;
             if (S >= 2 && S <= kMaxClusterSplit) {
@@ -974,7 +977,8 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     // finish) -- automatically for one expert and a planned split;
     // CAKE_GG_CSPLIT = S forces it
     const char *env_chunk = std::getenv("CAKE_GG_SPLIT_CHUNK");
-    const bool auto_cs = E == 1 && !(env_chunk && *env_chunk) && env_cs != 0 && plan->split_chunk > 0 &&
+    const bool auto_cs = E == 1 && !(env_chunk && *env_chunk) && env_cs != 0 && !(drop & kRuleCsplit) &&
+                         plan->split_chunk > 0 &&
                          plan->tail_splits == 0 && plan->streamk_kblocks == 0;
     if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->pair == 2 && bn <= 256 && (auto_cs || env_cs >= 2)) {
         const int64_t kbe = (M_max / E + bk - 1) / bk;
