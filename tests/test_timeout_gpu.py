@@ -87,3 +87,33 @@ def test_dropped_copy_in_a_cluster_split_times_out_and_context_survives():
     ref = oracle.wgrad(Gb, Xb, off, E)
     f = lambda t: float(np.abs(oracle.bf16_bits_to_f64(t)).max())
     assert (np.abs(good.double().cpu().numpy() - ref) <= oracle.tolerance(ref, M, f(Gb), f(Xb))).all()
+
+
+def test_dropped_copy_in_a_pair_cluster_split_times_out_and_context_survives(monkeypatch):
+    """A weight gradient of 256-row pair tiles whose two splits run as one cluster of two pairs
+    (4 CTAs) and reduce into each other's operand rings.  The even CTA of the first cluster's
+    first pair loses its first copy: that pair's MMA never completes, the other pair waits in
+    vain for the first pair's ring to be offered, and every role gives up on its bounded wait.
+    The call reports CAKE_GG_ERR_TIMEOUT and the next regular call is correct."""
+    import torch
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "2")
+    E, M, N, K = 1, 3000, 512, 512
+    rng = np.random.default_rng(42)
+    Xb = wl.randn_bf16((M, K), 1.0, rng)
+    Gb = wl.randn_bf16((M, N), 1.0, rng)
+    off = wl.offsets_from_sizes([M])
+    X, G = wl.to_torch_bf16(Xb, "cuda"), wl.to_torch_bf16(Gb, "cuda")
+    offs = torch.from_numpy(off).cuda()
+    plan = gg.cake_gg_plan("wgrad", E, M, N, K, "fp32", 1)
+    assert plan.cluster_splits == 2 and plan.pair == 2
+    plan.debug_flags = gg.CAKE_GG_DEBUG_DROP_FIRST_LOAD
+    plan.timeout_ns = 100_000_000  # 0.1 s
+    ws = gg.make_workspace(plan, "cuda")
+    out = torch.zeros((E, N, K), dtype=torch.float32, device="cuda")
+    assert gg.cake_gg_wgrad(plan, G, X, out, offs, "fp32", 1, ws) == gg.CAKE_GG_OK
+    assert gg.cake_gg_check_status(ws) == gg.CAKE_GG_ERR_TIMEOUT
+    good = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1)
+    torch.cuda.synchronize()
+    ref = oracle.wgrad(Gb, Xb, off, E)
+    f = lambda t: float(np.abs(oracle.bf16_bits_to_f64(t)).max())
+    assert (np.abs(good.double().cpu().numpy() - ref) <= oracle.tolerance(ref, M, f(Gb), f(Xb))).all()
