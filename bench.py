@@ -546,7 +546,8 @@ def run_ours(args, wk):
                        "launch": "cuda-graph replay per pass" if args.graph else "eager",
                        "plans": {p: {k: v for k, v in plans[p].as_dict().items()
                                      if k in ("tile_n", "tile_k", "stages", "pair", "swap_ab", "split_chunk",
-                                              "staging_bufs")} for p in passes}},
+                                              "staging_bufs", "cluster_splits", "tail_units", "tail_splits",
+                                              "epi_groups")} for p in passes}},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             **({"corun": corun} if corun else {}),
             "gpu_launches": len(passes) * args.steps, "clocks": clocks,
@@ -645,7 +646,7 @@ def projection_record(gg, dev, local, rank, d_in, d_out, passes, seconds=0.4, pe
             "tflops": round(flop / sec / 1e12, 1), "gbs": round(alg / sec / 1e9, 1),
             "plan": {k: v for k, v in plan.as_dict().items()
                      if k in ("tile_n", "tile_k", "stages", "pair", "swap_ab", "split_chunk", "cluster_splits",
-                              "tail_units", "tail_splits", "staging_bufs")},
+                              "tail_units", "tail_splits", "staging_bufs", "epi_groups")},
             "roofline": roof, "clocks": sampler.finish() if sampler else None}
         del wsp, out, graph
     out_rec["launch"] = (f"CUDA graph of {per_graph} back-to-back calls, replayed; {sets} input sets "
