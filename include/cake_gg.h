@@ -56,7 +56,9 @@
  *     (single CTAs only) or 2 (pairs wherever the tile allows), CAKE_GG_WIDE (0: no 256 x 512 weight-gradient tiles,
  *     2: wherever they fit), CAKE_GG_WIDE_FD=1 (512-wide forward / data-
  *     gradient tiles), CAKE_GG_SPLIT_CHUNK (k-blocks per split, 0 = no split),
- *     CAKE_GG_CSPLIT (0, or 2..8 cluster splits), CAKE_GG_TAIL=0 (no split
+ *     CAKE_GG_CSPLIT (0: splits through workspace slots; 2..8 cluster splits,
+ *     for pairs 2..4: clusters of two CTAs per split), CAKE_GG_EPI_GROUPS (1 or
+ *     2 epilogue warpgroups for the forward / data gradient), CAKE_GG_TAIL=0 (no split
  *     tail), CAKE_GG_STREAMK (0: never, the default; 1: by the cost rule;
  *     2: wherever the walk applies), CAKE_GG_STREAMK_KB (its segment length
  *     in k-blocks), CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2),
@@ -136,7 +138,8 @@ typedef struct cake_gg_plan {
     uint64_t workspace_bytes;/* bytes of workspace the compute call needs           */
     int32_t staging_bufs;    /* epilogue staging buffers per warp (1 or 2)          */
     int32_t cluster_splits;  /* weight gradient: >0 = that many splits per tile run as
-                                one cluster and reduce on chip (no workspace partials) */
+                                one cluster (of CTAs, or of pairs: 2 CTAs per split)
+                                and reduce on chip (no workspace partials)          */
     int32_t tail_units;      /* weight gradient: the last tail_units units of the walk */
     int32_t tail_splits;     /* are each split into tail_splits pieces whose FP32
                                 partials are summed in split order (0 = no tail split) */
