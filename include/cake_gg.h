@@ -58,8 +58,10 @@
  *     gradient tiles), CAKE_GG_SPLIT_CHUNK (k-blocks per split, 0 = no split),
  *     CAKE_GG_CSPLIT (0: splits through workspace slots; 2..8 cluster splits,
  *     for pairs 2..4: clusters of two CTAs per split), CAKE_GG_EPI_GROUPS (1 or
- *     2 epilogue warpgroups for the forward / data gradient), CAKE_GG_TAIL=0 (no split
- *     tail), CAKE_GG_STREAMK (0: never, the default; 1: by the cost rule;
+ *     2 epilogue warpgroups for the forward / data gradient), CAKE_GG_TAIL=0
+ *     (no split tail of either kind), CAKE_GG_NTAIL (N-split tail of 256 x 512
+ *     tiles: 0 = off, the default; 1 = by its rule; 2 or 4 = that many column
+ *     pieces), CAKE_GG_STREAMK (0: never, the default; 1: by the cost rule;
  *     2: wherever the walk applies), CAKE_GG_STREAMK_KB (its segment length
  *     in k-blocks), CAKE_GG_STAGES, CAKE_GG_STAGING_BUFS (1 or 2),
  *     CAKE_GG_DECIDED=0 (the non-deterministic planner ignores its table of
@@ -148,7 +150,11 @@ typedef struct cake_gg_plan {
                                 tile boundaries; a tile's pieces are summed in k order */
     int32_t epi_groups;      /* forward / data gradient: 2 = a second epilogue warpgroup
                                 takes every other tile (short reductions); else 1 */
-    int32_t reserved[2];
+    int32_t tail_nsplit;     /* weight gradient of 256 x 512 pair tiles: > 1 = the last
+                                tail_units units run as that many column pieces each,
+                                every piece over all k-blocks (no partials; the bits
+                                of the whole units); 0 = none                       */
+    int32_t reserved[1];
 } cake_gg_plan_t;
 
 /* Debug flag (tests only): the CTA that takes the walk's first unit (its even
@@ -284,8 +290,10 @@ int cake_gg_corun_spinner(int32_t ctas, uint64_t ns, void *stream);
 
 /* Host-side replica of the kernel's tile walk, for testing the scheduler on
  * any machine.  Given host offsets[E+1], writes up to `capacity` tiles, each
- * as 8 int32 {expert, m_tile, n_tile, split, n_splits, kblock_begin,
- * kblock_end, ticket}, in walk order (heaviest expert first for the weight
+ * as 10 int32 {expert, m_tile, n_tile, split, n_splits, kblock_begin,
+ * kblock_end, ticket, column_begin, column_count} (the last two: the columns
+ * of the n_tile the unit computes, all tile_n of them but for an N-split
+ * tail piece), in walk order (heaviest expert first for the weight
  * gradient; the order in which the CTAs take them from the tile counter, or
  * by a fixed stride), and stores the total tile count in *count.  Returns CAKE_GG_ERR_BAD_OFFSETS for offsets
  * the kernel would reject. */

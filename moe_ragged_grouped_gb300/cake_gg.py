@@ -69,7 +69,8 @@ class CakeGGPlan(ctypes.Structure):
         ("tail_splits", ctypes.c_int32),
         ("streamk_kblocks", ctypes.c_int32),
         ("epi_groups", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("tail_nsplit", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 1),
     ]
 
     def as_dict(self):
@@ -235,7 +236,7 @@ def cake_gg_corun_spinner(ctas, ns, stream) -> int:
 
 
 def cake_gg_tile_walk(plan, offsets) -> np.ndarray:
-    """cake_gg_tile_walk(): the kernel's tile list for host offsets, as an int32 [count, 8] array."""
+    """cake_gg_tile_walk(): the kernel's tile list for host offsets, as an int32 [count, 10] array."""
     lib = load_library()
     off = np.ascontiguousarray(offsets, dtype=np.int32)
     count = ctypes.c_int64(0)
@@ -243,7 +244,7 @@ def cake_gg_tile_walk(plan, offsets) -> np.ndarray:
                                None, ctypes.byref(count))
     if rc != CAKE_GG_OK:
         raise CakeGGError(rc, "cake_gg_tile_walk")
-    out = np.zeros((count.value, 8), dtype=np.int32)
+    out = np.zeros((count.value, 10), dtype=np.int32)
     rc = lib.cake_gg_tile_walk(ctypes.byref(plan), off.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                count.value, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                ctypes.byref(count))

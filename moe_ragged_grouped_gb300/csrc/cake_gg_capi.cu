@@ -128,6 +128,43 @@ void choose_tail(int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn, int
     }
 }
 
+// N-split tail of a weight gradient of 256 x 512 pair tiles (flashinfer PR
+// #7516, the #7575 text: the tail as one balanced wave, its tiles split along
+// N, each piece over the same K order with one rounding): when the last
+// partial wave of equal-length units is more than half full -- too many units
+// for the K-split tail -- and four 128-column pieces per unit fit in three
+// quarters of a wave, the last T units run as 4 pieces each (3 rounds of a
+// quarter unit's MMAs instead of one whole unit).  The pieces sum nothing, so
+// the results are bitwise those of the whole units.  Measured slower here and
+// off by default: a 128-column piece streams the unit's whole A operand for a
+// quarter of its FLOPs (2.7x the operand bytes per FLOP of a 512-wide unit),
+// so it runs bandwidth-bound at ~0.6 of a unit's time (two experts of 16384
+// rows, 3072 x 4096: 0.594 ms against 0.449 ms with whole tail units).
+// env: 0 = off (default), 1 = by the rule, 2 or 4 = that many pieces for the
+// last partial wave (or every unit if none).
+void choose_ntail(int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn, int32_t bk, int32_t pair, int env,
+                  int32_t *tail_units, int32_t *nsplit)
+{
+    *tail_units = 0;
+    *nsplit = 0;
+    if (bn != 512 || pair != 2 || env == 0) return;
+    const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, 0, 0, pair, bk);
+    const int64_t units = int64_t(E) * m_units_w(g) * g.n_tiles;
+    const int64_t P = kWaveCtas / pair;
+    int64_t T = units % P;
+    const int64_t kb_per_unit = (M_max / E) / bk;
+    if (env == 2 || env == 4) {
+        if (T == 0) T = units < P ? units : P;
+        *tail_units = int32_t(T);
+        *nsplit = env;
+        return;
+    }
+    if (env == 1 && T > 0 && 2 * T > P && 4 * T <= 3 * P && kb_per_unit >= 64) {
+        *tail_units = int32_t(T);
+        *nsplit = 4;
+    }
+}
+
 // Stream-K walk of a one-expert weight gradient whose pair tiles fill less
 // than two waves of the fixed 76-pair (152-CTA) wave: the n_tiles x KB
 // k-blocks of every m-unit are cut into V = 76 / m_units segments of equal
@@ -424,6 +461,11 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         plan->tail_units < 0 || plan->tail_splits < 0 || plan->tail_splits == 1 || plan->tail_splits > kMaxTailSplits ||
         (plan->tail_splits > 1 && (pass != CAKE_GG_WGRAD || plan->swap_ab || plan->split_chunk > 0 ||
                                    plan->cluster_splits > 0)) ||
+        plan->tail_nsplit < 0 || plan->tail_nsplit == 1 ||
+        (plan->tail_nsplit > 1 &&
+         (pass != CAKE_GG_WGRAD || plan->swap_ab || plan->pair != 2 || plan->tile_n != 512 ||
+          (plan->tail_nsplit != 2 && plan->tail_nsplit != 4) || plan->tail_splits > 1 || plan->split_chunk > 0 ||
+          plan->cluster_splits > 0 || plan->streamk_kblocks > 0)) ||
         plan->streamk_kblocks < 0 ||
         (plan->streamk_kblocks > 0 &&
          (pass != CAKE_GG_WGRAD || plan->E != 1 || plan->swap_ab || plan->split_chunk > 0 || plan->tail_splits > 1 ||
@@ -601,13 +643,18 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
     p.retire = p.dyn || ((mode == kModeWgrad) && (p.kchunk > 0 || plan->tail_splits > 1 || p.sk > 0)) ? 1 : 0;
     p.tail = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_units : 0;
     p.tail_s = mode == kModeWgrad && plan->tail_splits > 1 ? plan->tail_splits : 0;
+    // N-split tail pieces load whole atoms through the stacked B map; without it
+    // the tail units run whole (the same bits)
+    p.ntq = mode == kModeWgrad && plan->tail_nsplit > 1 && stack_b ? plan->tail_nsplit : 0;
+    p.ntail = p.ntq > 1 ? plan->tail_units : 0;
     if (p.prefetch < 0 || p.prefetch > 64) p.prefetch = 0;
     p.timeout_ns = plan->timeout_ns ? plan->timeout_ns : kDefaultTimeoutNs;
 
     // grid: one CTA per SM (capped by max_sms), no more than an upper bound on tiles
     const int P = plan->pair;
     const int CL = P * (p.csplit > 0 ? p.csplit : 1);   // CTAs per cluster (one unit per cluster)
-    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk, p.csplit, 0, 0, p.sk);
+    const Geom g = make_geom(mode, E, N, K, plan->M_max, bn, plan->swap_ab, p.kchunk, P, bk, p.csplit, 0, 0, p.sk,
+                             p.ntail, p.ntq);
     uint64_t unit_bound;
     if (mode == kModeWgrad && p.sk > 0) {
         // virtual pairs of the walk at M_max rows (the most there can be)
@@ -616,7 +663,8 @@ int run(const cake_gg_plan_t *plan, int mode, const void *opA, const void *opB, 
         uint64_t splits = uint64_t(E);
         if (p.kchunk > 0) splits = M / (uint64_t(bk) * uint64_t(p.kchunk)) + uint64_t(E) + 1;
         unit_bound = uint64_t(m_units_w(g)) * uint64_t(g.n_tiles) * splits +
-                     uint64_t(p.tail) * uint64_t(p.tail_s > 1 ? p.tail_s - 1 : 0);
+                     uint64_t(p.tail) * uint64_t(p.tail_s > 1 ? p.tail_s - 1 : 0) +
+                     uint64_t(p.ntail) * uint64_t(p.ntq > 1 ? p.ntq - 1 : 0);
     } else {
         unit_bound = (M / (uint64_t(kTileM) * P) + uint64_t(E) + 1) * uint64_t(g.n_tiles);
     }
@@ -908,6 +956,11 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->split_chunk == 0 && plan->cluster_splits == 0 &&
         env_int("CAKE_GG_TAIL", 1) != 0 && !(drop & kRuleTail))
         choose_tail(E, N, K, M_max, bn, bk, plan->pair, &plan->tail_units, &plan->tail_splits);
+    // ... or an N-split tail of 256 x 512 tiles when the last wave is too full for it
+    if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->split_chunk == 0 && plan->cluster_splits == 0 &&
+        plan->tail_splits == 0 && env_int("CAKE_GG_TAIL", 1) != 0 && !(drop & kRuleTail))
+        choose_ntail(E, N, K, M_max, bn, bk, plan->pair, env_int("CAKE_GG_NTAIL", 0), &plan->tail_units,
+                     &plan->tail_nsplit);
     // stream-K walk of a one-expert weight gradient (see choose_streamk); it
     // replaces a split or a split tail
     if (pass == CAKE_GG_WGRAD && E == 1 && !plan->swap_ab && plan->pair == 2 && bn <= 256 &&
@@ -1076,7 +1129,9 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
     Geom g = make_geom(mode, E, plan->N, plan->K, plan->M_max, plan->tile_n, plan->swap_ab,
                              mode == kModeWgrad ? plan->split_chunk : 0, plan->pair, plan->tile_k,
                              mode == kModeWgrad ? plan->cluster_splits : 0, tail ? plan->tail_units : 0,
-                             tail ? plan->tail_splits : 0, mode == kModeWgrad ? plan->streamk_kblocks : 0);
+                             tail ? plan->tail_splits : 0, mode == kModeWgrad ? plan->streamk_kblocks : 0,
+                             mode == kModeWgrad && plan->tail_nsplit > 1 ? plan->tail_units : 0,
+                             mode == kModeWgrad ? plan->tail_nsplit : 0);
     std::vector<int32_t> cnt(E), cost(E), order(E), pref(E + 1), spref(E + 1);
     for (int e = 0; e < E; ++e) {
         cnt[e] = expert_tiles(g, off[e + 1] - off[e]);
@@ -1112,7 +1167,7 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
             const Tile ti = decode_tile(g, t, off, order.data(), pref.data(), spref.data(), r);
             if (!ti.valid) continue;
             if (n < capacity) {
-                int32_t *o = tiles_out + n * 8;
+                int32_t *o = tiles_out + n * 10;
                 o[0] = ti.e;
                 o[1] = ti.mt;
                 o[2] = ti.nt;
@@ -1121,6 +1176,8 @@ int cake_gg_tile_walk(const cake_gg_plan_t *plan, const int32_t *off, int64_t ca
                 o[5] = ti.kb0;
                 o[6] = ti.kb1;
                 o[7] = ti.ticket;
+                o[8] = ti.c0;
+                o[9] = ti.cw;
             }
             ++n;
         }

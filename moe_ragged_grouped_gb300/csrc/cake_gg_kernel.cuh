@@ -43,7 +43,7 @@ constexpr uint32_t kRouterABytes = kTileM * 64 * 4;   // 32 KB: a 128 x 64 FP32 
 
 __host__ __device__ constexpr int threads_for(int kmode)
 {
-    return kmode == kModeRouter ? kThreadsRouter : kmode == kModeWgrad ? kThreads : kThreadsEpi2;
+    return kmode == kModeRouter ? kThreadsRouter : kmode == kModeWgrad || kmode == kModeWgradNT ? kThreads : kThreadsEpi2;
 }
 constexpr int kMaxStages = 8;
 constexpr int kMaxCsplit = 8;   // largest cluster split (portable cluster size)
@@ -86,6 +86,8 @@ struct KParams {
     int32_t tail;           // weight gradient: split tail units ...
     int32_t tail_s;         // ... and pieces per tail unit (0 = none)
     int32_t sk;             // weight gradient of one expert: stream-K segment length in k-blocks (0 = off)
+    int32_t ntail;          // weight gradient: N-split tail units ...
+    int32_t ntq;            // ... and column pieces per tail unit (0 = none)
     int32_t kstagger;       // router: unit t walks its k-blocks from (t * kstagger) mod their count (0 = in order)
     int32_t *sched;         // [0]: next unit, [32]: CTAs retired (zero between calls)
     uint64_t timeout_ns;
@@ -548,7 +550,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
 {
     // the router is the forward pass (walk, epilogue) with FP32 A tiles split by converter warps
     constexpr bool RT = KMODE == kModeRouter;
-    constexpr int MODE = RT ? kModeFwd : KMODE;
+    constexpr bool NT = KMODE == kModeWgradNT;   // N-split tail pieces
+    constexpr int MODE = RT ? kModeFwd : NT ? kModeWgrad : KMODE;
     constexpr bool A_MN = (MODE == kModeWgrad);
     constexpr bool B_MN = (MODE != kModeFwd);
 
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
     const int csplit = MODE == kModeWgrad && (SWAP || PAIR == 2) ? p.csplit : 0;
     Geom g = make_geom(MODE, E, p.N, p.K, p.M_max, p.bn, SWAP ? 1 : 0, p.kchunk, PAIR, p.bk, csplit,
                        MODE == kModeWgrad ? p.tail : 0, MODE == kModeWgrad ? p.tail_s : 0,
-                       MODE == kModeWgrad && !SWAP ? p.sk : 0);
+                       MODE == kModeWgrad && !SWAP ? p.sk : 0, NT && !SWAP ? p.ntail : 0, NT && !SWAP ? p.ntq : 0);
     // a cluster shares each unit: a pair (2 CTAs) computes m-tiles 2 * unit + h
     // as one 256-row MMA (the even CTA issues it; each CTA holds its A rows and
     // half of the B tile); a cluster split (csplit CTAs, or csplit pairs)
@@ -914,7 +917,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     const uint32_t fb = smem_u32(&c->full[stage]);
                     const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
                     const uint32_t sb = sa + a_bytes;
-                    mbar_arrive_expect_tx(fb, tx);
+                    // (an N-split tail piece of a 512-wide tile loads one B box: the
+                    // map's 256 / 64 / PAIR atoms from its first one)
+                    mbar_arrive_expect_tx(fb, NT && ti.cw < p.bn
+                                                  ? a_bytes + uint32_t(256 / 64 / PAIR) * atom_b
+                                                  : tx);
                     // test hook: the walk's first unit (whichever CTA takes it) loses its
                     // first copy on the even / single CTA
                     const bool drop = (p.debug_flags & 1) && t == 0 && kb == ti.kb0 && rank == 0;
@@ -949,7 +956,15 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                                 tma_load_2d(sa, &mapA, fb, ti.mt * kTileM, r);
                                 tma_load_2d(sa + atom_a, &mapA, fb, ti.mt * kTileM + 64, r);
                             }
-                            if (p.stack_b && p.bn > 256) {
+                            if (NT && p.stack_b && p.bn > 256 && ti.cw < p.bn) {
+                                // an N-split tail piece of a 512-wide tile: one box from
+                                // this CTA's first atom of the piece (cw / PAIR columns,
+                                // whole 64-wide atoms); the MMA reads cw / PAIR columns of
+                                // it, the rest of the box is the next columns (or the
+                                // zero fill past K)
+                                const int pa = ti.cw / 64 / PAIR;
+                                tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + ti.c0 / 64 + half * pa);
+                            } else if (p.stack_b && p.bn > 256) {
                                 // a 512-wide tile: this CTA's half of each 256-column MMA tile
                                 const int hb = 256 / 64 / PAIR;   // atoms per half per CTA
                                 tma_load_3d(sb, &mapB, fb, 0, r, ti.nt * nb + half * hb);
@@ -1035,6 +1050,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         // loaded stage and relays "stage loaded" to the even CTA's full barrier)
         // (a 512-wide tile is two MMAs of N = 256 per k-step, into TMEM columns 0 and 256)
         const uint32_t idesc = idesc_bf16_f32(kTileM * PAIR, uint32_t(p.bn > 256 ? 256 : p.bn), A_MN, B_MN);
+        // (an N-split tail piece is one MMA of its width per k-step)
+        const uint32_t idesc_piece =
+            NT ? idesc_bf16_f32(kTileM * PAIR, uint32_t(g.ntq > 1 ? p.bn / g.ntq : p.bn), A_MN, B_MN) : idesc;
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
@@ -1082,8 +1100,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 const uint32_t sa = ring_u32 + uint32_t(stage) * stage_bytes;
                 const uint32_t sb = sa + a_bytes;
                 if (MODE == kModeWgrad && kb == zero_kb)
-                    zero_stale_rows(ring, ring_u32, sa, sb, atom_a, atom_b, zero_valid, p.bk, 2 + p.bn / 64 / PAIR,
-                                    lane);
+                    zero_stale_rows(ring, ring_u32, sa, sb, atom_a, atom_b, zero_valid, p.bk,
+                                    2 + (NT ? ti.cw : p.bn) / 64 / PAIR, lane);
                 __syncwarp();
                 if (leader) {
                     if (lane == 0) {
@@ -1099,6 +1117,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                             issue_stage_mmas_ta<PAIR>(d_tmem, a_hi, bd0, idesc, first);
                             issue_stage_mmas_ta<PAIR>(d_tmem, a_hi, bl, idesc, false);
                             issue_stage_mmas_ta<PAIR>(d_tmem, a_hi + 32u, bd0, idesc, false);
+                        } else if (NT && ti.cw < p.bn) {
+                            issue_stage_mmas<1, A_MN, B_MN, PAIR>(d_tmem, ad0, bd0, idesc_piece, first, chunk_b);
                         } else if (p.bn > 256) {
                             // this CTA's halves of the two 256-column B tiles sit 2 * (128 / PAIR / 64) atoms apart
                             const uint32_t half = uint32_t(256 / 64 / PAIR) * atom_b;
@@ -1166,6 +1186,8 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             const int acc = nacc == 2 ? (it & 1) : 0;
             const uint32_t acc_phase = nacc == 2 ? (uint32_t(it >> 1) & 1u) : (uint32_t(it) & 1u);
             const bool empty_tile = ti.kb1 <= ti.kb0;
+            const int32_t tcw = NT ? ti.cw : p.bn;   // columns of the tile this unit computes
+            const int32_t tc0 = NT ? ti.c0 : 0;      // ... from this one
             const bool split = (MODE == kModeWgrad) && ti.S > 1 && ti.valid;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc) * acc_stride;
 
@@ -1185,10 +1207,11 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 rows_valid = ti.row_end - ti.row0;
                 cols_valid = p.K - ti.nt * p.bn;
             } else if (!SWAP) {
+                // (an N-split tail piece: columns [c0, c0 + cw) of the tile)
                 ld = p.K;
-                out_base = int64_t(ti.e) * p.N * p.K + int64_t(ti.mt) * kTileM * ld + int64_t(ti.nt) * p.bn;
+                out_base = int64_t(ti.e) * p.N * p.K + int64_t(ti.mt) * kTileM * ld + int64_t(ti.nt) * p.bn + tc0;
                 rows_valid = p.N - ti.mt * kTileM;
-                cols_valid = p.K - ti.nt * p.bn;
+                cols_valid = p.K - (ti.nt * p.bn + tc0);
             } else {
                 // C[m = k, n = n] -> dW[e, n, k]: transposed store
                 ld = p.K;
@@ -1196,7 +1219,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 rows_valid = p.K - ti.mt * kTileM;
                 cols_valid = p.N - ti.nt * p.bn;
             }
-            if (cols_valid > p.bn) cols_valid = p.bn;
+            if (cols_valid > tcw) cols_valid = tcw;
             const bool row_ok = lrow < rows_valid;
             // cluster split: this CTA's float4 columns [q0, q1) of the tile's nq
             // (pairs: whole 128-byte output rows per owner, stored by TMA)
@@ -1512,7 +1535,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 // only chunks that exist: every staging write must be followed by its
                 // committed store, or the alternating-buffer wait (all groups but the
                 // newest have read their buffers) would let a write overtake a store
-                for (int c0 = 0; c0 < p.bn && c0 < cols_valid; c0 += CW) {
+                for (int c0 = 0; c0 < tcw && c0 < cols_valid; c0 += CW) {
                     uint32_t w[32];
                     if (empty_tile) {
 #pragma unroll
@@ -1531,7 +1554,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                             w[16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
                         }
                     }
-                    const int32_t x = ti.nt * p.bn + c0;
+                    const int32_t x = ti.nt * p.bn + tc0 + c0;
                     if (MODE == kModeWgrad)
                         stage_and_store<MODE>(stg_base, stg_buf, p.staging_bufs, q, lane, w, &mapOut, x,
                                               ti.mt * kTileM + q * 32, ti.e);
@@ -1540,7 +1563,7 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                                               ti.row0 + q * 32, 0);
                 }
             }
-            for (int c0 = 0; c0 < p.bn && !tma_path; c0 += 32) {
+            for (int c0 = 0; c0 < tcw && !tma_path; c0 += 32) {
                 float v[32];
                 if (empty_tile) {
 #pragma unroll

@@ -59,8 +59,9 @@ cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const CUtenso
     }
     cfg.gridDim = dim3(grid, 1, 1);
     // (a forward / data gradient with one epilogue group runs without warps 6..9)
-    const int threads = MODE == kModeRouter || MODE == kModeWgrad ? threads_for(MODE)
-                                                                  : (p.epi_groups == 2 ? kThreadsEpi2 : kThreads);
+    const int threads = MODE == kModeRouter || MODE == kModeWgrad || MODE == kModeWgradNT
+                            ? threads_for(MODE)
+                            : (p.epi_groups == 2 ? kThreadsEpi2 : kThreads);
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -42,6 +42,9 @@ constexpr int kModeWgrad = 2;
 // The FP32 router GEMM (BF16x3): the forward pass's walk and epilogue, FP32
 // operand tiles split into BF16 high and low parts inside the kernel.
 constexpr int kModeRouter = 3;
+// the weight gradient with N-split tail pieces compiled in (a kernel of its own,
+// so that the other weight-gradient kernels carry none of that code)
+constexpr int kModeWgradNT = 4;
 
 constexpr int kTileM = 128;     // MMA rows (TMEM lanes)
 constexpr int kTileK = 64;      // reduction elements of one k-chunk (one 128-byte swizzle row)
@@ -66,15 +69,20 @@ struct Geom {
     int32_t tail;         // weight gradient: the last `tail` units of the walk are split ...
     int32_t tail_s;       // ... into tail_s pieces each (0 = no tail split)
     int32_t sk;           // weight gradient, one expert: stream-K segment length in k-blocks (0 = off)
+    int32_t ntail;        // weight gradient: the last `ntail` units of the walk run ...
+    int32_t ntq;          // ... as ntq column pieces each, every piece over all of its k-blocks (0 = off)
 };
 
 CAKE_HD int32_t ceil_div_i(int32_t a, int32_t b) { return (a + b - 1) / b; }
 
 CAKE_HD Geom make_geom(int32_t mode, int32_t E, int32_t N, int32_t K, int64_t M_max, int32_t bn,
                        int32_t swap, int32_t kchunk, int32_t pair = 1, int32_t bk = kTileK,
-                       int32_t csplit = 0, int32_t tail = 0, int32_t tail_s = 0, int32_t sk = 0)
+                       int32_t csplit = 0, int32_t tail = 0, int32_t tail_s = 0, int32_t sk = 0,
+                       int32_t ntail = 0, int32_t ntq = 0)
 {
     Geom g;
+    g.ntail = mode == kModeWgrad && ntq > 1 ? ntail : 0;
+    g.ntq = mode == kModeWgrad && ntq > 1 ? ntq : 0;
     g.sk = mode == kModeWgrad ? sk : 0;
     g.tail = tail_s > 1 ? tail : 0;
     g.tail_s = tail_s > 1 ? tail_s : 0;
@@ -196,6 +204,8 @@ struct Tile {
     int32_t row_end;  // one past the expert's last row
     int32_t ticket;   // wgrad: output tile index e * (m_tiles_w * n_tiles) + mt * n_tiles + nt
     int64_t slot;     // wgrad split: partial slot of this split
+    int32_t c0;       // wgrad N-split tail piece: first column of the piece within the tile (else 0)
+    int32_t cw;       // columns of the tile this unit computes (tile_n, or the piece's width)
     bool valid;       // false for a pair rank whose tile lies past the output
     bool tail;        // a piece of a split tail unit (partials in slots, also when non-deterministic)
 };
@@ -322,7 +332,8 @@ CAKE_HD bool tail_fits_whole(const Geom &g, const int32_t *off, const int32_t *o
 // g.tail_s positions (one per piece).
 CAKE_HD int64_t walk_length(const Geom &g, int64_t units)
 {
-    return units + int64_t(g.tail) * (g.tail_s > 1 ? g.tail_s - 1 : 0);
+    return units + int64_t(g.tail) * (g.tail_s > 1 ? g.tail_s - 1 : 0) +
+           int64_t(g.ntail) * (g.ntq > 1 ? g.ntq - 1 : 0);
 }
 
 // Tables: off[E+1] offsets; order[E] processing position -> expert;
@@ -343,6 +354,17 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
             t = main_units + tail_unit;
         }
     }
+    // a column piece of an N-split tail unit: position -> (unit, piece)
+    int32_t npiece = -1;
+    if (g.mode == kModeWgrad && g.ntail > 0) {
+        const int64_t main_units = int64_t(pref[g.E]) - g.ntail;
+        if (t >= main_units) {
+            const int64_t j = t - main_units;
+            const int64_t u = j / g.ntq;
+            npiece = int32_t(j - u * g.ntq);
+            t = main_units + u;
+        }
+    }
     // last position p with pref[p] <= t (positions of empty experts have
     // pref[p] == pref[p+1] and are never selected since t < pref[E])
     int32_t lo = 0, hi = g.E - 1;
@@ -352,6 +374,8 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
     }
     Tile ti;
     ti.tail = false;
+    ti.c0 = 0;
+    ti.cw = g.bn;
     const int32_t e = order[lo];
     const int32_t local = static_cast<int32_t>(t - pref[lo]);
     const int32_t r0 = off[e];
@@ -432,6 +456,12 @@ CAKE_HD Tile decode_tile(const Geom &g, int64_t t, const int32_t *off, const int
             ti.kb1 = (tail_piece + 1) * ch < nkb_e ? (tail_piece + 1) * ch : nkb_e;
             ti.slot = (tail_unit * g.pair + rank) * g.tail_s + tail_piece;
             ti.tail = true;
+        }
+        if (npiece >= 0) {
+            // the same k-blocks over a narrower column range: each output element's
+            // reduction order is unchanged (one rounding, the bits of the whole unit)
+            ti.cw = g.bn / g.ntq;
+            ti.c0 = npiece * ti.cw;
         }
     } else {
         ti.mt = (local / g.n_tiles) * g.pair + rank;

@@ -119,7 +119,7 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
     if pass_ in ("fwd", "dgrad"):
         nout = N if pass_ == "fwd" else K
         cover = np.zeros((M, nout), np.int32)
-        for e, mt, nt, s, S, kb0, kb1, _ in tiles:
+        for e, mt, nt, s, S, kb0, kb1, _ in tiles[:, :8]:
             assert S == 1 and s == 0 and kb0 == 0
             r0 = off[e] + mt * bm
             assert r0 < off[e + 1]
@@ -131,8 +131,21 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
         # exactly once <=> every (expert, m-tile, n-tile) block appears as one split group
         n_mt, n_nt = -(-mdim // bm), -(-ndim // bn)
         cover = np.zeros((len(sizes), n_mt, n_nt), np.int32)
+        # N-split tail pieces: column ranges of one tile that partition it, each over
+        # all of its k-blocks; every other unit covers the whole tile
+        pieces = {}
+        for e, mt, nt, s, S, kb0, kb1, ticket, c0, cw in tiles:
+            pieces.setdefault((e, mt, nt), []).append((c0, cw))
+        for key, cols in pieces.items():
+            cols = sorted(set(cols))
+            assert cols[0][0] == 0 and sum(w for _, w in cols) == bn
+            assert all(a[0] + a[1] == b[0] for a, b in zip(cols, cols[1:]))
         splits = {}
-        for e, mt, nt, s, S, kb0, kb1, ticket in tiles:
+        for e, mt, nt, s, S, kb0, kb1, ticket, c0, cw in tiles:
+            if cw < bn:
+                assert S == 1 and s == 0 and kb0 == 0
+                if c0 > 0:
+                    continue   # (counted once, with its first piece)
             splits.setdefault((e, mt, nt), []).append((s, S, kb0, kb1, ticket))
         for (e, mt, nt), lst in splits.items():
             lst.sort()
@@ -151,7 +164,7 @@ def _check_walk_coverage(pass_, sizes, N, K, det=1, env=None):
         assert (cover == 1).all()
         # heaviest-first over experts (k-blocks per split, ties by expert index)
         costs = []
-        for e, mt, nt, s, S, kb0, kb1, _ in tiles:
+        for e, mt, nt, s, S, kb0, kb1, _ in tiles[:, :8]:
             if not costs or costs[-1][0] != e:
                 costs.append((e, -(-(-(-(off[e + 1] - off[e]) // plan.tile_k)) // S)))
         seq = [c for _, c in costs]
@@ -200,6 +213,31 @@ def test_pair_cluster_split_needs_every_cluster_resident():
     # 5120 -> 512: 40 pair tiles, more two-pair clusters than fit at once -> global split slots
     plan = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
     assert plan.cluster_splits == 0 and plan.split_chunk > 0
+
+
+def test_tile_walk_nsplit_tail_two_experts():
+    """Two experts of 16384 rows, 3072 x 4096: 192 units of 256 x 512, a last wave of 40 of
+    the 76 pairs -- too full for the K-split tail -- runs by the N-split rule as 4 column pieces
+    of 128 per unit (160 pieces), each over all of its expert's k-blocks.  (The rule is off
+    unless asked for: measured slower.)"""
+    assert gg.cake_gg_plan("wgrad", 2, 32768, 3072, 4096, "bf16", 1).tail_nsplit == 0
+    plan, tiles = _check_walk_coverage("wgrad", [16384, 16384], N=3072, K=4096, env={"CAKE_GG_NTAIL": "1"})
+    assert plan.tile_n == 512 and plan.pair == 2
+    assert (plan.tail_units, plan.tail_nsplit, plan.tail_splits) == (40, 4, 0)
+    assert plan.workspace_bytes == 256
+    pieces = tiles[tiles[:, 9] < 512]
+    assert len(pieces) == 40 * 4 * 2 and set(pieces[:, 9]) == {128}
+    assert (pieces[:, 5] == 0).all() and (pieces[:, 6] == 16384 // plan.tile_k).all()
+
+
+def test_tile_walk_nsplit_tail_forced_ragged():
+    os.environ["CAKE_GG_WIDE"] = "2"
+    try:
+        plan, tiles = _check_walk_coverage("wgrad", [9000, 0, 16000], N=256, K=1152,
+                                           env={"CAKE_GG_NTAIL": "4", "CAKE_GG_SPLIT_CHUNK": "0"})
+    finally:
+        del os.environ["CAKE_GG_WIDE"]
+    assert plan.tile_n == 512 and plan.tail_nsplit == 4 and plan.tail_units == 9
 
 
 def test_tile_walk_cluster_split_with_small_and_empty_experts():
@@ -268,7 +306,7 @@ def test_tile_walk_streamk(sizes, N, K, force):
     m_units = -(-(-(-N // 128)) // 2)
     # each m-unit's pieces (its even CTA's tiles) as linear k-block ranges of [0, n_tiles * KB)
     per_v = {}
-    for e, mt, nt, s, S, kb0, kb1, _ in tiles:
+    for e, mt, nt, s, S, kb0, kb1, _ in tiles[:, :8]:
         if mt % 2 == 0:
             per_v.setdefault(mt // 2, []).append((nt * KB + kb0, nt * KB + kb1))
     assert len(per_v) == m_units

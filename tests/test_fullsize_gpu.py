@@ -266,3 +266,24 @@ def test_pair_cluster_split_bitwise_across_reductions_and_sm_caps(monkeypatch):
     monkeypatch.setenv("CAKE_GG_CSPLIT", "0")
     slots = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="fp32", deterministic=1)
     assert torch.equal(slots.view(torch.int32), ref.view(torch.int32))
+
+
+def test_nsplit_tail_two_experts(monkeypatch):
+    """Two experts of 16384 rows, 3072 x 4096, with the N-split tail rule on: a last wave of 40
+    of 76 pair units runs as 160 column pieces of 128; sampled against the oracle (every output
+    tile), and bitwise the plan without a tail split, also under SM caps."""
+    import torch
+    monkeypatch.setenv("CAKE_GG_NTAIL", "1")
+    wk = wl.Workload("moe_gate_up_E2_M32768_K4096_N3072", 2, 3072, 4096, wl.balanced_sizes(2, 32768))
+    plan = gg.cake_gg_plan("wgrad", wk.E, wk.M, wk.N, wk.K, "bf16", 1)
+    assert plan.tail_nsplit == 4 and plan.tail_units == 40
+    run_and_check(wk, "wgrad", "bf16", 1, np.random.default_rng(35))
+    X, W, G, _ = inputs(wk)
+    offs = torch.from_numpy(wk.offsets).cuda()
+    ref = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="bf16", deterministic=1)
+    for cap in (100, 0):
+        out = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="bf16", deterministic=1, max_sms=cap)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"max_sms={cap}"
+    monkeypatch.setenv("CAKE_GG_TAIL", "0")
+    whole = gg.grouped_gemm("wgrad", G, X, offs, out_dtype="bf16", deterministic=1)
+    assert torch.equal(whole.view(torch.int16), ref.view(torch.int16))

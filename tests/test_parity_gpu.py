@@ -331,6 +331,36 @@ def test_two_epilogue_groups_bitwise_equal_to_one(pass_, monkeypatch):
     assert torch.equal(two[:M].view(torch.int16), one[:M].view(torch.int16))
 
 
+@pytest.mark.parametrize("nq,det,out_dtype", [("4", 1, "fp32"), ("4", 0, "bf16"), ("2", 1, "bf16")])
+@pytest.mark.parametrize("max_sms", [0, 8])
+def test_nsplit_tail_weight_gradient(nq, det, out_dtype, max_sms, monkeypatch):
+    """256 x 512 weight-gradient tiles whose last units run as 2 or 4 column pieces, each over
+    all of its expert's k-blocks: ragged experts (one of 7600 rows: a partial last stage), a
+    partial last column tile (1152 = 2 x 512 + 128: pieces past K store nothing), every unit a
+    tail unit; on 8 SMs four pairs take every piece in turn."""
+    monkeypatch.setenv("CAKE_GG_WIDE", "2")
+    monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "0")
+    monkeypatch.setenv("CAKE_GG_NTAIL", nq)
+    plan = gg.cake_gg_plan("wgrad", 2, 16604, 256, 1152, out_dtype, det)
+    assert plan.tile_n == 512 and plan.tail_nsplit == int(nq) and plan.tail_units == 6
+    check_case("wgrad", [9000, 7600], 256, 1152, out_dtype, det, seed=33, extra_rows=4, max_sms=max_sms)
+
+
+def test_nsplit_tail_bitwise_equal_to_whole_units(monkeypatch):
+    """N-split tail pieces sum the same k-blocks in the same order as the whole unit: the bits of
+    the plan without a tail split."""
+    import torch
+    monkeypatch.setenv("CAKE_GG_WIDE", "2")
+    monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", "0")
+    Xb, Wb, Gb, off = make_inputs([9000, 7600], 256, 1152, seed=34, extra_rows=4)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    monkeypatch.setenv("CAKE_GG_NTAIL", "4")
+    pieces = run("wgrad", X, W, G, off, "fp32", 1)
+    monkeypatch.setenv("CAKE_GG_TAIL", "0")
+    whole = run("wgrad", X, W, G, off, "fp32", 1)
+    assert torch.equal(pieces.view(torch.int32), whole.view(torch.int32))
+
+
 @pytest.mark.parametrize("det", [1, 0])
 def test_thin_weight_gradient_through_workspace_slots(det, monkeypatch):
     """The same thin shape with the cluster reduction disabled: partials through the workspace."""
