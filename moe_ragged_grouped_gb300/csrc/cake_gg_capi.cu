@@ -67,9 +67,9 @@ double split_overhead_kb(int bn, int bk)
     return partial_kb + 4.0 / kps;
 }
 
-int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn, int bk, int64_t tail_s)
+int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn, int bk, int64_t tail_s,
+                           double *best_cost = nullptr)
 {
-    if (out_tiles <= 0 || kblocks_per_expert < 2 * kMinSplitChunk) return 0;
     const double c_split = split_overhead_kb(bn, bk);
     auto cost = [&](int64_t S) {
         const int64_t units = out_tiles * S;
@@ -85,14 +85,17 @@ int32_t choose_split_chunk(int64_t out_tiles, int64_t kblocks_per_expert, int bn
         return double(waves) * per;
     };
     int64_t best_s = 1;
-    double best = cost(1);
-    for (int64_t S = 2; S <= 64 && kblocks_per_expert / S >= kMinSplitChunk; ++S) {
-        const double c = cost(S);
-        if (c < best * 0.97) {
-            best = c;
-            best_s = S;
+    double best = out_tiles > 0 ? cost(1) : 0.0;
+    if (out_tiles > 0 && kblocks_per_expert >= 2 * kMinSplitChunk) {
+        for (int64_t S = 2; S <= 64 && kblocks_per_expert / S >= kMinSplitChunk; ++S) {
+            const double c = cost(S);
+            if (c < best * 0.97) {
+                best = c;
+                best_s = S;
+            }
         }
     }
+    if (best_cost) *best_cost = best;   // (in k-blocks of bn x bk per CTA)
     if (best_s == 1) return 0;
     return int32_t((kblocks_per_expert + best_s - 1) / best_s);
 }
@@ -886,10 +889,45 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     const int env_wide = (drop & kRuleWide) ? 0 : env_int("CAKE_GG_WIDE", 1);   // 0 off, 1 by the rule, 2 wherever they fit
     const int64_t wide_units = int64_t(E) * ((N + 2 * kTileM - 1) / (2 * kTileM)) * ((int64_t(K) + 511) / 512);
     if (pass == CAKE_GG_WGRAD && plan->pair == 2 && !plan->swap_ab && bn == 256 && K >= 1024 &&
-        M_max / E >= 4096 && (wide_units >= kWaveCtas / 2 || env_wide == 2) && env_wide != 0) {
-        bn = 512;
-        plan->tile_n = bn;
-        wide = true;
+        M_max / E >= 4096 && env_wide != 0) {
+        bool take = wide_units >= kWaveCtas / 2 || env_wide == 2;
+        if (!take) {
+            // fewer wide tiles than half a wave: take them when the 256-wide plan
+            // would split through workspace slots (several clusters' worth of
+            // tiles, no on-chip reduction) and the wide tiles, split as the split
+            // model splits them, finish no later (waves x k-blocks per unit, in
+            // FLOPs).  Dense 5120 -> 512: 20 wide tiles x 3 splits in one wave,
+            // against 40 x 3 in two -- the same FLOPs per pair, a quarter fewer
+            // operand bytes per FLOP and half the partial tiles: 77 against 86 us.
+            const int64_t rows = M_max / E;
+            const Geom g2 = make_geom(kModeWgrad, E, N, K, M_max, 256, 0, 0, 2);
+            const Geom g5 = make_geom(kModeWgrad, E, N, K, M_max, 512, 0, 0, 2);
+            const int64_t kb2 = (rows + 127) / 128, kb5 = (rows + 63) / 64;
+            const int64_t t2 = int64_t(m_units_w(g2)) * g2.n_tiles * E;   // pair tiles
+            const int64_t t5 = int64_t(m_units_w(g5)) * g5.n_tiles * E;
+            // (each width's split as the rules would choose it, split tail included;
+            // the decided points are left out: a plan measured at such a point
+            // keeps its width)
+            int32_t tu2 = 0, ts2 = 0, tu5 = 0, ts5 = 0;
+            if (env_int("CAKE_GG_TAIL", 1) != 0) {
+                choose_tail(E, N, K, M_max, 256, 128, 2, &tu2, &ts2);
+                choose_tail(E, N, K, M_max, 512, 64, 2, &tu5, &ts5);
+            }
+            const int32_t ch2 = choose_split_chunk(2 * t2, kb2, 256, 128, ts2);
+            const int32_t ch5 = choose_split_chunk(2 * t5, kb5, 512, 64, ts5);
+            const int64_t s2 = ch2 > 0 ? (kb2 + ch2 - 1) / ch2 : 1;
+            const int64_t s5 = ch5 > 0 ? (kb5 + ch5 - 1) / ch5 : 1;
+            const int64_t P = kWaveCtas / 2;
+            const double m2 = double((t2 * s2 + P - 1) / P) * double(ch2 > 0 ? ch2 : kb2) * 256.0 * 128.0;
+            const double m5 = double((t5 * s5 + P - 1) / P) * double(ch5 > 0 ? ch5 : kb5) * 512.0 * 64.0;
+            const bool on_chip2 = E == 1 && s2 >= 2 && s2 <= 4 && t2 <= resident_pair_clusters(int(s2));
+            take = s2 > 1 && !on_chip2 && m5 <= m2;
+        }
+        if (take) {
+            bn = 512;
+            plan->tile_n = bn;
+            wide = true;
+        }
     }
     if (pass != CAKE_GG_WGRAD && plan->pair == 2 && bn == 256 && out_w % 512 == 0 &&
         (pass == CAKE_GG_FWD ? K : N) >= 1024 && env_int("CAKE_GG_WIDE_FD", 0) != 0) {

@@ -209,6 +209,20 @@ def test_tile_walk_pair_cluster_split_with_small_and_empty_experts():
     assert plan.pair == 2 and plan.cluster_splits == 3
 
 
+def test_few_tile_weight_gradient_width_choice():
+    """Few-tile dense weight gradients (T = 16384): 5120 -> 512 takes 256 x 512 tiles split in
+    three (20 x 3 units in one wave instead of 40 x 3 in two); 4096 -> 512 keeps 256-wide tiles
+    reduced on chip; 4096 -> 1024 and 5120 -> 1024 keep 256-wide tiles (unsplit / split tail)."""
+    p = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
+    assert (p.tile_n, p.tile_k, p.split_chunk) == (512, 64, 86)
+    p = gg.cake_gg_plan("wgrad", 1, 16384, 512, 4096, "fp32", 1)
+    assert p.tile_n == 256 and p.cluster_splits == 2
+    p = gg.cake_gg_plan("wgrad", 1, 16384, 1024, 4096, "fp32", 1)
+    assert p.tile_n == 256 and p.split_chunk == 0
+    p = gg.cake_gg_plan("wgrad", 1, 16384, 1024, 5120, "fp32", 1)
+    assert p.tile_n == 256 and (p.tail_units, p.tail_splits) == (4, 8)
+
+
 def test_pair_cluster_split_needs_every_cluster_resident():
     # 5120 -> 512: 40 pair tiles, more two-pair clusters than fit at once -> global split slots
     plan = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
