@@ -430,15 +430,15 @@ int resident_pair_clusters(int S)
 }
 
 // A cluster split: swapped single CTAs (a receive buffer of their own), or
-// pairs of at most 256-column tiles whose receive buffer fits their ring (the
+// pairs whose receive window fits their ring in at most 4 rounds (the
 // cluster, 2 CTAs per split, within the portable size).
 bool cluster_split_fits(const cake_gg_plan_t &pl)
 {
     const int S = pl.cluster_splits;
     if (pl.swap_ab) return pl.pair == 1 && S <= kMaxClusterSplit;
-    return pl.pair == 2 && pl.tile_n <= 256 && 2 * S <= kMaxClusterSplit &&
-           pair_csplit_ring_bytes(pl.tile_n, S, pl.out_dtype == CAKE_GG_FP32) <=
-               size_t(pl.stages) * stage_bytes_for(pl.tile_n, pl.tile_k / 64, 2);
+    return pl.pair == 2 && pl.tile_n <= 512 && 2 * S <= kMaxClusterSplit &&
+           pair_csplit_rounds(pl.tile_n, S, pl.out_dtype == CAKE_GG_FP32,
+                              size_t(pl.stages) * stage_bytes_for(pl.tile_n, pl.tile_k / 64, 2)) > 0;
 }
 
 // Checks shared by the three compute calls.
@@ -455,8 +455,7 @@ int check_call(const cake_gg_plan_t *plan, int pass, const void *a, const void *
         (plan->pair != 1 && plan->pair != 2) ||
         (plan->pair == 2 && (plan->tile_n % 128 != 0 || (pass == CAKE_GG_WGRAD && plan->swap_ab))) ||
         plan->tile_n < 64 || plan->tile_n % 64 != 0 || plan->stages < 2 ||
-        (plan->tile_n > 256 && (plan->tile_n != 512 || plan->pair != 2 || plan->swap_ab ||
-                                plan->tile_k != 64 || plan->cluster_splits > 0)) ||
+        (plan->tile_n > 256 && (plan->tile_n != 512 || plan->pair != 2 || plan->swap_ab || plan->tile_k != 64)) ||
         plan->stages > kMaxStages || plan->split_chunk < 0 ||
         (plan->staging_bufs != 1 && plan->staging_bufs != 2) || plan->cluster_splits < 0 ||
         plan->cluster_splits > kMaxClusterSplit ||
@@ -1073,7 +1072,7 @@ int cake_gg_plan(cake_gg_plan_t *plan, int pass, int32_t E, int64_t M_max, int32
     const bool auto_cs = E == 1 && !(env_chunk && *env_chunk) && env_cs != 0 && !(drop & kRuleCsplit) &&
                          plan->split_chunk > 0 &&
                          plan->tail_splits == 0 && plan->streamk_kblocks == 0;
-    if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->pair == 2 && bn <= 256 && (auto_cs || env_cs >= 2)) {
+    if (pass == CAKE_GG_WGRAD && !plan->swap_ab && plan->pair == 2 && bn <= 512 && (auto_cs || env_cs >= 2)) {
         const int64_t kbe = (M_max / E + bk - 1) / bk;
         const int64_t S = env_cs >= 2 ? env_cs : (kbe + plan->split_chunk - 1) / plan->split_chunk;
         const Geom g = make_geom(kModeWgrad, E, N, K, M_max, bn, 0, 0, 2, bk);

@@ -152,14 +152,26 @@ __host__ __device__ constexpr size_t csplit_bytes_for(int bn, int csplit, int pa
 // and the ring bytes it takes: the receive buffer (the S - 1 peers' parts of
 // the slice), then the slice's output staged for TMA stores (per warp, one 4 KB slab of
 // 32 rows x 128 bytes per 128-byte row chunk).
-__host__ __device__ constexpr int pair_csplit_per(int cols4, int csplit, bool out_f32)
+// A slice too large for the ring is reduced in `rounds` windows of per / rounds
+// columns (per a multiple of rounds row chunks).
+__host__ __device__ constexpr int pair_csplit_per(int cols4, int csplit, bool out_f32, int rounds = 1)
 {
-    return ((cols4 + csplit - 1) / csplit + (out_f32 ? 8 : 16) - 1) / (out_f32 ? 8 : 16) * (out_f32 ? 8 : 16);
+    return ((cols4 + csplit - 1) / csplit + rounds * (out_f32 ? 8 : 16) - 1) / (rounds * (out_f32 ? 8 : 16)) *
+           (rounds * (out_f32 ? 8 : 16));
 }
-__host__ __device__ constexpr size_t pair_csplit_ring_bytes(int bn, int csplit, bool out_f32)
+__host__ __device__ constexpr size_t pair_csplit_ring_bytes(int bn, int csplit, bool out_f32, int rounds = 1)
 {
-    return size_t(csplit - 1) * size_t(pair_csplit_per(bn / 4, csplit, out_f32)) * size_t(kTileM) * 16u +
-           4u * size_t(pair_csplit_per(bn / 4, csplit, out_f32) / (out_f32 ? 8 : 16)) * 4096u;
+    return size_t(csplit - 1) * size_t(pair_csplit_per(bn / 4, csplit, out_f32, rounds) / rounds) * size_t(kTileM) *
+               16u +
+           4u * size_t(pair_csplit_per(bn / 4, csplit, out_f32, rounds) / rounds / (out_f32 ? 8 : 16)) * 4096u;
+}
+// Fewest rounds (1, 2 or 4) whose window fits a ring of ring_bytes; 0 if none.
+__host__ __device__ constexpr int pair_csplit_rounds(int bn, int csplit, bool out_f32, size_t ring_bytes)
+{
+    return pair_csplit_ring_bytes(bn, csplit, out_f32, 1) <= ring_bytes   ? 1
+           : pair_csplit_ring_bytes(bn, csplit, out_f32, 2) <= ring_bytes ? 2
+           : pair_csplit_ring_bytes(bn, csplit, out_f32, 4) <= ring_bytes ? 4
+                                                                          : 0;
 }
 
 __host__ __device__ constexpr size_t smem_bytes_for(int bn, int stages, int kps, int staging_bufs, int csplit,
@@ -1169,6 +1181,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
         const int ngroups = p.epi_groups == 2 && nacc == 2 ? 2 : 1;
         const uint32_t ebar = eg == 0 ? 1u : 3u;   // the group's named barrier
         const int etid = (tid - 64) & 127; // 0..127 within the group
+        // cluster split of pairs: rounds of the reduction (a slice wider than the ring holds)
+        const int cs_rounds =
+            PAIR == 2 && csplit > 0 ? pair_csplit_rounds(p.bn, csplit, OUT_F32, size_t(p.stages) * stage_bytes) : 1;
         uint8_t *const stg_base = staging + size_t(eg) * p.staging_bufs * kStagingBytes;
         int it = 0;
         int cs_it = 0;                     // cluster-split tiles reduced so far
@@ -1224,8 +1239,9 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
             // cluster split: this CTA's float4 columns [q0, q1) of the tile's nq
             // (pairs: whole 128-byte output rows per owner, stored by TMA)
             const int nq = (cols_valid > 0 ? cols_valid : 0) / 4;
-            const int per_c = csplit > 0 ? (PAIR == 2 ? pair_csplit_per(nq, csplit, OUT_F32) : (nq + csplit - 1) / csplit)
-                                         : 1;
+            const int per_c = csplit > 0
+                                  ? (PAIR == 2 ? pair_csplit_per(nq, csplit, OUT_F32, cs_rounds) : (nq + csplit - 1) / csplit)
+                                  : 1;
             const int per = per_c > 0 ? per_c : 1;   // (>= 1: also keeps pruned code free of a zero divisor)
             const int q0 = srank * per;
             const int q1 = q0 + per < nq ? q0 + per : nq;
@@ -1261,151 +1277,179 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 uint8_t *rec = kRing ? ring : reinterpret_cast<uint8_t *>(red_buf);
                 const uint32_t rec_u32 = smem_u32(rec);
                 if (kRing) {
-                    if (etid == 0) {
-                        mbar_arrive(smem_u32(&c->red_ready));
+                    // R rounds, round r taking columns [o per + r pr, o per + (r + 1) pr)
+                    // of every owner o's slice (pr = per / R): the receive buffer and the
+                    // staged output are one window's
+                    const int pr = per / (cs_rounds > 0 ? cs_rounds : 1);
+                    bool cs_ok = true;
+                    for (int rd = 0; rd < cs_rounds; ++rd) {
+                        if (rd > 0) {
+                            // the previous window is summed and its slabs' stores have read
+                            // them: this CTA's window is free again
+                            if (lane == 0) bulk_wait_read_all();
+                            __syncwarp();
+                            fence_proxy_async_smem();
+                            named_bar_sync(ebar, 128);
+                            cs_open = true;
+                        }
+                        if (etid == 0) {
+                            mbar_arrive(smem_u32(&c->red_ready));
+                            for (int j = 0; j < csplit; ++j)
+                                mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_consumed), uint32_t(j * PAIR + half)));
+                        }
+                        cs_armed = true;
+                        bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t(cs_it & 1), c, p);
+                        if (!named_bar_and(ebar, 128, okc)) {
+                            cs_ok = false;
+                            break;
+                        }
+                        // Pairs: each owner's window of the other splits' partials goes out
+                        // straight from TMEM (whole 32-column chunks: pr is a multiple of 8)
+                        // as plain stores into the owner's ring, rec[s'][q - q_window][row]
+                        // with s' the pusher's split among the owner's S - 1 peers; the
+                        // owner's own part stays in TMEM until its sum.
+                        for (int o = 0; o < csplit; ++o) {
+                            if (o == srank) continue;
+                            const int qa = o * per + rd * pr;
+                            const int qb = qa + pr < nq ? qa + pr : nq;
+                            const int slot = srank < o ? srank : srank - 1;
+                            const uint32_t rbase = map_to_cta(
+                                rec_u32 + uint32_t((slot * pr * kTileM + lrow) * 16), uint32_t(o * PAIR + half));
+                            for (int qc = qa; qc < qb; qc += 16) {   // two 32-column chunks per TMEM wait
+                                uint32_t r0[32], r1[32];
+                                const bool two = qc + 8 < qb;
+                                if (empty_tile) {
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                                } else {
+                                    tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc), r0);
+                                    if (two) tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc + 32), r1);
+                                    tmem_ld_wait();
+                                }
+#pragma unroll
+                                for (int j4 = 0; j4 < 16; ++j4) {
+                                    const uint32_t *rr = j4 < 8 ? r0 : r1;
+                                    const int jj = j4 & 7;
+                                    if (qc + j4 < qb)
+                                        st_cluster_v4(rbase + uint32_t((qc + j4 - qa) * kTileM * 16),
+                                                      make_float4(__uint_as_float(rr[4 * jj]),
+                                                                  __uint_as_float(rr[4 * jj + 1]),
+                                                                  __uint_as_float(rr[4 * jj + 2]),
+                                                                  __uint_as_float(rr[4 * jj + 3])));
+                                }
+                            }
+                        }
+                        // plain stores, made visible by one release arrival per thread on
+                        // every other owner (fewer barrier updates than a byte count per store)
                         for (int j = 0; j < csplit; ++j)
-                            mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_consumed), uint32_t(j * PAIR + half)));
-                    }
-                    cs_armed = true;
-                    bool okc = cluster_wait(smem_u32(&c->red_consumed), uint32_t(cs_it & 1), c, p);
-                    if (!named_bar_and(ebar, 128, okc)) break;
-                    // Pairs: each owner's slice of the other splits' partials goes out
-                    // straight from TMEM (whole 32-column chunks: per is a multiple of 8)
-                    // as plain stores into the owner's ring, rec[s'][q - q_owner][row]
-                    // with s' the pusher's split among the owner's S - 1 peers; the
-                    // owner's own part stays in TMEM until its sum.
-                    for (int o = 0; o < csplit; ++o) {
-                        if (o == srank) continue;
-                        const int qa = o * per;
-                        const int qb = qa + per < nq ? qa + per : nq;
-                        const int slot = srank < o ? srank : srank - 1;
-                        const uint32_t rbase = map_to_cta(
-                            rec_u32 + uint32_t((slot * per * kTileM + lrow) * 16), uint32_t(o * PAIR + half));
-                        for (int qc = qa; qc < qb; qc += 16) {   // two 32-column chunks per TMEM wait
-                            uint32_t r0[32], r1[32];
-                            const bool two = qc + 8 < qb;
+                            if (j != srank)
+                                mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), uint32_t(j * PAIR + half)));
+                        bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
+                        if (!named_bar_and(ebar, 128, okr)) {
+                            cs_ok = false;
+                            break;
+                        }
+                        cs_open = false;   // every peer's part of the window has landed
+                        ++cs_it;
+                        // My window, summed over the splits in split order (s = 0, 1, ...,
+                        // S - 1; this CTA's own part from TMEM), staged per warp in the ring
+                        // after the receive buffer as 4 KB slabs (32 rows x one 128-byte
+                        // output row chunk) whose TMA stores go out back to back.
+                        constexpr int CW = OUT_F32 ? 32 : 64;   // columns per 128-byte output row
+                        constexpr int C4 = CW / 4;
+                        const int w0 = q0 + rd * pr;
+                        const int w1 = w0 + pr < q1 ? w0 + pr : q1;
+                        const uint32_t ostg = rec_u32 + uint32_t(csplit - 1) * uint32_t(pr) * kTileM * 16u +
+                                              uint32_t(q) * uint32_t(pr / C4) * 4096u;
+                        const bool stage_out = p.tma_store && ti.valid && q * 32 < rows_valid;
+                        for (int qc = w0; qc < w1; qc += C4) {
+                            // this CTA's own part of the row chunk, from TMEM
+                            uint32_t own[CW];
                             if (empty_tile) {
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) r0[j] = r1[j] = 0u;
+                                for (int j = 0; j < CW; ++j) own[j] = 0u;
                             } else {
-                                tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc), r0);
-                                if (two) tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc + 32), r1);
+                                tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc), *reinterpret_cast<uint32_t(*)[32]>(own));
+                                if (CW == 64)
+                                    tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc + 32),
+                                                       *reinterpret_cast<uint32_t(*)[32]>(own + (CW == 64 ? 32 : 0)));
                                 tmem_ld_wait();
                             }
-#pragma unroll
-                            for (int j4 = 0; j4 < 16; ++j4) {
-                                const uint32_t *rr = j4 < 8 ? r0 : r1;
-                                const int jj = j4 & 7;
-                                if (qc + j4 < qb)
-                                    st_cluster_v4(rbase + uint32_t((qc + j4 - qa) * kTileM * 16),
-                                                  make_float4(__uint_as_float(rr[4 * jj]), __uint_as_float(rr[4 * jj + 1]),
-                                                              __uint_as_float(rr[4 * jj + 2]),
-                                                              __uint_as_float(rr[4 * jj + 3])));
-                            }
-                        }
-                    }
-                    // plain stores, made visible by one release arrival per thread on
-                    // every other owner (fewer barrier updates than a byte count per store)
-                    for (int j = 0; j < csplit; ++j)
-                        if (j != srank)
-                            mbar_arrive_cluster(map_to_cta(smem_u32(&c->red_ready), uint32_t(j * PAIR + half)));
-                    bool okr = cluster_wait(smem_u32(&c->red_ready), uint32_t(cs_it & 1), c, p);
-                    if (!named_bar_and(ebar, 128, okr)) break;
-                    cs_open = false;   // every peer's part of the slice has landed
-                    // My slice, summed over the splits in split order (s = 0, 1, ..., S - 1;
-                    // this CTA's own part from TMEM), staged per warp in the ring after the
-                    // receive buffer as 4 KB slabs (32 rows x one 128-byte output row chunk)
-                    // whose TMA stores go out back to back.
-                    constexpr int CW = OUT_F32 ? 32 : 64;   // columns per 128-byte output row
-                    constexpr int C4 = CW / 4;
-                    const uint32_t ostg = rec_u32 + uint32_t(csplit - 1) * uint32_t(per) * kTileM * 16u +
-                                          uint32_t(q) * uint32_t(per / C4) * 4096u;
-                    const bool stage_out = p.tma_store && ti.valid && q * 32 < rows_valid;
-                    for (int qc = q0; qc < q1; qc += C4) {
-                        // this CTA's own part of the row chunk, from TMEM
-                        uint32_t own[CW];
-                        if (empty_tile) {
-#pragma unroll
-                            for (int j = 0; j < CW; ++j) own[j] = 0u;
-                        } else {
-                            tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc), *reinterpret_cast<uint32_t(*)[32]>(own));
-                            if (CW == 64)
-                                tmem_ld_32x32b_x32(t_row + uint32_t(4 * qc + 32),
-                                                   *reinterpret_cast<uint32_t(*)[32]>(own + (CW == 64 ? 32 : 0)));
-                            tmem_ld_wait();
-                        }
-                        const int col = qc * 4;
-                        const bool live = ti.valid && col < cols_valid;
-                        uint32_t w[32];   // the chunk's 128-byte output row
-                        const uint32_t src0 = rec_u32 + uint32_t(((qc - q0) * kTileM + lrow) * 16);
-                        const uint32_t sstride = uint32_t(per) * kTileM * 16u;   // between peers' parts
-#pragma unroll
-                        for (int j = 0; j < C4; ++j) {
-                            float4 a = make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
-                                                   __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]));
-                            const uint32_t sj = src0 + uint32_t(j * kTileM * 16);
-                            if (csplit == 2) {
-                                // two splits: p0 + p1 == p1 + p0 (one rounding either way)
-                                const float4 b = lds_v4(sj);
-                                a.x += b.x;
-                                a.y += b.y;
-                                a.z += b.z;
-                                a.w += b.w;
-                            } else {
-                                // split order s = 0, 1, ..., S - 1 with this CTA's own part at srank
-                                float4 t = srank == 0 ? a : lds_v4(sj);
-#pragma unroll 1
-                                for (int sp = 1; sp < csplit; ++sp) {
-                                    const float4 b = sp == srank ? a : lds_v4(sj + uint32_t(sp - (sp > srank)) * sstride);
-                                    t.x += b.x;
-                                    t.y += b.y;
-                                    t.z += b.z;
-                                    t.w += b.w;
-                                }
-                                a = t;
-                            }
-                            if (OUT_F32) {
-                                w[4 * j] = __float_as_uint(a.x);
-                                w[4 * j + 1] = __float_as_uint(a.y);
-                                w[4 * j + 2] = __float_as_uint(a.z);
-                                w[4 * j + 3] = __float_as_uint(a.w);
-                            } else {
-                                w[2 * j] = pack_bf16x2(a.x, a.y);
-                                w[2 * j + 1] = pack_bf16x2(a.z, a.w);
-                            }
-                        }
-                        if (!p.tma_store && live && row_ok) {
-                            // no TMA stores: the row chunk's float4 columns straight to its row
+                            const int col = qc * 4;
+                            const bool live = ti.valid && col < cols_valid;
+                            uint32_t w[32];   // the chunk's 128-byte output row
+                            const uint32_t src0 = rec_u32 + uint32_t(((qc - w0) * kTileM + lrow) * 16);
+                            const uint32_t sstride = uint32_t(pr) * kTileM * 16u;   // between peers' parts
 #pragma unroll
                             for (int j = 0; j < C4; ++j) {
-                                if (qc + j >= q1 || col + 4 * j >= cols_valid) continue;
-                                const int64_t o = out_base + int64_t(lrow) * ld + col + 4 * j;
-                                if (OUT_F32)
-                                    *reinterpret_cast<uint4 *>(static_cast<float *>(p.out) + o) =
-                                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                                else
-                                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + o) =
-                                        make_uint2(w[2 * j], w[2 * j + 1]);
+                                float4 a = make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                                       __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]));
+                                const uint32_t sj = src0 + uint32_t(j * kTileM * 16);
+                                if (csplit == 2) {
+                                    // two splits: p0 + p1 == p1 + p0 (one rounding either way)
+                                    const float4 b = lds_v4(sj);
+                                    a.x += b.x;
+                                    a.y += b.y;
+                                    a.z += b.z;
+                                    a.w += b.w;
+                                } else {
+                                    // split order s = 0, 1, ..., S - 1 with this CTA's own part at srank
+                                    float4 t = srank == 0 ? a : lds_v4(sj);
+#pragma unroll 1
+                                    for (int sp = 1; sp < csplit; ++sp) {
+                                        const float4 b =
+                                            sp == srank ? a : lds_v4(sj + uint32_t(sp - (sp > srank)) * sstride);
+                                        t.x += b.x;
+                                        t.y += b.y;
+                                        t.z += b.z;
+                                        t.w += b.w;
+                                    }
+                                    a = t;
+                                }
+                                if (OUT_F32) {
+                                    w[4 * j] = __float_as_uint(a.x);
+                                    w[4 * j + 1] = __float_as_uint(a.y);
+                                    w[4 * j + 2] = __float_as_uint(a.z);
+                                    w[4 * j + 3] = __float_as_uint(a.w);
+                                } else {
+                                    w[2 * j] = pack_bf16x2(a.x, a.y);
+                                    w[2 * j + 1] = pack_bf16x2(a.z, a.w);
+                                }
                             }
-                        }
-                        if (stage_out && live) {
-                            // a 4 KB slab: 32 rows x 128 bytes, 128-byte swizzle (rows past the
-                            // output and columns past the slice's end are clipped by the map)
-                            const uint32_t slab = ostg + uint32_t((qc - q0) / C4) * 4096u;
-                            const uint32_t rowp = slab + uint32_t(lane) * 128u;
+                            if (!p.tma_store && live && row_ok) {
+                                // no TMA stores: the row chunk's float4 columns straight to its row
 #pragma unroll
-                            for (int ch = 0; ch < 8; ++ch)
-                                sts_v4(rowp + uint32_t((ch ^ (lane & 7)) << 4), w[4 * ch], w[4 * ch + 1], w[4 * ch + 2],
-                                       w[4 * ch + 3]);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_store_3d(&mapOut, slab, ti.nt * p.bn + col, ti.mt * kTileM + q * 32, ti.e);
-                                bulk_commit_group();
+                                for (int j = 0; j < C4; ++j) {
+                                    if (qc + j >= w1 || col + 4 * j >= cols_valid) continue;
+                                    const int64_t o = out_base + int64_t(lrow) * ld + col + 4 * j;
+                                    if (OUT_F32)
+                                        *reinterpret_cast<uint4 *>(static_cast<float *>(p.out) + o) =
+                                            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                                    else
+                                        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + o) =
+                                            make_uint2(w[2 * j], w[2 * j + 1]);
+                                }
                             }
-                            __syncwarp();
+                            if (stage_out && live) {
+                                // a 4 KB slab: 32 rows x 128 bytes, 128-byte swizzle (rows past the
+                                // output and columns past the slice's end are clipped by the map)
+                                const uint32_t slab = ostg + uint32_t((qc - w0) / C4) * 4096u;
+                                const uint32_t rowp = slab + uint32_t(lane) * 128u;
+#pragma unroll
+                                for (int ch = 0; ch < 8; ++ch)
+                                    sts_v4(rowp + uint32_t((ch ^ (lane & 7)) << 4), w[4 * ch], w[4 * ch + 1],
+                                           w[4 * ch + 2], w[4 * ch + 3]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_3d(&mapOut, slab, ti.nt * p.bn + col, ti.mt * kTileM + q * 32, ti.e);
+                                    bulk_commit_group();
+                                }
+                                __syncwarp();
+                            }
                         }
                     }
+                    if (!cs_ok) break;
                     // the accumulator is read: free for the MMA warp (of the even CTA)
                     tc_fence_before_sync();
                     __syncwarp();
@@ -1420,7 +1464,6 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                     fence_proxy_async_smem();
                     named_bar_sync(ebar, 128);
                     if (etid == 0) mbar_arrive(smem_u32(&c->ring_free));
-                    ++cs_it;
                     continue;
                 } else {
                     if (cs_it > 0) {

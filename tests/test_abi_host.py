@@ -211,10 +211,11 @@ def test_tile_walk_pair_cluster_split_with_small_and_empty_experts():
 
 def test_few_tile_weight_gradient_width_choice():
     """Few-tile dense weight gradients (T = 16384): 5120 -> 512 takes 256 x 512 tiles split in
-    three (20 x 3 units in one wave instead of 40 x 3 in two); 4096 -> 512 keeps 256-wide tiles
-    reduced on chip; 4096 -> 1024 and 5120 -> 1024 keep 256-wide tiles (unsplit / split tail)."""
+    three (20 x 3 units in one wave instead of 40 x 3 in two), reduced on chip by clusters of
+    three pairs; 4096 -> 512 keeps 256-wide tiles reduced on chip; 4096 -> 1024 and 5120 -> 1024
+    keep 256-wide tiles (unsplit / split tail)."""
     p = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
-    assert (p.tile_n, p.tile_k, p.split_chunk) == (512, 64, 86)
+    assert (p.tile_n, p.tile_k, p.cluster_splits, p.split_chunk, p.workspace_bytes) == (512, 64, 3, 0, 256)
     p = gg.cake_gg_plan("wgrad", 1, 16384, 512, 4096, "fp32", 1)
     assert p.tile_n == 256 and p.cluster_splits == 2
     p = gg.cake_gg_plan("wgrad", 1, 16384, 1024, 4096, "fp32", 1)
@@ -224,9 +225,14 @@ def test_few_tile_weight_gradient_width_choice():
 
 
 def test_pair_cluster_split_needs_every_cluster_resident():
-    # 5120 -> 512: 40 pair tiles, more two-pair clusters than fit at once -> global split slots
-    plan = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
-    assert plan.cluster_splits == 0 and plan.split_chunk > 0
+    # 5120 -> 512 with 256-wide tiles: 40 pair tiles split in three, more clusters of three
+    # pairs than fit at once (23) -> global split slots
+    os.environ["CAKE_GG_WIDE"] = "0"
+    try:
+        plan = gg.cake_gg_plan("wgrad", 1, 16384, 512, 5120, "fp32", 1)
+    finally:
+        del os.environ["CAKE_GG_WIDE"]
+    assert plan.tile_n == 256 and plan.cluster_splits == 0 and plan.split_chunk > 0
 
 
 def test_tile_walk_nsplit_tail_two_experts():

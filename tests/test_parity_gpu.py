@@ -331,6 +331,35 @@ def test_two_epilogue_groups_bitwise_equal_to_one(pass_, monkeypatch):
     assert torch.equal(two[:M].view(torch.int16), one[:M].view(torch.int16))
 
 
+@pytest.mark.parametrize("csplit,out_dtype", [("2", "fp32"), ("3", "fp32"), ("4", "fp32"), ("3", "bf16")])
+@pytest.mark.parametrize("max_sms", [0, 12])
+def test_wide_pair_cluster_split_in_rounds(csplit, out_dtype, max_sms, monkeypatch):
+    """256 x 512 pair tiles split by clusters of S pairs: each owner's slice is wider than the
+    ring holds at once, so the reduction runs in rounds over column windows of it (the receive
+    buffer and the staged output one window's); ragged experts, a partial last column tile
+    (1152 = 2 x 512 + 128), and on 12 SMs one or two clusters taking every tile in turn."""
+    monkeypatch.setenv("CAKE_GG_WIDE", "2")
+    monkeypatch.setenv("CAKE_GG_CSPLIT", csplit)
+    plan = gg.cake_gg_plan("wgrad", 2, 16604, 256, 1152, out_dtype, 1)
+    assert plan.tile_n == 512 and plan.pair == 2 and plan.cluster_splits == int(csplit)
+    check_case("wgrad", [9000, 7600], 256, 1152, out_dtype, 1, seed=36, extra_rows=4, max_sms=max_sms)
+
+
+def test_wide_pair_cluster_split_bitwise_equal_to_workspace_slots(monkeypatch):
+    """Three splits of 256 x 512 tiles summed on chip in two rounds give the bits of the same
+    three splits summed from workspace slots."""
+    import torch
+    monkeypatch.setenv("CAKE_GG_WIDE", "2")
+    Xb, Wb, Gb, off = make_inputs([16600], 256, 1152, seed=37, extra_rows=4)
+    X, W, G = to_dev(Xb), to_dev(Wb), to_dev(Gb)
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "3")
+    on_chip = run("wgrad", X, W, G, off, "fp32", 1)
+    monkeypatch.setenv("CAKE_GG_CSPLIT", "0")
+    monkeypatch.setenv("CAKE_GG_SPLIT_CHUNK", str(-(-(-(-16600 // 64)) // 3)))
+    slots = run("wgrad", X, W, G, off, "fp32", 1)
+    assert torch.equal(on_chip.view(torch.int32), slots.view(torch.int32))
+
+
 @pytest.mark.parametrize("nq,det,out_dtype", [("4", 1, "fp32"), ("4", 0, "bf16"), ("2", 1, "bf16")])
 @pytest.mark.parametrize("max_sms", [0, 8])
 def test_nsplit_tail_weight_gradient(nq, det, out_dtype, max_sms, monkeypatch):
