@@ -225,6 +225,7 @@ constexpr DecidedPoint kDecidedPoints[] = {
     {1, 4096, 4096, 15565, 17203, kRuleWide},      // dense 4096 -> 4096, T = 16384
     {8, 4096, 6144, 124518, 137626, kRuleTail},    // gate_up E8 M131072 (N 4096, K 6144), balanced
     {1, 48, 4096, 15565, 17203, kRuleCsplit},      // dense 4096 -> 48, T = 16384
+    {1, 512, 5120, 15565, 17203, kRuleCsplit},     // dense 5120 -> 512, T = 16384
 };
 
 int decided_drop(int32_t E, int32_t N, int32_t K, int64_t M_max)

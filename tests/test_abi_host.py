@@ -367,6 +367,7 @@ def test_tile_walk_streamk_empty_expert_writes_zero_tiles():
     (1, 16384, 4096, 4096, "fp32", "tile_n", 512),        # 256 x 512 tiles dropped
     (8, 131072, 4096, 6144, "bf16", "tail_splits", 2),    # split tail dropped
     (1, 16384, 48, 4096, "fp32", "cluster_splits", 4),    # on-chip reduction dropped (workspace slots)
+    (1, 16384, 512, 5120, "fp32", "cluster_splits", 3),
 ])
 def test_nondeterministic_planner_drops_rules_that_failed_the_decision_protocol(E, M, N, K, od, field, det_value):
     """At points where a plan rule failed the pages' decision protocol (measured with bench.py
