@@ -89,15 +89,19 @@ def test_dropped_copy_in_a_cluster_split_times_out_and_context_survives():
     assert (np.abs(good.double().cpu().numpy() - ref) <= oracle.tolerance(ref, M, f(Gb), f(Xb))).all()
 
 
-def test_dropped_copy_in_a_pair_cluster_split_times_out_and_context_survives(monkeypatch):
-    """A weight gradient of 256-row pair tiles whose two splits run as one cluster of two pairs
-    (4 CTAs) and reduce into each other's operand rings.  The even CTA of the first cluster's
-    first pair loses its first copy: that pair's MMA never completes, the other pair waits in
-    vain for the first pair's ring to be offered, and every role gives up on its bounded wait.
-    The call reports CAKE_GG_ERR_TIMEOUT and the next regular call is correct."""
+@pytest.mark.parametrize("csplit,wide", [("2", False), ("3", True)])
+def test_dropped_copy_in_a_pair_cluster_split_times_out_and_context_survives(csplit, wide, monkeypatch):
+    """A weight gradient of 256-row pair tiles whose splits run as one cluster of pairs and
+    reduce into each other's operand rings (256 x 512 tiles: in rounds over column windows).
+    The even CTA of the first cluster's first pair loses its first copy: that pair's MMA never
+    completes, the other pairs wait in vain for the first pair's ring to be offered, and every
+    role gives up on its bounded wait.  The call reports CAKE_GG_ERR_TIMEOUT and the next
+    regular call is correct."""
     import torch
-    monkeypatch.setenv("CAKE_GG_CSPLIT", "2")
-    E, M, N, K = 1, 3000, 512, 512
+    monkeypatch.setenv("CAKE_GG_CSPLIT", csplit)
+    if wide:
+        monkeypatch.setenv("CAKE_GG_WIDE", "2")
+    E, M, N, K = (1, 8300, 256, 1152) if wide else (1, 3000, 512, 512)
     rng = np.random.default_rng(42)
     Xb = wl.randn_bf16((M, K), 1.0, rng)
     Gb = wl.randn_bf16((M, N), 1.0, rng)
@@ -105,7 +109,7 @@ def test_dropped_copy_in_a_pair_cluster_split_times_out_and_context_survives(mon
     X, G = wl.to_torch_bf16(Xb, "cuda"), wl.to_torch_bf16(Gb, "cuda")
     offs = torch.from_numpy(off).cuda()
     plan = gg.cake_gg_plan("wgrad", E, M, N, K, "fp32", 1)
-    assert plan.cluster_splits == 2 and plan.pair == 2
+    assert plan.cluster_splits == int(csplit) and plan.pair == 2 and plan.tile_n == (512 if wide else 256)
     plan.debug_flags = gg.CAKE_GG_DEBUG_DROP_FIRST_LOAD
     plan.timeout_ns = 100_000_000  # 0.1 s
     ws = gg.make_workspace(plan, "cuda")
