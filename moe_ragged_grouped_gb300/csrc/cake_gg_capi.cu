@@ -732,6 +732,12 @@ int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, f
     if (rc != CAKE_GG_OK) return rc;
     if ((rc = get_encoder()) != CAKE_GG_OK) return rc;
     const int N = plan->N, K = plan->K, bn = plan->tile_n, P = plan->pair;
+    // the tile shape and ring depth are the planner's (the tensor-memory A
+    // slots and the shared-memory layout depend on them)
+    cake_gg_plan_t ref;
+    if (router_plan(&ref, plan->M_max, N, K, plan->max_sms) != CAKE_GG_OK || ref.tile_n != bn || ref.pair != P ||
+        ref.stages != plan->stages || ref.tile_k != plan->tile_k || ref.staging_bufs != plan->staging_bufs)
+        return CAKE_GG_ERR_INVALID_ARG;
     const uint64_t M = uint64_t(plan->M_max);
     if (M == 0) return CAKE_GG_OK;
     CUtensorMap ma, mb, mo;
@@ -757,7 +763,7 @@ int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, f
     p.bk = 64;
     p.stages = plan->stages;
     p.det = 1;
-    p.tmem_cols = tmem_cols_for(bn);
+    p.tmem_cols = 512;   // the accumulator's 256 columns and the stages' A slots after it, whatever R
     p.tma_store = 1;
     p.epoch_word = reinterpret_cast<uint32_t *>(wsb + kEpochOffset);
     p.pdl = env_int("CAKE_GG_PDL", 1) != 0 ? 1 : 0;

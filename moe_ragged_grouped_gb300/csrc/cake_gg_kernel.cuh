@@ -917,6 +917,14 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                 // pairs to start hold two units while late ones find none)
                 const int32_t fetch_kb = ti.kb1 - (p.stages + 1) > ti.kb0 ? ti.kb1 - (p.stages + 1) : ti.kb0;
                 bool fetched = !(p.dyn && leader) || skw;
+                // (the router staggers each unit's k order: with one output-column
+                // tile every pair reads the same weight slices, and in lock step they
+                // would all read the same lines at once.  The unit's rotation is
+                // taken once here: a 64-bit remainder per stage sat between each
+                // stage's wait and its copies, on the one thread that issues them,
+                // and cost the router 6 %.)
+                const int32_t nk = ti.kb1 - ti.kb0;
+                const int32_t krot = RT && p.kstagger > 0 && nk > 0 ? int32_t((t * p.kstagger) % nk) : 0;
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
                     if (!fetched && kb == fetch_kb) {
                         nxt = atomicAdd(p.sched, 1);  // in flight while the copies go out
@@ -942,13 +950,10 @@ __global__ void __launch_bounds__(threads_for(KMODE), 1)
                         const int nb = p.bn / 64;
                         const int jb0 = PAIR == 2 ? half * nb / 2 : 0;
                         const int jb1 = PAIR == 2 ? (half + 1) * nb / 2 : nb;
-                        // (the router staggers each unit's k order: with one output-column
-                        // tile every pair reads the same weight slices, and in lock step
-                        // they would all read the same lines at once)
                         int32_t kbr = kb;
-                        if (RT && p.kstagger > 0) {
-                            const int32_t nk = ti.kb1 - ti.kb0;
-                            kbr = ti.kb0 + int32_t((int64_t(kb - ti.kb0) + (t * p.kstagger) % nk) % nk);
+                        if (RT) {
+                            kbr = kb + krot;
+                            if (kbr >= ti.kb1) kbr -= nk;
                         }
                         const int32_t k0 = kbr * p.bk;      // first reduction element of the stage
                         if (MODE == kModeWgrad) {

@@ -106,3 +106,23 @@ def test_router_full_size_sampled(oracle_lib):
     abs_dot = np.einsum("ik,ik->i", np.abs(X[ts]).astype(np.float64), np.abs(W[rs]).astype(np.float64))
     gpu = Y.cpu().numpy()[ts, rs].astype(np.float64)
     assert np.all(np.abs(gpu - emu) <= oracle.router_tolerance(abs_dot, 3 * K))
+
+
+def test_router_full_size_every_logit_and_bitwise(oracle_lib):
+    """T = 16384, K = 4096, R = 256, every logit: within the emulation's bound of the
+    definition X W^T (summed in FP64), and bitwise equal across repeated calls and an SM
+    cap (a k-block whose split A tile were read before it was written, or overwritten
+    while read, would break both)."""
+    import torch
+    T, K, R = wl.ROUTER_T, wl.ROUTER_K, wl.ROUTER_R
+    Xd, Wd = wl.router_inputs_torch(T, K, R, seed=3)
+    runs = []
+    for cap in (0, 0, 0, 64):
+        runs.append(gg.router_gemm(Xd, Wd, max_sms=cap).cpu().numpy())
+    for r in runs[1:]:
+        assert np.array_equal(runs[0].view(np.int32), r.view(np.int32))
+    X, W = Xd.cpu().numpy().astype(np.float64), Wd.cpu().numpy().astype(np.float64)
+    ref = X @ W.T
+    abs_dot = np.abs(X) @ np.abs(W).T
+    tol = oracle.router_tolerance(abs_dot, 3 * K) + oracle.router_emulation_bound(abs_dot)
+    assert np.all(np.abs(runs[0].astype(np.float64) - ref) <= tol)
