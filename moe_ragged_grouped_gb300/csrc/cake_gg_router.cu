@@ -14,6 +14,7 @@
 //      and the tensor cores sum x_hi w_hi + x_hi w_lo + x_lo w_hi, every product
 //      exact, in one FP32 accumulator.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include <cuda_bf16.h>
@@ -63,10 +64,16 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b)
 
 // One thread: 8 consecutive values of one row of W (two float4 loads), their
 // BF16 high and low parts written as 16-byte vectors at k and K + k of W'.
+// (Launched as a programmatic dependent of the previous kernel in the stream,
+// which may still read W' or write W: every block first waits for it.  Each
+// block lets the router kernel launch at once; that kernel's set-up touches
+// no global memory before it waits for this grid in turn.)
 __global__ void __launch_bounds__(kSplitThreads)
     router_split_w_kernel(const float *__restrict__ W, uint16_t *__restrict__ Ws, int32_t R, int32_t K, int64_t T,
                           int32_t *__restrict__ offsets)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t groups_per_row = K / 8;
     const int64_t total = int64_t(R) * groups_per_row;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -146,8 +153,21 @@ int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const f
     const int64_t cap = int64_t(sms) * 8;   // a few resident blocks per SM, grid-stride beyond
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    router_split_w_kernel<<<unsigned(blocks), kSplitThreads, 0, s>>>(W, wsplit, rp->R, rp->K, rp->T, offsets);
-    if (cudaGetLastError() != cudaSuccess) return CAKE_GG_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks), 1, 1);
+    cfg.blockDim = dim3(kSplitThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    const char *pdl_env = std::getenv("CAKE_GG_PDL");
+    if (!(pdl_env && std::atoi(pdl_env) == 0)) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, router_split_w_kernel, W, wsplit, rp->R, rp->K, rp->T, offsets) != cudaSuccess)
+        return CAKE_GG_ERR_CUDA;
     return cakegg::router_run(&rp->gemm, X, wsplit, Y, offsets, workspace, s);
 }
 
