@@ -266,9 +266,13 @@ int cake_gg_router_plan(cake_gg_router_plan_t *rp, int64_t T, int32_t R, int32_t
  * with zeros once after allocation (as for cake_gg_fwd), unused by anyone else
  * until the stream has run the call.  Enqueues two kernels on `stream` (W's
  * split into W', then the router kernel); allocates nothing, never
- * synchronises.  Host-detected errors return non-zero and enqueue nothing; the
- * router kernel's device-detected errors land in the workspace's status word
- * (cake_gg_check_status). */
+ * synchronises.  Host-detected errors return non-zero and enqueue nothing
+ * (CAKE_GG_ERR_INVALID_ARG also for a plan whose forward plan's tile shape or
+ * ring depth is not the one cake_gg_router_plan gives); the router kernel's
+ * device-detected errors land in the workspace's status word
+ * (cake_gg_check_status).  The split kernel is a programmatic dependent of
+ * the stream's previous kernel (it waits for it before touching memory;
+ * CAKE_GG_PDL=0 launches it plainly). */
 int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const float *W, float *Y,
                         void *workspace, size_t workspace_bytes, void *stream);
 

@@ -724,6 +724,16 @@ int router_plan(cake_gg_plan_t *plan, int64_t T, int32_t R, int32_t K, int32_t m
     return CAKE_GG_OK;
 }
 
+// The tile shape and ring depth are the planner's: the tensor-memory A slots
+// and the shared-memory layout depend on them.
+bool router_plan_matches(const cake_gg_plan_t *plan)
+{
+    cake_gg_plan_t ref;
+    return router_plan(&ref, plan->M_max, plan->N, plan->K, plan->max_sms) == CAKE_GG_OK &&
+           ref.tile_n == plan->tile_n && ref.pair == plan->pair && ref.stages == plan->stages &&
+           ref.tile_k == plan->tile_k && ref.staging_bufs == plan->staging_bufs && ref.tile_m == plan->tile_m;
+}
+
 int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, float *Y, const int32_t *offsets,
                void *ws, cudaStream_t stream)
 {
@@ -732,12 +742,7 @@ int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, f
     if (rc != CAKE_GG_OK) return rc;
     if ((rc = get_encoder()) != CAKE_GG_OK) return rc;
     const int N = plan->N, K = plan->K, bn = plan->tile_n, P = plan->pair;
-    // the tile shape and ring depth are the planner's (the tensor-memory A
-    // slots and the shared-memory layout depend on them)
-    cake_gg_plan_t ref;
-    if (router_plan(&ref, plan->M_max, N, K, plan->max_sms) != CAKE_GG_OK || ref.tile_n != bn || ref.pair != P ||
-        ref.stages != plan->stages || ref.tile_k != plan->tile_k || ref.staging_bufs != plan->staging_bufs)
-        return CAKE_GG_ERR_INVALID_ARG;
+    if (!router_plan_matches(plan)) return CAKE_GG_ERR_INVALID_ARG;
     const uint64_t M = uint64_t(plan->M_max);
     if (M == 0) return CAKE_GG_OK;
     CUtensorMap ma, mb, mo;

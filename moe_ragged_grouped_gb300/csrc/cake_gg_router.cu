@@ -27,6 +27,7 @@ namespace cakegg {
 int router_plan(cake_gg_plan_t *plan, int64_t T, int32_t R, int32_t K, int32_t max_sms);
 int router_run(const cake_gg_plan_t *plan, const float *X, const void *Wsplit, float *Y, const int32_t *offsets,
                void *ws, cudaStream_t stream);
+bool router_plan_matches(const cake_gg_plan_t *plan);
 }  // namespace cakegg
 
 namespace {
@@ -135,7 +136,8 @@ int cake_gg_router_fp32(const cake_gg_router_plan_t *rp, const float *X, const f
     if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(Y) |
          reinterpret_cast<uintptr_t>(workspace)) % 16 != 0)
         return CAKE_GG_ERR_ALIGNMENT;
-    if (rp->gemm.K != rp->K || rp->gemm.N != rp->R || rp->gemm.M_max != rp->T || rp->gemm.E != 1)
+    if (rp->gemm.K != rp->K || rp->gemm.N != rp->R || rp->gemm.M_max != rp->T || rp->gemm.E != 1 ||
+        !cakegg::router_plan_matches(&rp->gemm))
         return CAKE_GG_ERR_INVALID_ARG;
     const RouterLayout L = router_layout(*rp);
     if (workspace_bytes < L.total || rp->workspace_bytes != L.total) return CAKE_GG_ERR_WORKSPACE;

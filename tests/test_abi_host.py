@@ -482,6 +482,14 @@ def test_router_call_rejects_bad_arguments_before_any_cuda_call():
     bad = gg.CakeGGRouterPlan.from_buffer_copy(rp)
     bad.gemm.K = 3 * rp.K                                                       # plan / call mismatch
     assert lib.cake_gg_router_fp32(ctypes.byref(bad), good, good, good, good, nb, None) == gg.CAKE_GG_ERR_INVALID_ARG
+    # a tile shape or ring depth other than the planner's (the kernel's tensor-memory
+    # A slots and shared-memory layout follow them)
+    for field, value in (("stages", rp.gemm.stages - 1), ("tile_n", 128), ("pair", 3 - rp.gemm.pair),
+                         ("tile_k", 128)):
+        bad = gg.CakeGGRouterPlan.from_buffer_copy(rp)
+        setattr(bad.gemm, field, value)
+        assert lib.cake_gg_router_fp32(ctypes.byref(bad), good, good, good, good, nb, None) == \
+            gg.CAKE_GG_ERR_INVALID_ARG, field
 
 
 C_PROGRAM = r"""
