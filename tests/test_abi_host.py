@@ -462,6 +462,20 @@ def test_router_plan_validates_and_sizes_its_workspace():
     assert capped.workspace_bytes == rp.workspace_bytes and capped.gemm.stages == g.stages
 
 
+def test_router_plans_fit_the_kernels_tensor_memory():
+    """The router kernel keeps its accumulator in TMEM columns 0..tile_n-1 and each stage's
+    split A tile (32 columns of BF16 high parts, 32 of low parts) at 256 + 64 * stage, in a
+    512-column allocation: every plan has tile_n <= 256 and 2..4 stages of 64-deep k-blocks,
+    pairs only on tiles whose half is a whole number of 64-row W boxes."""
+    for R in (8, 16, 24, 64, 120, 128, 136, 192, 248, 256, 264, 512, 1024):
+        for K in (8, 64, 1096, 4096):
+            g = gg.cake_gg_router_plan(1000, R, K).gemm
+            assert g.tile_n <= 256 and g.tile_n % 64 == 0 and g.tile_n >= min(R, 256), (R, K)
+            assert 256 + 64 * g.stages <= 512 and g.stages >= 2, (R, K)
+            assert g.tile_k == 64
+            assert g.pair in (1, 2) and (g.pair == 1 or (g.tile_n // 2) % 64 == 0), (R, K)
+
+
 def test_router_plan_struct_layout():
     """The ctypes mirror of cake_gg_router_plan_t: 8-byte aligned fields, the nested forward plan last."""
     assert gg.CakeGGRouterPlan.gemm.offset % 8 == 0
